@@ -1,0 +1,355 @@
+// fa_api.cu -- the C ABI of libfa.so (include/fa.h): argument validation,
+// plane geometry, workspace layouts, the decode split plan, and the device
+// error word. Everything here runs on the host; all arithmetic of the method
+// runs in the kernels of the other translation units.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+// The device error word (one per device that loads the library). Kernels set
+// FA_ERRBIT_* bits with atomicOr; fa_get_device_error reads and clears it.
+__device__ unsigned int g_fa_device_error;
+
+constexpr int kMaxDevices = 64;
+
+cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;  // fa_set_kernel_events
+
+cudaError_t record_start(cudaStream_t s) {
+    return (g_ev_start && g_ev_stop) ? cudaEventRecord(g_ev_start, s) : cudaSuccess;
+}
+cudaError_t record_stop(cudaStream_t s) {
+    return (g_ev_start && g_ev_stop) ? cudaEventRecord(g_ev_stop, s) : cudaSuccess;
+}
+
+struct DeviceInfo {
+    std::once_flag once;
+    unsigned *err = nullptr;
+    int sms = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+DeviceInfo *device_info() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    DeviceInfo *d = &g_dev[dev];
+    std::call_once(d->once, [d, dev]() {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_fa_device_error) == cudaSuccess)
+            d->err = static_cast<unsigned *>(p);
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+            d->sms = sms;
+    });
+    return d;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_hd(int hd) { return hd == 64 || hd == 128 || hd == 256; }
+
+bool supported_group(int hq, int hkv) {
+    if (hkv < 1 || hq < 1 || hq % hkv) return false;
+    const int G = hq / hkv;
+    return G == 1 || G == 2 || G == 4 || G == 8 || G == 16;
+}
+
+fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Heads and shapes shared by prefill and decode.
+fa_status check_heads(int n_q_heads, int n_kv_heads, int head_dim) {
+    if (n_q_heads < 1 || n_kv_heads < 1 || head_dim < 1) return FA_ERR_INVALID;
+    if (n_q_heads % n_kv_heads) return FA_ERR_INVALID;
+    if (head_dim % 32) return FA_ERR_INVALID;
+    if (!supported_hd(head_dim) || !supported_group(n_q_heads, n_kv_heads))
+        return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+fa_status check_shadow(int kv_fmt, int shadow_sink, int shadow_win) {
+    if (kv_fmt == FA_KV_F32) return (shadow_sink == 0 && shadow_win == 0) ? FA_OK : FA_ERR_INVALID;
+    if (kv_fmt != FA_KV_Q4_0) return FA_ERR_INVALID;
+    if (shadow_sink < 0 || shadow_sink > FA_Q4_SINK_MAX) return FA_ERR_INVALID;
+    if (shadow_win < 0 || shadow_win > FA_Q4_RING_ROWS) return FA_ERR_INVALID;
+    return FA_OK;
+}
+
+// fp16 staging for prefill: Q [n][Hq][hd], K and V [Hkv][n][hd].
+struct PrefillWs {
+    size_t q_off, k_off, v_off, bytes;
+};
+PrefillWs prefill_ws(int n, int hq, int hkv, int hd) {
+    PrefillWs w;
+    w.q_off = 0;
+    w.k_off = up256(static_cast<size_t>(n) * hq * hd * 2);
+    const size_t kv = up256(static_cast<size_t>(hkv) * n * hd * 2);
+    w.v_off = w.k_off + kv;
+    w.bytes = w.v_off + kv;
+    return w;
+}
+
+}  // namespace
+
+namespace fa {
+
+bool plane_geom(int fmt, int n_kv, int max_seq, int hd, PlaneGeom *g) {
+    if (n_kv < 1 || max_seq < 1 || hd < 32 || hd % 32) return false;
+    if (fmt != FA_KV_F32 && fmt != FA_KV_Q4_0) return false;
+    g->fmt = fmt;
+    g->n_kv = n_kv;
+    g->max_seq = max_seq;
+    g->hd = hd;
+    g->row_bytes = fmt == FA_KV_F32 ? static_cast<size_t>(hd) * 4
+                                    : static_cast<size_t>(hd / kQ4Block) * kQ4BlockBytes;
+    g->body_off = 0;
+    const size_t body = up256(static_cast<size_t>(n_kv) * max_seq * g->row_bytes);
+    if (fmt == FA_KV_F32) {
+        g->sink_off = 0;
+        g->ring_off = 0;
+        g->bytes = body;
+    } else {
+        g->sink_off = body;
+        g->ring_off = body + up256(static_cast<size_t>(n_kv) * kSinkMax * hd * 2);
+        g->bytes = g->ring_off + up256(static_cast<size_t>(n_kv) * kRingRows * hd * 2);
+    }
+    return true;
+}
+
+int device_sm_count() {
+    DeviceInfo *d = device_info();
+    return (d && d->sms > 0) ? d->sms : 148;
+}
+
+}  // namespace fa
+
+extern "C" {
+
+int fa_version(void) { return 100; }
+
+const char *fa_status_string(fa_status s) {
+    switch (s) {
+        case FA_OK: return "ok";
+        case FA_ERR_INVALID: return "invalid argument";
+        case FA_ERR_UNSUPPORTED: return "unsupported shape or format";
+        case FA_ERR_CUDA: return "CUDA runtime error";
+        case FA_ERR_DEVICE: return "a kernel met invalid device-side data";
+        case FA_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
+        case FA_ERR_WORKSPACE: return "workspace too small";
+    }
+    return "unknown status";
+}
+
+size_t fa_kv_plane_bytes(int kv_fmt, int n_kv_heads, int max_seq, int head_dim) {
+    fa::PlaneGeom g;
+    if (!supported_hd(head_dim) || !fa::plane_geom(kv_fmt, n_kv_heads, max_seq, head_dim, &g))
+        return 0;
+    return g.bytes;
+}
+
+fa_status fa_kv_plane_layout(int kv_fmt, int n_kv_heads, int max_seq, int head_dim,
+                             size_t *row_bytes, size_t *body_offset, size_t *sink_offset,
+                             size_t *ring_offset) {
+    fa::PlaneGeom g;
+    if (!fa::plane_geom(kv_fmt, n_kv_heads, max_seq, head_dim, &g)) return FA_ERR_INVALID;
+    if (!supported_hd(head_dim)) return FA_ERR_UNSUPPORTED;
+    if (row_bytes) *row_bytes = g.row_bytes;
+    if (body_offset) *body_offset = g.body_off;
+    if (sink_offset) *sink_offset = g.sink_off;
+    if (ring_offset) *ring_offset = g.ring_off;
+    return FA_OK;
+}
+
+fa_status fa_kv_append(const float *k_new, const float *v_new, void *k_planes, void *v_planes,
+                       const int32_t *pos0, int nslots, int n, int n_kv_heads, int head_dim,
+                       int max_seq, int kv_fmt, int shadow_sink, int shadow_win,
+                       fa_stream_t stream) {
+    if (nslots < 0 || n < 0) return FA_ERR_INVALID;
+    if (n_kv_heads < 1 || max_seq < 1 || head_dim < 32 || head_dim % 32) return FA_ERR_INVALID;
+    if (!supported_hd(head_dim)) return FA_ERR_UNSUPPORTED;
+    fa_status st = check_shadow(kv_fmt, shadow_sink, shadow_win);
+    if (st != FA_OK) return st;
+    if (n > max_seq) return FA_ERR_INVALID;
+    if (nslots == 0 || n == 0) return FA_OK;
+    if (!k_new || !v_new || !k_planes || !v_planes || !pos0) return FA_ERR_INVALID;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_planes) || !aligned16(v_planes) ||
+        (reinterpret_cast<uintptr_t>(pos0) & 3u))
+        return FA_ERR_INVALID;
+    fa::PlaneGeom g;
+    if (!fa::plane_geom(kv_fmt, n_kv_heads, max_seq, head_dim, &g)) return FA_ERR_INVALID;
+    DeviceInfo *d = device_info();
+    if (!d || !d->err) return FA_ERR_CUDA;
+    return from_cuda(fa::launch_kv_append(k_new, v_new, static_cast<uint8_t *>(k_planes),
+                                          static_cast<uint8_t *>(v_planes), pos0, nslots, n, g,
+                                          shadow_sink, shadow_win, d->err,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t fa_prefill_workspace_bytes(int n, int n_q_heads, int n_kv_heads, int head_dim) {
+    if (n < 0 || n_q_heads < 1 || n_kv_heads < 1 || head_dim < 1) return 0;
+    return prefill_ws(n, n_q_heads, n_kv_heads, head_dim).bytes;
+}
+
+fa_status fa_prefill_tile_shape(int head_dim, int *bq, int *bk) {
+    if (!supported_hd(head_dim)) return FA_ERR_UNSUPPORTED;
+    if (bq) *bq = fa::kPrefillBQ;
+    if (bk) *bk = fa::kPrefillBK;
+    return FA_OK;
+}
+
+fa_status fa_prefill(const float *q, const void *k, const void *v, float *out, int n,
+                     int n_q_heads, int n_kv_heads, int head_dim, int sink, int win, int kv_fmt,
+                     int max_seq, int shadow_sink, int shadow_win, void *workspace,
+                     size_t workspace_bytes, uint8_t *tile_map, fa_stream_t stream) {
+    fa_status st = check_heads(n_q_heads, n_kv_heads, head_dim);
+    if (st != FA_OK) return st;
+    if (n < 0 || sink < 0 || max_seq < 1 || n > max_seq) return FA_ERR_INVALID;
+    st = check_shadow(kv_fmt, shadow_sink, shadow_win);
+    if (st != FA_OK) return st;
+    if (kv_fmt == FA_KV_Q4_0 && shadow_win != 0 && shadow_win != FA_Q4_RING_ROWS)
+        return FA_ERR_UNSUPPORTED;
+    if (n == 0) return FA_OK;
+    if (!q || !k || !v || !out || !workspace) return FA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+        !aligned16(workspace))
+        return FA_ERR_INVALID;
+    const PrefillWs w = prefill_ws(n, n_q_heads, n_kv_heads, head_dim);
+    if (workspace_bytes < w.bytes) return FA_ERR_WORKSPACE;
+    fa::PlaneGeom g;
+    if (!fa::plane_geom(kv_fmt, n_kv_heads, max_seq, head_dim, &g)) return FA_ERR_INVALID;
+    DeviceInfo *d = device_info();
+    if (!d || !d->err) return FA_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    __half *qh = reinterpret_cast<__half *>(ws + w.q_off);
+    __half *kh = reinterpret_cast<__half *>(ws + w.k_off);
+    __half *vh = reinterpret_cast<__half *>(ws + w.v_off);
+    cudaError_t e =
+        fa::launch_stage_q(q, qh, static_cast<size_t>(n) * n_q_heads * head_dim, s);
+    if (e == cudaSuccess)
+        e = fa::launch_stage_kv(static_cast<const uint8_t *>(k), kh, n, g, shadow_sink,
+                                shadow_win, s);
+    if (e == cudaSuccess)
+        e = fa::launch_stage_kv(static_cast<const uint8_t *>(v), vh, n, g, shadow_sink,
+                                shadow_win, s);
+    if (e != cudaSuccess) return FA_ERR_CUDA;
+    fa::PrefillArgs a;
+    a.qh = qh;
+    a.kh = kh;
+    a.vh = vh;
+    a.out = out;
+    a.tile_map = tile_map;
+    a.n = n;
+    a.n_q_heads = n_q_heads;
+    a.n_kv_heads = n_kv_heads;
+    a.head_dim = head_dim;
+    a.sink = sink;
+    a.win = win;
+    a.scale = 1.0f / sqrtf(static_cast<float>(head_dim));
+    e = record_start(s);
+    if (e == cudaSuccess) e = fa::launch_prefill_tc(a, d->err, s);
+    if (e == cudaSuccess) e = record_stop(s);
+    return from_cuda(e);
+}
+
+size_t fa_decode_workspace_bytes(int nslots, int n_q_heads, int head_dim, int max_splits) {
+    if (nslots < 1 || n_q_heads < 1 || head_dim < 1 || max_splits < 1) return 0;
+    return fa::decode_ws_bytes(nslots, n_q_heads, head_dim, max_splits);
+}
+
+fa_status fa_decode(const float *q, const void *k_planes, const void *v_planes,
+                    const int32_t *pos, int nslots, int n_q_heads, int n_kv_heads, int head_dim,
+                    int max_seq, int sink, int win, int kv_fmt, int shadow_sink, int shadow_win,
+                    int split_keys, int max_splits, void *workspace, size_t workspace_bytes,
+                    fa_stream_t stream) {
+    fa_status st = check_heads(n_q_heads, n_kv_heads, head_dim);
+    if (st != FA_OK) return st;
+    if (nslots < 0 || sink < 0 || max_seq < 1 || split_keys < 1 || max_splits < 1)
+        return FA_ERR_INVALID;
+    st = check_shadow(kv_fmt, shadow_sink, shadow_win);
+    if (st != FA_OK) return st;
+    if (nslots == 0) return FA_OK;
+    if (!q || !k_planes || !v_planes || !pos || !workspace) return FA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k_planes) || !aligned16(v_planes) || !aligned16(workspace) ||
+        (reinterpret_cast<uintptr_t>(pos) & 3u))
+        return FA_ERR_INVALID;
+    if (workspace_bytes < fa::decode_ws_bytes(nslots, n_q_heads, head_dim, max_splits))
+        return FA_ERR_WORKSPACE;
+    fa::PlaneGeom g;
+    if (!fa::plane_geom(kv_fmt, n_kv_heads, max_seq, head_dim, &g)) return FA_ERR_INVALID;
+    DeviceInfo *d = device_info();
+    if (!d || !d->err) return FA_ERR_CUDA;
+    fa::DecodeWs ws;
+    fa::decode_ws_carve(workspace, nslots, n_q_heads, head_dim, max_splits, &ws);
+    // Merge runs of plan splits inside one block so that about four blocks per
+    // SM cover every (slot, kv head) pair.
+    const long long pairs = static_cast<long long>(nslots) * n_kv_heads;
+    const long long target = 4LL * fa::device_sm_count();
+    long long cpc = (pairs * max_splits + target - 1) / target;
+    if (cpc < 1) cpc = 1;
+    if (cpc > max_splits) cpc = max_splits;
+    ws.splits_per_cta = static_cast<int>(cpc);
+    ws.entries = static_cast<int>((max_splits + cpc - 1) / cpc);
+    fa::DecodeArgs a;
+    a.q = q;
+    a.k_planes = static_cast<const uint8_t *>(k_planes);
+    a.v_planes = static_cast<const uint8_t *>(v_planes);
+    a.pos = pos;
+    a.nslots = nslots;
+    a.n_q_heads = n_q_heads;
+    a.n_kv_heads = n_kv_heads;
+    a.sink = sink;
+    a.win = win;
+    a.shadow_sink = kv_fmt == FA_KV_Q4_0 ? shadow_sink : 0;
+    a.shadow_win = kv_fmt == FA_KV_Q4_0 ? shadow_win : 0;
+    a.split_keys = split_keys;
+    a.max_splits = max_splits;
+    a.g = g;
+    a.scale = 1.0f / sqrtf(static_cast<float>(head_dim));
+    a.workspace = workspace;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = record_start(s);
+    if (e == cudaSuccess) e = fa::launch_decode(a, ws, d->err, s);
+    if (e == cudaSuccess) e = record_stop(s);
+    return from_cuda(e);
+}
+
+fa_status fa_decode_combine(const void *workspace, float *out, int nslots, int n_q_heads,
+                            int head_dim, int max_splits, fa_stream_t stream) {
+    if (nslots < 0 || n_q_heads < 1 || max_splits < 1) return FA_ERR_INVALID;
+    if (!supported_hd(head_dim)) return head_dim % 32 ? FA_ERR_INVALID : FA_ERR_UNSUPPORTED;
+    if (nslots == 0) return FA_OK;
+    if (!workspace || !out || !aligned16(workspace) || !aligned16(out)) return FA_ERR_INVALID;
+    DeviceInfo *d = device_info();
+    if (!d || !d->err) return FA_ERR_CUDA;
+    return from_cuda(fa::launch_combine(workspace, out, nslots, n_q_heads, head_dim, max_splits,
+                                        d->err, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_set_kernel_events(void *start, void *stop) {
+    g_ev_start = static_cast<cudaEvent_t>(start);
+    g_ev_stop = static_cast<cudaEvent_t>(stop);
+    return FA_OK;
+}
+
+fa_status fa_get_device_error(fa_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return FA_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_fa_device_error, sizeof(v)) != cudaSuccess) return FA_ERR_CUDA;
+    if (v) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(g_fa_device_error, &zero, sizeof(zero)) != cudaSuccess)
+            return FA_ERR_CUDA;
+    }
+    if (v & FA_ERRBIT_TIMEOUT) return FA_ERR_TIMEOUT;
+    if (v & FA_ERRBIT_DEVICE) return FA_ERR_DEVICE;
+    return FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,94 @@
+// fa_internal.h -- declarations shared by the translation units of libfa.so
+// (not part of the public C ABI, which is include/fa.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+// Bits of the device error word.
+#define FA_ERRBIT_DEVICE 1u   // bad device-side data (a position out of range, header mismatch)
+#define FA_ERRBIT_TIMEOUT 2u  // a bounded wait gave up
+
+namespace fa {
+
+constexpr int kQ4Block = 32;       // elements per Q4_0 block
+constexpr int kQ4BlockBytes = 18;  // bytes per Q4_0 block
+constexpr int kSinkMax = 8;        // fp16 sink rows per kv head
+constexpr int kRingRows = 256;     // fp16 ring rows per kv head
+
+// Plane geometry of one slot's K or V cache (see include/fa.h).
+struct PlaneGeom {
+    int fmt;
+    int n_kv;
+    int max_seq;
+    int hd;
+    size_t row_bytes;
+    size_t body_off;
+    size_t sink_off;  // Q4_0 only
+    size_t ring_off;  // Q4_0 only
+    size_t bytes;     // whole plane, multiple of 256
+};
+
+bool plane_geom(int fmt, int n_kv, int max_seq, int hd, PlaneGeom *g);
+
+// ---- kv_append.cu
+cudaError_t launch_kv_append(const float *k_new, const float *v_new, uint8_t *k_planes,
+                             uint8_t *v_planes, const int32_t *pos0, int nslots, int n,
+                             const PlaneGeom &g, int shadow_sink, int shadow_win,
+                             unsigned *err, cudaStream_t stream);
+
+// ---- prefill_stage.cu: fp16 staging of Q and of the K/V rows a prefill reads
+cudaError_t launch_stage_q(const float *q, __half *qh, size_t count, cudaStream_t stream);
+cudaError_t launch_stage_kv(const uint8_t *plane, __half *dst, int n, const PlaneGeom &g,
+                            int shadow_sink, int shadow_win, cudaStream_t stream);
+
+// ---- prefill_tc.cu
+struct PrefillArgs {
+    const __half *qh;   // [n][Hq][hd] fp16
+    const __half *kh;   // [Hkv][n][hd] fp16
+    const __half *vh;   // [Hkv][n][hd] fp16
+    float *out;         // [n][Hq][hd] fp32
+    uint8_t *tile_map;  // optional
+    int n, n_q_heads, n_kv_heads, head_dim, sink, win;
+    float scale;
+};
+constexpr int kPrefillBQ = 128;
+constexpr int kPrefillBK = 128;
+cudaError_t launch_prefill_tc(const PrefillArgs &a, unsigned *err, cudaStream_t stream);
+
+// ---- decode.cu
+struct DecodeArgs {
+    const float *q;
+    const uint8_t *k_planes;
+    const uint8_t *v_planes;
+    const int32_t *pos;
+    int nslots, n_q_heads, n_kv_heads, sink, win, shadow_sink, shadow_win;
+    int split_keys, max_splits;
+    PlaneGeom g;
+    float scale;
+    void *workspace;
+};
+struct DecodeWs {
+    uint32_t *header;
+    float *m, *l, *acc;
+    int stride;          // entry stride per (slot, head) = max_splits
+    int entries;         // partials written per (slot, head), <= stride
+    int splits_per_cta;  // plan splits merged inside one block
+};
+size_t decode_ws_bytes(int nslots, int n_q_heads, int head_dim, int max_splits);
+void decode_ws_carve(void *ws, int nslots, int n_q_heads, int head_dim, int max_splits,
+                     DecodeWs *out);
+cudaError_t launch_decode(const DecodeArgs &a, const DecodeWs &ws, unsigned *err,
+                          cudaStream_t stream);
+cudaError_t launch_combine(const void *workspace, float *out, int nslots, int n_q_heads,
+                           int head_dim, int max_splits, unsigned *err, cudaStream_t stream);
+
+constexpr uint32_t kDecodeMagic = 0x46414443u;  // "FADC"
+
+// ---- fa_api.cu
+int device_sm_count();
+
+}  // namespace fa

@@ -1,0 +1,136 @@
+// prefill_stage.cu -- fp16 staging for the tensor-core prefill.
+//
+// The prefill kernel runs its two contractions on tcgen05 tensor cores with
+// fp16 operands, fed by TMA. These single-pass kernels produce those operands:
+//   * Q: fp32 [n][Hq][hd] -> fp16 [n][Hq][hd], round to nearest even;
+//   * K and V: the cache rows 0..n-1 of every kv head -> fp16 [Hkv][n][hd],
+//     the value each key has for every query of the prefill. For an fp32 cache
+//     that is the fp32 value rounded to fp16. For a Q4_0 cache it is the fp16
+//     sink copy for s < shadow_sink, the fp16 ring copy for the 256 newest
+//     rows when the shadow window is 256 wide ("attention.cu",
+//     fc_kvq4_is_fp16 with the ring liveness floor of fc_attn_flash_prefill_q4,
+//     which for that width depends on s alone), and otherwise the decoded
+//     (c - 8) * d, exact in fp32, rounded once to fp16.
+// Dequantising once here, instead of inside every prefill block that reads a
+// key tile, keeps the Q4_0 ALU work O(n) instead of O(n^2 / 128).
+#include "fa_device.cuh"
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads)
+    stage_q_kernel(const float4 *__restrict__ q, uint2 *__restrict__ qh, long long count4) {
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < count4;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const float4 x = __ldg(q + i);
+        qh[i] = make_uint2(pack_half2(x.x, x.y), pack_half2(x.z, x.w));
+    }
+}
+
+// fp32 cache rows -> fp16, one thread per 4 values.
+__global__ void __launch_bounds__(kThreads)
+    stage_kv_f32_kernel(const uint8_t *__restrict__ plane, uint2 *__restrict__ dst, int n,
+                        int n_kv, int hd, int max_seq, size_t body_off) {
+    const int q4 = hd / 4;
+    const long long total = static_cast<long long>(n_kv) * n * q4;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int e4 = static_cast<int>(i % q4);
+        const long long r = i / q4;
+        const int s = static_cast<int>(r % n);
+        const int g = static_cast<int>(r / n);
+        const float4 x = __ldg(reinterpret_cast<const float4 *>(
+            plane + body_off + ((static_cast<size_t>(g) * max_seq + s) * hd + 4 * e4) * 4));
+        dst[i] = make_uint2(pack_half2(x.x, x.y), pack_half2(x.z, x.w));
+    }
+}
+
+// Q4_0 cache rows -> fp16 value seen by every query of the prefill; one
+// thread per 32-value block (4 x 16-byte stores).
+__global__ void __launch_bounds__(kThreads)
+    stage_kv_q4_kernel(const uint8_t *__restrict__ plane, uint4 *__restrict__ dst, int n,
+                       int n_kv, int hd, int max_seq, size_t body_off, size_t row_bytes,
+                       size_t sink_off, size_t ring_off, int shadow_sink, int shadow_win) {
+    const int nb = hd / kQ4Block;
+    const long long total = static_cast<long long>(n_kv) * n * nb;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int b = static_cast<int>(i % nb);
+        const long long r = i / nb;
+        const int s = static_cast<int>(r % n);
+        const int g = static_cast<int>(r / n);
+        uint4 *out = dst + i * 4;  // 32 fp16 = 4 x uint4
+        const uint4 *f16 = nullptr;
+        if (s < shadow_sink)
+            f16 = reinterpret_cast<const uint4 *>(
+                plane + sink_off + ((static_cast<size_t>(g) * kSinkMax + s) * hd + b * kQ4Block) * 2);
+        else if (shadow_win >= kRingRows && s >= n - kRingRows)
+            f16 = reinterpret_cast<const uint4 *>(
+                plane + ring_off +
+                ((static_cast<size_t>(g) * kRingRows + (s % kRingRows)) * hd + b * kQ4Block) * 2);
+        if (f16) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) out[k] = __ldg(f16 + k);
+            continue;
+        }
+        const uint8_t *blk =
+            plane + body_off + (static_cast<size_t>(g) * max_seq + s) * row_bytes + b * kQ4BlockBytes;
+        const uint16_t *w16 = reinterpret_cast<const uint16_t *>(blk);  // 2-byte aligned
+        const float d = __half2float(__ushort_as_half(__ldg(w16)));
+        uint32_t codes[4];  // the 16 code bytes
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            codes[k] = static_cast<uint32_t>(__ldg(w16 + 1 + 2 * k)) |
+                       (static_cast<uint32_t>(__ldg(w16 + 2 + 2 * k)) << 16);
+        uint32_t h[16];  // 32 fp16 values, element order
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+            const uint32_t bj0 = (codes[j / 4] >> (8 * (j % 4))) & 0xffu;
+            const uint32_t bj1 = (codes[(j + 1) / 4] >> (8 * ((j + 1) % 4))) & 0xffu;
+            // low nibbles: elements j, j+1; high nibbles: elements j+16, j+17
+            h[j / 2] = pack_half2(static_cast<float>(static_cast<int>(bj0 & 15u) - 8) * d,
+                                  static_cast<float>(static_cast<int>(bj1 & 15u) - 8) * d);
+            h[8 + j / 2] = pack_half2(static_cast<float>(static_cast<int>(bj0 >> 4) - 8) * d,
+                                      static_cast<float>(static_cast<int>(bj1 >> 4) - 8) * d);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) out[k] = make_uint4(h[4 * k], h[4 * k + 1], h[4 * k + 2], h[4 * k + 3]);
+    }
+}
+
+int grid_for(long long items) {
+    long long blocks = (items + kThreads - 1) / kThreads;
+    const long long cap = static_cast<long long>(device_sm_count()) * 16;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return static_cast<int>(blocks);
+}
+
+}  // namespace
+
+cudaError_t launch_stage_q(const float *q, __half *qh, size_t count, cudaStream_t stream) {
+    const long long c4 = static_cast<long long>(count / 4);
+    stage_q_kernel<<<grid_for(c4), kThreads, 0, stream>>>(reinterpret_cast<const float4 *>(q),
+                                                           reinterpret_cast<uint2 *>(qh), c4);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stage_kv(const uint8_t *plane, __half *dst, int n, const PlaneGeom &g,
+                            int shadow_sink, int shadow_win, cudaStream_t stream) {
+    if (g.fmt == 0) {
+        const long long items = static_cast<long long>(g.n_kv) * n * (g.hd / 4);
+        stage_kv_f32_kernel<<<grid_for(items), kThreads, 0, stream>>>(
+            plane, reinterpret_cast<uint2 *>(dst), n, g.n_kv, g.hd, g.max_seq, g.body_off);
+    } else {
+        const long long items = static_cast<long long>(g.n_kv) * n * (g.hd / kQ4Block);
+        stage_kv_q4_kernel<<<grid_for(items), kThreads, 0, stream>>>(
+            plane, reinterpret_cast<uint4 *>(dst), n, g.n_kv, g.hd, g.max_seq, g.body_off,
+            g.row_bytes, g.sink_off, g.ring_off, shadow_sink, shadow_win);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace fa

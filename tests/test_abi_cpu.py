@@ -1,0 +1,125 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point include/fa.h declares, reports the documented plane and
+workspace sizes, and rejects bad arguments before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def fa():
+    from causal_gqa_flash_attn_gb300 import build
+    build.build()
+    import causal_gqa_flash_attn_gb300 as fa
+    fa.lib()
+    return fa
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(fa):
+    names = header_functions()
+    assert len(names) >= 12
+    for name in names:
+        assert hasattr(fa.lib(), name), name
+    assert set(names) == set(fa.SIGNATURES)
+
+
+def test_version_and_status_strings(fa):
+    assert fa.version() >= 100
+    for s in range(7):
+        assert fa.status_string(s)
+    assert "unknown" in fa.status_string(99)
+
+
+def test_plane_sizes(fa):
+    # Q4_0 row = hd/32 blocks of 18 bytes ("attention.cu", fc_kvq4_row_bytes)
+    for hd, rb in ((64, 36), (128, 72), (256, 144)):
+        row, body, sink, ring = fa.kv_plane_layout(fa.KV_Q4_0, 2, 1000, hd)
+        assert row == rb and body == 0
+        assert sink == ((2 * 1000 * rb + 255) // 256) * 256
+        assert ring == sink + ((2 * 8 * hd * 2 + 255) // 256) * 256
+        pb = fa.kv_plane_bytes(fa.KV_Q4_0, 2, 1000, hd)
+        assert pb == ring + ((2 * 256 * hd * 2 + 255) // 256) * 256
+        assert pb % 256 == 0
+        row, body, sink, ring = fa.kv_plane_layout(fa.KV_F32, 2, 1000, hd)
+        assert row == 4 * hd and sink == 0 and ring == 0
+        assert fa.kv_plane_bytes(fa.KV_F32, 2, 1000, hd) == ((2 * 1000 * 4 * hd + 255) // 256) * 256
+    assert fa.kv_plane_bytes(fa.KV_F32, 2, 1000, 96) == 0
+    assert fa.kv_plane_bytes(7, 2, 1000, 64) == 0
+    assert fa.kv_plane_bytes(fa.KV_F32, 0, 1000, 64) == 0
+
+
+def test_workspace_sizes(fa):
+    n, hq, hkv, hd = 8192, 16, 2, 256
+    assert fa.prefill_workspace_bytes(n, hq, hkv, hd) >= 2 * (n * hq * hd + 2 * hkv * n * hd)
+    d = fa.decode_workspace_bytes(32, 16, 256, 128)
+    assert d >= 256 + 32 * 16 * 128 * (2 + 256) * 4
+    assert fa.decode_workspace_bytes(0, 16, 256, 128) == 0
+    assert fa.prefill_tile_shape(256) == (128, 128)
+    with pytest.raises(fa.FAError):
+        fa.prefill_tile_shape(96)
+
+
+def _prefill_status(fa, **kw):
+    args = dict(q=16, k=16, v=16, out=16, n=16, hq=8, hkv=2, hd=64, sink=0, win=0, fmt=0,
+                max_seq=16, ss=0, sw=0, ws=16, wsb=1 << 30, tile_map=None)
+    args.update(kw)
+    L = fa.lib()
+    return L.fa_prefill(args["q"], args["k"], args["v"], args["out"], args["n"], args["hq"],
+                        args["hkv"], args["hd"], args["sink"], args["win"], args["fmt"],
+                        args["max_seq"], args["ss"], args["sw"], args["ws"], args["wsb"],
+                        args["tile_map"], None)
+
+
+def test_prefill_validation(fa):
+    assert _prefill_status(fa, hd=96) == fa.ERR_UNSUPPORTED
+    assert _prefill_status(fa, hd=100) == fa.ERR_INVALID
+    assert _prefill_status(fa, hq=6, hkv=4) == fa.ERR_INVALID
+    assert _prefill_status(fa, hq=12, hkv=1) == fa.ERR_UNSUPPORTED   # group 12
+    assert _prefill_status(fa, q=None) == fa.ERR_INVALID
+    assert _prefill_status(fa, out=24) == fa.ERR_INVALID           # misaligned
+    assert _prefill_status(fa, n=17, max_seq=16) == fa.ERR_INVALID
+    assert _prefill_status(fa, sink=-1) == fa.ERR_INVALID
+    assert _prefill_status(fa, fmt=3) == fa.ERR_INVALID
+    assert _prefill_status(fa, fmt=0, ss=4) == fa.ERR_INVALID       # shadows only for Q4_0
+    assert _prefill_status(fa, fmt=1, ss=9) == fa.ERR_INVALID
+    assert _prefill_status(fa, fmt=1, sw=257) == fa.ERR_INVALID
+    assert _prefill_status(fa, fmt=1, sw=100) == fa.ERR_UNSUPPORTED
+    assert _prefill_status(fa, wsb=10) == fa.ERR_WORKSPACE
+    assert _prefill_status(fa, n=0) == fa.OK                       # empty input: nothing to do
+
+
+def test_decode_and_append_validation(fa):
+    L = fa.lib()
+    # fa_decode(q, k, v, pos, nslots, hq, hkv, hd, max_seq, sink, win, fmt, ss, sw, kps, cap, ws, wsb, stream)
+    base = [16, 16, 16, 16, 2, 16, 2, 256, 100, 0, 0, 1, 4, 0, 256, 4, 16, 1 << 30, None]
+
+    def dec(**kw):
+        a = list(base)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return L.fa_decode(*a)
+    assert dec(a14=0) == fa.ERR_INVALID        # split_keys
+    assert dec(a15=0) == fa.ERR_INVALID        # max_splits
+    assert dec(a3=None) == fa.ERR_INVALID      # pos
+    assert dec(a3=18) == fa.ERR_INVALID        # pos misaligned
+    assert dec(a17=100) == fa.ERR_WORKSPACE
+    assert dec(a7=48) == fa.ERR_INVALID
+    assert dec(a4=0) == fa.OK                  # no slots
+    assert L.fa_decode_combine(16, 16, 2, 16, 256, 0, None) == fa.ERR_INVALID
+    assert L.fa_decode_combine(16, 16, 2, 16, 96, 4, None) == fa.ERR_UNSUPPORTED
+    # fa_kv_append(k, v, kp, vp, pos0, nslots, n, hkv, hd, max_seq, fmt, ss, sw, stream)
+    assert L.fa_kv_append(16, 16, 16, 16, 16, 1, 8, 2, 64, 4, 1, 0, 0, None) == fa.ERR_INVALID
+    assert L.fa_kv_append(16, 16, 16, 16, 16, 1, 8, 2, 64, 16, 0, 1, 0, None) == fa.ERR_INVALID
+    assert L.fa_kv_append(16, 16, 16, 16, 16, 1, 8, 2, 96, 16, 1, 0, 0, None) == fa.ERR_UNSUPPORTED
+    assert L.fa_kv_append(None, 16, 16, 16, 16, 1, 8, 2, 64, 16, 1, 0, 0, None) == fa.ERR_INVALID
+    assert L.fa_kv_append(16, 16, 16, 16, 16, 0, 8, 2, 64, 16, 1, 0, 0, None) == fa.OK
