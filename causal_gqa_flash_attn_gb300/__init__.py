@@ -39,6 +39,8 @@ SIGNATURES = {
     "fa_decode": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _SZ,
                        _P]),
     "fa_decode_combine": (_I, [_P, _P, _I, _I, _I, _I, _P]),
+    "fa_decode_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                               _P, _P]),
     "fa_set_kernel_events": (_I, [_P, _P]),
     "fa_get_device_error": (_I, [_P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
@@ -185,6 +187,22 @@ def decode_combine(workspace, out, *, nslots: int, n_q_heads: int, head_dim: int
     _check(lib().fa_decode_combine(
         _dev(workspace, torch.uint8, "workspace"), _dev(out, torch.float32, "out"), nslots,
         n_q_heads, head_dim, max_splits, _stream(stream)), "fa_decode_combine")
+
+
+def decode_noalloc(q, k_planes, v_planes, pos, out, *, n_q_heads: int, n_kv_heads: int,
+                   head_dim: int, max_seq: int, sink: int, win: int, kv_fmt: int,
+                   shadow_sink: int = 0, shadow_win: int = 0, split_keys: int = 256,
+                   max_splits: int, stream=None):
+    """fa_decode_noalloc: decode + combine into out [nslots][Hq][hd] with the
+    partials in the library's fixed device array; for callers that cannot
+    allocate device memory. Calls that overlap on the GPU race on that array."""
+    nslots = q.shape[0]
+    _check(lib().fa_decode_noalloc(
+        _dev(q, torch.float32, "q"), _dev(k_planes, torch.uint8, "k_planes"),
+        _dev(v_planes, torch.uint8, "v_planes"), _dev(pos, torch.int32, "pos"), nslots,
+        n_q_heads, n_kv_heads, head_dim, max_seq, sink, win, kv_fmt, shadow_sink, shadow_win,
+        split_keys, max_splits, _dev(out, torch.float32, "out"), _stream(stream)),
+        "fa_decode_noalloc")
 
 
 def set_kernel_events(start, stop):

@@ -126,6 +126,11 @@ int device_sm_count() {
     return (d && d->sms > 0) ? d->sms : 148;
 }
 
+unsigned *device_error_word() {
+    DeviceInfo *d = device_info();
+    return d ? d->err : nullptr;
+}
+
 }  // namespace fa
 
 extern "C" {

@@ -90,5 +90,6 @@ constexpr uint32_t kDecodeMagic = 0x46414443u;  // "FADC"
 
 // ---- fa_api.cu
 int device_sm_count();
+unsigned *device_error_word();  // this device's error word (device address)
 
 }  // namespace fa

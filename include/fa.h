@@ -213,6 +213,32 @@ fa_status fa_decode(const float *q, const void *k_planes, const void *v_planes,
 fa_status fa_decode_combine(const void *workspace, float *out, int nslots, int n_q_heads,
                             int head_dim, int max_splits, fa_stream_t stream);
 
+/* Decode without any caller-provided device memory. The pages have no
+ * counterpart to this call; it exists for callers that cannot allocate
+ * device memory at all (a plugin inside a host whose allocator owns the
+ * GPU's memory, or a serving loop where cudaMalloc/cudaFree are banned because
+ * they can synchronise the device). It computes exactly what fa_decode
+ * followed by fa_decode_combine computes, writing out [nslots][n_q_heads]
+ * [head_dim] fp32 (device), with the same arguments and rules as fa_decode.
+ *
+ * The partials live in a fixed 8 MiB array in the library's device memory
+ * (held by every GPU that loads the library until the process exits), laid
+ * out as fa_decode's workspace with the entry stride equal to the number of
+ * entries E. A problem whose partials need more than 8 MiB
+ * (256 + 2*nslots*n_q_heads*E*4 + nslots*n_q_heads*E*head_dim*4 bytes, parts
+ * rounded up to 256) returns FA_ERR_WORKSPACE before any launch. The call
+ * allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ * Every call shares the array and it keeps the last call's contents; calls
+ * that overlap on the GPU (other streams, other host threads on the device)
+ * race on it, so serialise them. The first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture. */
+fa_status fa_decode_noalloc(const float *q, const void *k_planes, const void *v_planes,
+                            const int32_t *pos, int nslots, int n_q_heads, int n_kv_heads,
+                            int head_dim, int max_seq, int sink, int win, int kv_fmt,
+                            int shadow_sink, int shadow_win, int split_keys, int max_splits,
+                            float *out, fa_stream_t stream);
+
 /* ---------------------------------------------------------------- profiling */
 
 /* Optional timing hook. While both events are non-NULL (cudaEvent_t handles
