@@ -3,20 +3,29 @@
 // "Multi-user decode attention": fc_attn_dec_plan, fc_attn_flash_decode_slots,
 // fc_attn_flash_decode_combine).
 //
-// Decode reads every cached key once per (slot, kv head) and does 2 x 8 x hd
-// multiply-adds per key and q head; at 288 bytes per key (K+V, Q4_0, hd 256)
-// that is about 28 flop/byte, more than the CUDA cores can sustain at HBM
-// speed, so both contractions run on the warp-level tensor-core path:
-//   S^T (16 keys x 8 heads) = K (16 x hd) . Q^T   mma.m16n8k16, f16 -> f32
-//   O^T (hd x 8 heads)     += V^T (hd x 16) . P^T  same instruction
-// The 8 query heads sharing a kv head are exactly the n8 dimension, so each
-// K/V row is read once for the whole group. P^T is formed in registers with
-// movmatrix. tcgen05 is not used here: its smallest M is 64 and the work is
-// bound by memory and dequantisation, not by MMA rate.
+// Decode reads every cached key once per (slot, kv head) and does 2 x G x hd
+// multiply-adds per key; at 288 bytes per key (K+V, Q4_0, hd 256) and G = 8
+// that is about 28 flop/byte, more than the CUDA cores sustain at HBM speed,
+// so both contractions run on the warp-level tensor-core path
+// (mma.sync.m16n8k16, fp16 in, fp32 accumulate):
+//   S^T (16 keys x 8 heads) = K (16 x hd) . Q^T
+//   O^T (hd x 8 heads)     += V^T (hd x 16 keys) . P^T
+// The 8 query heads sharing a kv head are the n8 dimension, so each K/V row is
+// read once for the group; P^T is formed in registers with movmatrix. tcgen05
+// is not used here: its smallest M is 64 and this work is bound by memory and
+// by the dequantisation, not by the MMA rate.
 //
-// Block = 4 warps on one (slot, kv head, entry). The entry covers a run of
-// consecutive splits of the slot's plan; warps take 16-key chunks in turn,
-// each with its own online softmax, and merge at the end into one partial.
+// Two kernels write the same partials (m, l, acc per slot, q head, entry):
+//  * decode_q4_kernel (Q4_0 cache, group <= 8): per warp a 3-stage ring of raw
+//    Q4_0 K/V tiles (32 keys) filled by one bulk copy each; nibbles become fp16
+//    MMA operands in registers. For K the operand is 1024 + c (one LOP3) and the
+//    -1032 * sum(q) bias of each 32-element block is preloaded into a fresh
+//    accumulator, then scaled by the block's d; for V the operand is c - 8
+//    and d is folded into P. Keys held as fp16 shadows (sinks, recent ring)
+//    are left to one extra entry per (slot, kv head), run by the generic path.
+//  * decode_kernel (fp32 caches, group 16, and that shadow entry): stages
+//    16-key fp16 tiles in shared memory, reads fragments with ldmatrix.
+// Each block merges its warps; fa_decode_combine merges the entries.
 #include "fa_device.cuh"
 #include "fa_internal.h"
 
@@ -24,7 +33,15 @@ namespace fa {
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kChunk = 16;  // keys per warp step
+constexpr int kChunk = 16;     // keys per step of the generic path
+constexpr int kTileKeys = 32;  // keys per stage of the Q4_0 path
+constexpr int kStages = 3;     // stages per warp of the Q4_0 path
+// Lazy rescale threshold (log2 units) of the running max: O and l keep a
+// stale reference until the max grows past it. In the Q4_0 path P is
+// multiplied by the block scale d in fp16, so P <= 2^2 keeps P*d finite for
+// any |d| < 8192 (inputs within the fp16 range).
+constexpr float kRescaleGeneric = 8.0f;
+constexpr float kRescaleQ4 = 2.0f;
 
 struct DecodeParams {
     const float *q;
@@ -34,7 +51,10 @@ struct DecodeParams {
     float *ws_m, *ws_l, *ws_acc;
     uint32_t *ws_header;
     int nslots, Hq, Hkv, max_seq, sink, win, fmt, shadow_sink, shadow_win;
-    int split_keys, max_splits, cpc, entries, stride;
+    int split_keys, max_splits, cpc;
+    int entries;       // entries written per (slot, head)
+    int stride;        // entry stride of the workspace
+    int shadow_entry;  // entry index of the fp16-shadow keys, or -1
     size_t plane_bytes, body_off, row_bytes, sink_off, ring_off;
     float sl2;  // scale * log2(e)
     unsigned *err;
@@ -48,6 +68,133 @@ __device__ __forceinline__ int dec_plan(int seq_len, int kps, int cap, int *spli
     *split_len = sl;
     return (seq_len + sl - 1) / sl;
 }
+
+// Is key s read from an fp16 shadow copy by the decode query at p?
+__device__ __forceinline__ bool is_shadow_key(const DecodeParams &P, int p, int s) {
+    return P.fmt != 0 && (s < P.shadow_sink || (P.shadow_win > 0 && s > p - P.shadow_win));
+}
+
+__device__ __forceinline__ void write_empty(const DecodeParams &P, size_t head0, int G, int e) {
+    for (int hh = threadIdx.x; hh < G; hh += blockDim.x) {
+        P.ws_m[(head0 + hh) * P.stride + e] = -INFINITY;
+        P.ws_l[(head0 + hh) * P.stride + e] = 0.0f;
+    }
+}
+
+// Merge the kWarps per-warp online-softmax states of a block and write the
+// block's partial. Per thread: m_used/m_true/lsum of heads nt*8 + 2t + {0,1}
+// (exp2 domain, lsum already summed over the warp), o[mt][nt][k] of rows
+// 16mt + r (+8 for k >= 2), heads nt*8 + 2t + (k & 1).
+template <int HD, int NT>
+__device__ __forceinline__ void merge_and_write(const DecodeParams &P, uint8_t *dsmem,
+                                                size_t head0, int G, int e,
+                                                const float (&m_used)[NT][2],
+                                                const float (&m_true)[NT][2],
+                                                const float (&lsum)[NT][2],
+                                                const float (&o)[HD / 16][NT][4]) {
+    constexpr int MT = HD / 16;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = lane >> 2, t = lane & 3;
+    __syncthreads();
+    float *sm_mu = reinterpret_cast<float *>(dsmem);  // [kWarps][16]
+    float *sm_mt = sm_mu + kWarps * 16;
+    float *sm_l = sm_mt + kWarps * 16;
+    float *sm_f = sm_l + kWarps * 16;
+    float *sm_o = sm_f + kWarps * 16;  // [kWarps][16][HD]
+    if (r == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int head = nt * 8 + 2 * t + hh;
+                sm_mu[warp * 16 + head] = m_used[nt][hh];
+                sm_mt[warp * 16 + head] = m_true[nt][hh];
+                sm_l[warp * 16 + head] = lsum[nt][hh];
+            }
+    }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int head = nt * 8 + 2 * t + (k & 1);
+                const int dim = 16 * mt + r + ((k >> 1) << 3);
+                sm_o[(warp * 16 + head) * HD + dim] = o[mt][nt][k];
+            }
+    __syncthreads();
+    if (threadIdx.x < G) {
+        const int head = threadIdx.x;
+        float M = -INFINITY;
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_mt[w * 16 + head]);
+        float L = 0.0f;
+        for (int w = 0; w < kWarps; ++w) {
+            const float mu = sm_mu[w * 16 + head];
+            const float f = (mu == -INFINITY || M == -INFINITY) ? 0.0f : ex2(mu - M);
+            sm_f[w * 16 + head] = f;
+            L += f * sm_l[w * 16 + head];
+        }
+        // natural-log reference: s * scale = (s * scale * log2 e) * ln 2
+        P.ws_m[(head0 + head) * P.stride + e] =
+            (M == -INFINITY) ? -INFINITY : M * 0.69314718055994531f;
+        P.ws_l[(head0 + head) * P.stride + e] = L;
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < G * HD; idx += blockDim.x) {
+        const int head = idx / HD, dim = idx % HD;
+        if (sm_mt[head] == -INFINITY && sm_mt[16 + head] == -INFINITY &&
+            sm_mt[32 + head] == -INFINITY && sm_mt[48 + head] == -INFINITY)
+            continue;  // empty for this head: acc is never read
+        float a = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) a += sm_f[w * 16 + head] * sm_o[(w * 16 + head) * HD + dim];
+        P.ws_acc[((head0 + head) * P.stride + e) * HD + dim] = a;
+    }
+}
+
+// Online-softmax fold of one group of scores of two heads (exp2 domain).
+// sv: this thread's scores (-inf when masked), n of them per head.
+template <int MT, int NT, int N>
+__device__ __forceinline__ void fold_scores(float (&sv)[2][N], float sl2, float thr,
+                                            float &mu0, float &mu1, float &mt0, float &mt1,
+                                            float &ls0, float &ls1, float (&o)[MT][NT][4],
+                                            int nt, float (&pv)[2][N]) {
+    float *mu[2] = {&mu0, &mu1};
+    float *mtr[2] = {&mt0, &mt1};
+    float *ls[2] = {&ls0, &ls1};
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        float mx = sv[hh][0];
+#pragma unroll
+        for (int k = 1; k < N; ++k) mx = fmaxf(mx, sv[hh][k]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mx2 = mx * sl2;
+        *mtr[hh] = fmaxf(*mtr[hh], mx2);
+        const float m_new = fmaxf(*mu[hh], mx2);
+        if (m_new > *mu[hh] + thr) {
+            const float corr = ex2(*mu[hh] - m_new);  // 0 while nothing was seen
+            *ls[hh] *= corr;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                o[mt][nt][hh] *= corr;
+                o[mt][nt][2 + hh] *= corr;
+            }
+            *mu[hh] = m_new;
+        }
+        const float mref = (*mu[hh] == -INFINITY) ? 0.0f : *mu[hh];
+        float s = 0.0f;
+#pragma unroll
+        for (int k = 0; k < N; ++k) {
+            pv[hh][k] = ex2(fmaf(sv[hh][k], sl2, -mref));
+            s += pv[hh][k];
+        }
+        *ls[hh] += s;
+    }
+}
+
+// ============================================================ generic path
 
 // Stage the fp16 values of keys [c0, c0+16) (clamped to kmax) of one K or V
 // plane into a [16][HD+8] fp16 tile; the read rule picks the fp16 sink, the
@@ -98,45 +245,19 @@ __device__ __forceinline__ void stage_rows(const DecodeParams &P, const uint8_t 
     }
 }
 
+// Generic body: 16-key chunks of the given key ranges, round-robin over the
+// warps. With shadow_only, keys that are not fp16 shadows are masked (they
+// belong to the Q4_0 path).
 template <int HD, int NT>
-__global__ void __launch_bounds__(kWarps * 32) decode_kernel(const DecodeParams P) {
+__device__ __forceinline__ void generic_body(const DecodeParams &P, uint8_t *dsmem, int e, int g,
+                                             int u, int p, int lo0, int hi0, int lo1, int hi1,
+                                             bool shadow_only) {
     constexpr int STRIDE = HD + 8;
     constexpr int MT = HD / 16;
-    extern __shared__ __align__(16) uint8_t dsmem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = lane >> 2, t = lane & 3;
-    const int e = blockIdx.x, g = blockIdx.y, u = blockIdx.z;
     const int G = P.Hq / P.Hkv;
-
-    if (e == 0 && g == 0 && u == 0 && threadIdx.x == 0) {
-        P.ws_header[0] = kDecodeMagic;
-        P.ws_header[1] = static_cast<uint32_t>(P.nslots);
-        P.ws_header[2] = static_cast<uint32_t>(P.Hq);
-        P.ws_header[3] = static_cast<uint32_t>(HD);
-        P.ws_header[4] = static_cast<uint32_t>(P.entries);
-    }
-
-    const int p = P.pos[u];
-    int k_lo = 0, k_hi = 0;
-    if (p < 0 || p >= P.max_seq) {
-        if (threadIdx.x == 0 && e == 0 && g == 0) flag_error(P.err, FA_ERRBIT_DEVICE);
-    } else {
-        int split_len;
-        const int ns = dec_plan(p + 1, P.split_keys, P.max_splits, &split_len);
-        const int s_lo = e * P.cpc, s_hi = min(ns, s_lo + P.cpc);
-        if (s_lo < s_hi) {
-            k_lo = s_lo * split_len;
-            k_hi = min(p + 1, s_hi * split_len);
-        }
-    }
     const size_t head0 = static_cast<size_t>(u) * P.Hq + static_cast<size_t>(g) * G;
-    if (k_lo >= k_hi) {  // empty entry
-        for (int hh = threadIdx.x; hh < G; hh += blockDim.x) {
-            P.ws_m[(head0 + hh) * P.stride + e] = -INFINITY;
-            P.ws_l[(head0 + hh) * P.stride + e] = 0.0f;
-        }
-        return;
-    }
 
     __half *tk = reinterpret_cast<__half *>(dsmem) + warp * 2 * kChunk * STRIDE;
     __half *tv = tk + kChunk * STRIDE;
@@ -182,7 +303,12 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(const DecodeParams 
         }
 
     const uint32_t tk_s = smem_u32(tk), tv_s = smem_u32(tv);
-    for (int c0 = k_lo + kChunk * warp; c0 < k_hi; c0 += kChunk * kWarps) {
+    const int n0 = max(0, hi0 - lo0 + kChunk - 1) / kChunk;
+    const int n1 = max(0, hi1 - lo1 + kChunk - 1) / kChunk;
+    for (int ci = warp; ci < n0 + n1; ci += kWarps) {
+        const bool first = ci < n0;
+        const int c0 = first ? lo0 + kChunk * ci : lo1 + kChunk * (ci - n0);
+        const int k_hi = first ? hi0 : hi1;
         if (P.win > 0 && !(c0 < P.sink || c0 + kChunk - 1 >= p - P.win + 1)) continue;
         stage_rows<HD>(P, kplane, g, p, c0, k_hi - 1, tk, lane);
         stage_rows<HD>(P, vplane, g, p, c0, k_hi - 1, tv, lane);
@@ -204,41 +330,27 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(const DecodeParams 
             }
         }
         const int keyA = c0 + r, keyB = c0 + r + 8;
-        const bool visA = keyA < k_hi && key_visible(p, keyA, P.sink, P.win);
-        const bool visB = keyB < k_hi && key_visible(p, keyB, P.sink, P.win);
+        bool visA = keyA < k_hi && key_visible(p, keyA, P.sink, P.win);
+        bool visB = keyB < k_hi && key_visible(p, keyB, P.sink, P.win);
+        if (shadow_only) {
+            visA = visA && is_shadow_key(P, p, keyA);
+            visB = visB && is_shadow_key(P, p, keyB);
+        }
         uint32_t pb[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            float pa[2], pbv[2];
+            float sv[2][2], pv[2][2];
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                const float sA = visA ? sacc[nt][hh] : -INFINITY;
-                const float sB = visB ? sacc[nt][2 + hh] : -INFINITY;
-                float mx = fmaxf(sA, sB);
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                const float mx2 = mx * P.sl2;
-                m_true[nt][hh] = fmaxf(m_true[nt][hh], mx2);
-                const float m_new = fmaxf(m_used[nt][hh], mx2);
-                if (m_new > m_used[nt][hh] + 8.0f) {
-                    const float corr = ex2(m_used[nt][hh] - m_new);
-                    lsum[nt][hh] *= corr;
-#pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) {
-                        o[mt][nt][hh] *= corr;
-                        o[mt][nt][2 + hh] *= corr;
-                    }
-                    m_used[nt][hh] = m_new;
-                }
-                const float mref = (m_used[nt][hh] == -INFINITY) ? 0.0f : m_used[nt][hh];
-                pa[hh] = ex2(fmaf(sA, P.sl2, -mref));
-                pbv[hh] = ex2(fmaf(sB, P.sl2, -mref));
-                lsum[nt][hh] += pa[hh] + pbv[hh];
+                sv[hh][0] = visA ? sacc[nt][hh] : -INFINITY;
+                sv[hh][1] = visB ? sacc[nt][2 + hh] : -INFINITY;
             }
+            fold_scores<MT, NT, 2>(sv, P.sl2, kRescaleGeneric, m_used[nt][0], m_used[nt][1],
+                                   m_true[nt][0], m_true[nt][1], lsum[nt][0], lsum[nt][1], o, nt,
+                                   pv);
             // rows = keys, cols = heads 2t, 2t+1  ->  transpose to B fragments
-            pb[nt][0] = movmatrix_trans(pack_half2(pa[0], pa[1]));
-            pb[nt][1] = movmatrix_trans(pack_half2(pbv[0], pbv[1]));
+            pb[nt][0] = movmatrix_trans(pack_half2(pv[0][0], pv[1][0]));
+            pb[nt][1] = movmatrix_trans(pack_half2(pv[0][1], pv[1][1]));
         }
         {
             // V^T A fragments: matrix q of ldmatrix.x4.trans reads keys
@@ -256,7 +368,6 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(const DecodeParams 
         __syncwarp();
     }
 
-    // per-head sums over the 8 lanes that share t
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -267,59 +378,364 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(const DecodeParams 
             v += __shfl_xor_sync(0xffffffffu, v, 16);
             lsum[nt][hh] = v;
         }
+    merge_and_write<HD, NT>(P, dsmem, head0, G, e, m_used, m_true, lsum, o);
+}
 
-    // ---- merge the 4 warps: per warp m_used, m_true, l [16] and O [16][HD]
-    __syncthreads();
-    float *sm_mu = reinterpret_cast<float *>(dsmem);      // [kWarps][16]
-    float *sm_mt = sm_mu + kWarps * 16;                   // [kWarps][16]
-    float *sm_l = sm_mt + kWarps * 16;                    // [kWarps][16]
-    float *sm_f = sm_l + kWarps * 16;                     // [kWarps][16] weights
-    float *sm_o = sm_f + kWarps * 16;                     // [kWarps][16][HD]
-    if (r == 0) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int head = nt * 8 + 2 * t + hh;
-                sm_mu[warp * 16 + head] = m_used[nt][hh];
-                sm_mt[warp * 16 + head] = m_true[nt][hh];
-                sm_l[warp * 16 + head] = lsum[nt][hh];
-            }
+__device__ __forceinline__ void write_header(const DecodeParams &P, int hd) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0) {
+        P.ws_header[0] = kDecodeMagic;
+        P.ws_header[1] = static_cast<uint32_t>(P.nslots);
+        P.ws_header[2] = static_cast<uint32_t>(P.Hq);
+        P.ws_header[3] = static_cast<uint32_t>(hd);
+        P.ws_header[4] = static_cast<uint32_t>(P.entries);
     }
+}
+
+// Key range of body entry e of slot u: the run of plan splits [e*cpc, ...).
+__device__ __forceinline__ bool entry_range(const DecodeParams &P, int e, int p, int *k_lo,
+                                            int *k_hi) {
+    int split_len;
+    const int ns = dec_plan(p + 1, P.split_keys, P.max_splits, &split_len);
+    const int s_lo = e * P.cpc, s_hi = min(ns, s_lo + P.cpc);
+    if (s_lo >= s_hi) return false;
+    *k_lo = s_lo * split_len;
+    *k_hi = min(p + 1, s_hi * split_len);
+    return *k_lo < *k_hi;
+}
+
+// Shadow entry: the fp16 sink rows and the fp16 ring rows the query reads.
+template <int HD, int NT>
+__device__ __forceinline__ void shadow_entry(const DecodeParams &P, uint8_t *dsmem, int e, int g,
+                                             int u, int p) {
+    const int G = P.Hq / P.Hkv;
+    const size_t head0 = static_cast<size_t>(u) * P.Hq + static_cast<size_t>(g) * G;
+    const int lo0 = 0, hi0 = min(P.shadow_sink, p + 1);
+    int lo1 = 0, hi1 = 0;
+    if (P.shadow_win > 0) {
+        lo1 = max(hi0, p - P.shadow_win + 1);
+        hi1 = p + 1;
+    }
+    if (hi0 <= lo0 && hi1 <= lo1) {
+        write_empty(P, head0, G, e);
+        return;
+    }
+    generic_body<HD, NT>(P, dsmem, e, g, u, p, lo0, hi0, lo1, hi1, true);
+}
+
+template <int HD, int NT>
+__global__ void __launch_bounds__(kWarps * 32) decode_kernel(const DecodeParams P) {
+    extern __shared__ __align__(128) uint8_t dsmem[];
+    const int e = blockIdx.x, g = blockIdx.y, u = blockIdx.z;
+    const int G = P.Hq / P.Hkv;
+    write_header(P, HD);
+    const int p = P.pos[u];
+    const size_t head0 = static_cast<size_t>(u) * P.Hq + static_cast<size_t>(g) * G;
+    if (p < 0 || p >= P.max_seq) {
+        if (threadIdx.x == 0 && e == 0 && g == 0) flag_error(P.err, FA_ERRBIT_DEVICE);
+        write_empty(P, head0, G, e);
+        return;
+    }
+    if (e == P.shadow_entry) {
+        shadow_entry<HD, NT>(P, dsmem, e, g, u, p);
+        return;
+    }
+    int k_lo, k_hi;
+    if (!entry_range(P, e, p, &k_lo, &k_hi)) {
+        write_empty(P, head0, G, e);
+        return;
+    }
+    generic_body<HD, NT>(P, dsmem, e, g, u, p, k_lo, k_hi, 0, 0, false);
+}
+
+// ============================================================== Q4_0 path
+
+template <int HD>
+struct Q4Cfg {
+    static constexpr int NB = HD / kQ4Block;                  // blocks per row
+    static constexpr int MT = HD / 16;                        // m16 tiles of head_dim
+    static constexpr int ROWB = NB * kQ4BlockBytes;           // bytes per row
+    static constexpr int TILE = kTileKeys * ROWB;             // bytes of K (or V) per stage
+    static constexpr int TILE_ALLOC = (TILE + 127) / 128 * 128;
+    static constexpr int WARP_BYTES = kStages * 2 * TILE_ALLOC;
+    static constexpr int BAR_OFF = kWarps * WARP_BYTES;
+    static constexpr int SMEM_PIPE = BAR_OFF + kWarps * kStages * 8 + 16;
+    static constexpr int SMEM_GENERIC = kWarps * 2 * kChunk * (HD + 8) * 2;
+    static constexpr int SMEM_MERGE = kWarps * 16 * (4 + HD) * 4;
+    static constexpr int SMEM = SMEM_PIPE > SMEM_GENERIC
+                                    ? (SMEM_PIPE > SMEM_MERGE ? SMEM_PIPE : SMEM_MERGE)
+                                    : (SMEM_GENERIC > SMEM_MERGE ? SMEM_GENERIC : SMEM_MERGE);
+};
+
+__device__ __forceinline__ uint32_t nib_lo(uint32_t x) {  // fp16 1024 + c, two lanes
+    return (x & 0x000F000Fu) | 0x64006400u;
+}
+__device__ __forceinline__ uint32_t nib_hi(uint32_t x) {
+    return ((x >> 4) & 0x000F000Fu) | 0x64006400u;
+}
+__device__ __forceinline__ uint32_t hsub1032(uint32_t x) {  // (1024 + c) - 1032 = c - 8, exact
+    __half2 h = *reinterpret_cast<__half2 *>(&x);
+    h = __hsub2(h, __half2half2(__ushort_as_half(0x6408u)));  // 1032.0
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
+    __half2 x = *reinterpret_cast<__half2 *>(&a), y = *reinterpret_cast<__half2 *>(&b);
+    x = __hmul2(x, y);
+    return *reinterpret_cast<uint32_t *>(&x);
+}
+
+template <int HD>
+__device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, int e, int g,
+                                        int u, int p, int k_lo, int k_hi) {
+    using C = Q4Cfg<HD>;
+    constexpr int NB = C::NB, MT = C::MT, ROWB = C::ROWB;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = lane >> 2, t = lane & 3;
+    const int G = P.Hq / P.Hkv;
+    const size_t head0 = static_cast<size_t>(u) * P.Hq + static_cast<size_t>(g) * G;
+    uint8_t *wbase = dsmem + warp * C::WARP_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(dsmem + C::BAR_OFF) + warp * kStages;
+    volatile int *abort = reinterpret_cast<volatile int *>(dsmem + C::BAR_OFF + kWarps * kStages * 8);
+
+    if (threadIdx.x == 0) *abort = 0;
+    if (lane == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    const uint8_t *kbody = P.k_planes + static_cast<size_t>(u) * P.plane_bytes + P.body_off +
+                           static_cast<size_t>(g) * P.max_seq * ROWB;
+    const uint8_t *vbody = P.v_planes + static_cast<size_t>(u) * P.plane_bytes + P.body_off +
+                           static_cast<size_t>(g) * P.max_seq * ROWB;
+    const int ss = P.shadow_sink, sw = P.shadow_win;
+    const int ntiles = (k_hi - k_lo + kTileKeys - 1) / kTileKeys;
+    // A tile is worth loading if some key in it is visible and not a shadow key.
+    auto tile_ok = [&](int i) -> bool {
+        const int t0 = k_lo + kTileKeys * i;
+        const int t1 = min(k_hi, t0 + kTileKeys) - 1;
+        if (P.win > 0 && !(t0 < P.sink || t1 >= p - P.win + 1)) return false;
+        if (t1 < ss) return false;
+        if (sw > 0 && t0 > p - sw) return false;
+        return true;
+    };
+    auto next_tile = [&](int i) -> int {
+        while (i < ntiles && !tile_ok(i)) i += kWarps;
+        return i;
+    };
+    auto issue = [&](int i, int s) {
+        const int t0 = k_lo + kTileKeys * i;
+        const int nk = min(kTileKeys, k_hi - t0);
+        const uint32_t bytes = (static_cast<uint32_t>(nk * ROWB) + 15u) & ~15u;
+        mbar_arrive_expect_tx(&bars[s], 2 * bytes);
+        bulk_copy_g2s(wbase + s * 2 * C::TILE_ALLOC, kbody + static_cast<size_t>(t0) * ROWB, bytes,
+                      &bars[s]);
+        bulk_copy_g2s(wbase + s * 2 * C::TILE_ALLOC + C::TILE_ALLOC,
+                      vbody + static_cast<size_t>(t0) * ROWB, bytes, &bars[s]);
+    };
+
+    // Q^T B fragments (natural head_dim order) and the per-block bias
+    // -1032 * sum of the fp16-rounded q over the block, for heads 2t, 2t+1.
+    uint32_t qb[MT][2];
+    float bias[NB][2];
+    {
+        const int hh = r;
+        const float *qr = P.q + (head0 + (hh < G ? hh : 0)) * HD;
+#pragma unroll
+        for (int kk = 0; kk < MT; ++kk) {
+            const int d0 = 16 * kk + 2 * t;
+            if (hh < G) {
+                const float2 a = *reinterpret_cast<const float2 *>(qr + d0);
+                const float2 b = *reinterpret_cast<const float2 *>(qr + d0 + 8);
+                qb[kk][0] = pack_half2(a.x, a.y);
+                qb[kk][1] = pack_half2(b.x, b.y);
+            } else {
+                qb[kk][0] = 0u;
+                qb[kk][1] = 0u;
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            float ps = 0.0f;
+#pragma unroll
+            for (int kk = 2 * b; kk < 2 * b + 2; ++kk)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&qb[kk][j]));
+                    ps += f.x + f.y;
+                }
+            ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+            ps += __shfl_xor_sync(0xffffffffu, ps, 2);  // head r's block sum
+            bias[b][0] = -1032.0f * __shfl_sync(0xffffffffu, ps, (2 * t) * 4);
+            bias[b][1] = -1032.0f * __shfl_sync(0xffffffffu, ps, (2 * t + 1) * 4);
+        }
+    }
+
+    float o[MT][1][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int k = 0; k < 4; ++k) o[mt][0][k] = 0.0f;
+    float m_used[1][2] = {{-INFINITY, -INFINITY}}, m_true[1][2] = {{-INFINITY, -INFINITY}};
+    float lsum[1][2] = {{0.0f, 0.0f}};
+
+    // pipeline: stage s holds tile tiles[s] (ntiles = none)
+    int tiles[kStages];
+    int issued = next_tile(warp);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int head = nt * 8 + 2 * t + (k & 1);
-                const int dim = 16 * mt + r + ((k >> 1) << 3);
-                sm_o[(warp * 16 + head) * HD + dim] = o[mt][nt][k];
-            }
-    __syncthreads();
-    if (threadIdx.x < G) {
-        const int head = threadIdx.x;
-        float M = -INFINITY;
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_mt[w * 16 + head]);
-        float L = 0.0f;
-        for (int w = 0; w < kWarps; ++w) {
-            const float mu = sm_mu[w * 16 + head];
-            const float f = (mu == -INFINITY || M == -INFINITY) ? 0.0f : ex2(mu - M);
-            sm_f[w * 16 + head] = f;
-            L += f * sm_l[w * 16 + head];
+    for (int s = 0; s < kStages; ++s) {
+        tiles[s] = issued;
+        if (issued < ntiles) {
+            if (lane == 0) issue(issued, s);
+            issued = next_tile(issued + kWarps);
         }
-        // natural-log reference: s * scale = (s * scale * log2 e) * ln 2
-        P.ws_m[(head0 + head) * P.stride + e] = (M == -INFINITY) ? -INFINITY : M * 0.69314718055994531f;
-        P.ws_l[(head0 + head) * P.stride + e] = L;
     }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < G * HD; idx += blockDim.x) {
-        const int head = idx / HD, dim = idx % HD;
-        float a = 0.0f;
+    uint32_t phase = 0;
+    int s = 0;
+    bool ok = true;
+    while (tiles[s] < ntiles) {
+        const int i = tiles[s];
+        ok = mbar_wait(&bars[s], (phase >> s) & 1u, abort, P.err);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        phase ^= 1u << s;
+        const uint8_t *Ks = wbase + s * 2 * C::TILE_ALLOC;
+        const uint8_t *Vs = Ks + C::TILE_ALLOC;
+        const int t0 = k_lo + kTileKeys * i;
+
+        // ---- scores of the 32 keys: half h2 holds keys t0 + 16 h2 + {r, r+8}
+        float sc[2][4];
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) a += sm_f[w * 16 + head] * sm_o[(w * 16 + head) * HD + dim];
-        P.ws_acc[((head0 + head) * P.stride + e) * HD + dim] = a;
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const uint8_t *KA = Ks + (16 * h2 + r) * ROWB;
+            const uint8_t *KB = KA + 8 * ROWB;
+            float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                const uint32_t dA = lds_u16(KA + kQ4BlockBytes * b);
+                const uint32_t dB = lds_u16(KB + kQ4BlockBytes * b);
+                const uint32_t xA0 = __byte_perm(lds_u16(KA + kQ4BlockBytes * b + 2 + 2 * t), 0u, 0x4140);
+                const uint32_t xA1 = __byte_perm(lds_u16(KA + kQ4BlockBytes * b + 10 + 2 * t), 0u, 0x4140);
+                const uint32_t xB0 = __byte_perm(lds_u16(KB + kQ4BlockBytes * b + 2 + 2 * t), 0u, 0x4140);
+                const uint32_t xB1 = __byte_perm(lds_u16(KB + kQ4BlockBytes * b + 10 + 2 * t), 0u, 0x4140);
+                const uint32_t alo[4] = {nib_lo(xA0), nib_lo(xB0), nib_lo(xA1), nib_lo(xB1)};
+                const uint32_t ahi[4] = {nib_hi(xA0), nib_hi(xB0), nib_hi(xA1), nib_hi(xB1)};
+                float acc[4] = {bias[b][0], bias[b][1], bias[b][0], bias[b][1]};
+                mma_16816(acc, alo, qb[2 * b]);
+                mma_16816(acc, ahi, qb[2 * b + 1]);
+                const float fA = __half2float(__ushort_as_half(static_cast<uint16_t>(dA)));
+                const float fB = __half2float(__ushort_as_half(static_cast<uint16_t>(dB)));
+                s4[0] = fmaf(fA, acc[0], s4[0]);
+                s4[1] = fmaf(fA, acc[1], s4[1]);
+                s4[2] = fmaf(fB, acc[2], s4[2]);
+                s4[3] = fmaf(fB, acc[3], s4[3]);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) sc[h2][k] = s4[k];
+        }
+        // ---- mask and fold: key of score sc[h2][k] is t0 + 16 h2 + r + 8 (k >> 1)
+        float sv[2][4], pv[2][4];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int key = t0 + 16 * h2 + r + 8 * half;
+                const bool vis = key < k_hi && key_visible(p, key, P.sink, P.win) &&
+                                 !(key < ss || (sw > 0 && key > p - sw));
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+                    sv[hh][2 * h2 + half] = vis ? sc[h2][2 * half + hh] : -INFINITY;
+            }
+        fold_scores<MT, 1, 4>(sv, P.sl2, kRescaleQ4, m_used[0][0], m_used[0][1], m_true[0][0],
+                              m_true[0][1], lsum[0][0], lsum[0][1], o, 0, pv);
+
+        // ---- O^T += V^T P'^T per 16-key half
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            // P^T B fragments: keys 2t,2t+1 (b0) and 2t+8,2t+9 (b1) of head r
+            const uint32_t pb0 = movmatrix_trans(pack_half2(pv[0][2 * h2], pv[1][2 * h2]));
+            const uint32_t pb1 = movmatrix_trans(pack_half2(pv[0][2 * h2 + 1], pv[1][2 * h2 + 1]));
+            const uint8_t *V0 = Vs + (16 * h2 + 2 * t) * ROWB;   // key 2t
+            const uint8_t *V1 = V0 + ROWB;                       // key 2t+1
+            const uint8_t *V2 = V0 + 8 * ROWB;                   // key 2t+8
+            const uint8_t *V3 = V2 + ROWB;                       // key 2t+9
+            const int kb = t0 + 16 * h2 + 2 * t;
+            // a key past the range has P = 0; force its scale to 0 so that no
+            // stale or uninitialised bytes can turn 0 * d into NaN
+            const uint32_t mask01 = (kb < k_hi ? 0x0000FFFFu : 0u) | (kb + 1 < k_hi ? 0xFFFF0000u : 0u);
+            const uint32_t mask23 = (kb + 8 < k_hi ? 0x0000FFFFu : 0u) | (kb + 9 < k_hi ? 0xFFFF0000u : 0u);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                const int off = kQ4BlockBytes * b;
+                const uint32_t d01 = __byte_perm(lds_u16(V0 + off), lds_u16(V1 + off), 0x5410) & mask01;
+                const uint32_t d23 = __byte_perm(lds_u16(V2 + off), lds_u16(V3 + off), 0x5410) & mask23;
+                const uint32_t bb[2] = {hmul2u(pb0, d01), hmul2u(pb1, d23)};
+                const uint32_t x01 = __byte_perm(lds_u8(V0 + off + 2 + r), lds_u8(V1 + off + 2 + r), 0x5410);
+                const uint32_t x23 = __byte_perm(lds_u8(V2 + off + 2 + r), lds_u8(V3 + off + 2 + r), 0x5410);
+                const uint32_t y01 = __byte_perm(lds_u8(V0 + off + 10 + r), lds_u8(V1 + off + 10 + r), 0x5410);
+                const uint32_t y23 = __byte_perm(lds_u8(V2 + off + 10 + r), lds_u8(V3 + off + 10 + r), 0x5410);
+                const uint32_t alo[4] = {hsub1032(nib_lo(x01)), hsub1032(nib_lo(y01)),
+                                         hsub1032(nib_lo(x23)), hsub1032(nib_lo(y23))};
+                const uint32_t ahi[4] = {hsub1032(nib_hi(x01)), hsub1032(nib_hi(y01)),
+                                         hsub1032(nib_hi(x23)), hsub1032(nib_hi(y23))};
+                mma_16816(o[2 * b][0], alo, bb);
+                mma_16816(o[2 * b + 1][0], ahi, bb);
+            }
+        }
+        __syncwarp();
+        // refill this stage with the warp's next tile
+        tiles[s] = issued;
+        if (issued < ntiles) {
+            if (lane == 0) issue(issued, s);
+            issued = next_tile(issued + kWarps);
+        }
+        s = (s + 1 == kStages) ? 0 : s + 1;
     }
+    if (!ok) {
+        // let the copies already issued land before the shared memory is reused
+        for (int k = 0; k < kStages; ++k) {
+            const int st = (s + k) % kStages;
+            if (tiles[st] < ntiles) {
+                const long long c0 = clock64();
+                while (!mbar_try_wait(&bars[st], (phase >> st) & 1u) && clock64() - c0 < kSpinCycles) {
+                }
+                phase ^= 1u << st;
+            }
+        }
+    }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        float v = lsum[0][hh];
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        v += __shfl_xor_sync(0xffffffffu, v, 8);
+        v += __shfl_xor_sync(0xffffffffu, v, 16);
+        lsum[0][hh] = v;
+    }
+    merge_and_write<HD, 1>(P, dsmem, head0, G, e, m_used, m_true, lsum, o);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kWarps * 32, 2) decode_q4_kernel(const DecodeParams P) {
+    extern __shared__ __align__(128) uint8_t dsmem[];
+    const int e = blockIdx.x, g = blockIdx.y, u = blockIdx.z;
+    const int G = P.Hq / P.Hkv;
+    write_header(P, HD);
+    const int p = P.pos[u];
+    const size_t head0 = static_cast<size_t>(u) * P.Hq + static_cast<size_t>(g) * G;
+    if (p < 0 || p >= P.max_seq) {
+        if (threadIdx.x == 0 && e == 0 && g == 0) flag_error(P.err, FA_ERRBIT_DEVICE);
+        write_empty(P, head0, G, e);
+        return;
+    }
+    if (e == P.shadow_entry) {
+        shadow_entry<HD, 1>(P, dsmem, e, g, u, p);
+        return;
+    }
+    int k_lo, k_hi;
+    if (!entry_range(P, e, p, &k_lo, &k_hi)) {
+        write_empty(P, head0, G, e);
+        return;
+    }
+    q4_body<HD>(P, dsmem, e, g, u, p, k_lo, k_hi);
 }
 
 // One warp per (slot, q head): ascending merge of the entries.
@@ -380,7 +796,7 @@ __global__ void __launch_bounds__(128)
 }
 
 template <int HD, int NT>
-cudaError_t launch_decode_t(const DecodeParams &P, cudaStream_t stream) {
+cudaError_t launch_generic(const DecodeParams &P, cudaStream_t stream) {
     const size_t tiles = static_cast<size_t>(kWarps) * 2 * kChunk * (HD + 8) * 2;
     const size_t merge = static_cast<size_t>(kWarps) * 16 * (4 + HD) * 4;
     const size_t smem = tiles > merge ? tiles : merge;
@@ -393,15 +809,47 @@ cudaError_t launch_decode_t(const DecodeParams &P, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-}  // namespace
-
-size_t decode_ws_bytes(int nslots, int n_q_heads, int head_dim, int max_splits) {
-    auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-    const size_t heads = static_cast<size_t>(nslots) * n_q_heads;
-    return 256 + 2 * up(heads * max_splits * 4) + up(heads * max_splits * head_dim * 4);
+template <int HD>
+cudaError_t launch_q4(const DecodeParams &P, cudaStream_t stream) {
+    using C = Q4Cfg<HD>;
+    cudaError_t e = cudaFuncSetAttribute(decode_q4_kernel<HD>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    dim3 grid(P.entries, P.Hkv, P.nslots);
+    decode_q4_kernel<HD><<<grid, kWarps * 32, C::SMEM, stream>>>(P);
+    return cudaGetLastError();
 }
 
-void decode_ws_carve(void *ws, int nslots, int n_q_heads, int head_dim, int max_splits,
+}  // namespace
+
+DecodeShape decode_shape(int nslots, int n_q_heads, int n_kv_heads, int kv_fmt, int shadow_sink,
+                         int shadow_win, int max_splits, int max_seq, size_t row_bytes) {
+    DecodeShape d;
+    const int G = n_q_heads / n_kv_heads;
+    // The Q4_0 path bulk-copies rows [t0, t0+32) of a kv head; the copy must
+    // start 16-byte aligned, so every head's body must start 16-byte aligned.
+    d.fast = kv_fmt == 1 && G <= 8 && (static_cast<size_t>(max_seq) * row_bytes) % 16 == 0;
+    // Blocks per wave: the Q4_0 path keeps 2 blocks per SM; aim at about four
+    // waves so the last one is short.
+    const long long pairs = static_cast<long long>(nslots) * n_kv_heads;
+    const long long target = (d.fast ? 8LL : 4LL) * device_sm_count();
+    long long cpc = (pairs * max_splits + target - 1) / target;
+    if (cpc < 1) cpc = 1;
+    if (cpc > max_splits) cpc = max_splits;
+    d.splits_per_cta = static_cast<int>(cpc);
+    d.body_entries = static_cast<int>((max_splits + cpc - 1) / cpc);
+    d.shadow_entry = (d.fast && (shadow_sink > 0 || shadow_win > 0)) ? d.body_entries : -1;
+    d.entries = d.body_entries + (d.shadow_entry >= 0 ? 1 : 0);
+    return d;
+}
+
+size_t decode_ws_bytes(int nslots, int n_q_heads, int head_dim, int stride) {
+    auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    const size_t heads = static_cast<size_t>(nslots) * n_q_heads;
+    return 256 + 2 * up(heads * stride * 4) + up(heads * stride * head_dim * 4);
+}
+
+void decode_ws_carve(void *ws, int nslots, int n_q_heads, int head_dim, int stride,
                      DecodeWs *out) {
     (void)head_dim;
     auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
@@ -409,13 +857,13 @@ void decode_ws_carve(void *ws, int nslots, int n_q_heads, int head_dim, int max_
     uint8_t *b = static_cast<uint8_t *>(ws);
     out->header = reinterpret_cast<uint32_t *>(b);
     out->m = reinterpret_cast<float *>(b + 256);
-    out->l = reinterpret_cast<float *>(b + 256 + up(heads * max_splits * 4));
-    out->acc = reinterpret_cast<float *>(b + 256 + 2 * up(heads * max_splits * 4));
-    out->stride = max_splits;
+    out->l = reinterpret_cast<float *>(b + 256 + up(heads * stride * 4));
+    out->acc = reinterpret_cast<float *>(b + 256 + 2 * up(heads * stride * 4));
+    out->stride = stride;
 }
 
-cudaError_t launch_decode(const DecodeArgs &a, const DecodeWs &ws, unsigned *err,
-                          cudaStream_t stream) {
+cudaError_t launch_decode(const DecodeArgs &a, const DecodeWs &ws, const DecodeShape &d,
+                          unsigned *err, cudaStream_t stream) {
     DecodeParams P;
     P.q = a.q;
     P.k_planes = a.k_planes;
@@ -436,9 +884,10 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodeWs &ws, unsigned *err
     P.shadow_win = a.shadow_win;
     P.split_keys = a.split_keys;
     P.max_splits = a.max_splits;
-    P.cpc = ws.splits_per_cta;
-    P.entries = ws.entries;
+    P.cpc = d.splits_per_cta;
+    P.entries = d.entries;
     P.stride = ws.stride;
+    P.shadow_entry = d.shadow_entry;
     P.plane_bytes = a.g.bytes;
     P.body_off = a.g.body_off;
     P.row_bytes = a.g.row_bytes;
@@ -446,20 +895,29 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodeWs &ws, unsigned *err
     P.ring_off = a.g.ring_off;
     P.sl2 = a.scale * 1.4426950408889634f;
     P.err = err;
+    if (d.entries > ws.stride) return cudaErrorInvalidValue;
     const int G = a.n_q_heads / a.n_kv_heads;
+    if (d.fast) {
+        switch (a.g.hd) {
+            case 64: return launch_q4<64>(P, stream);
+            case 128: return launch_q4<128>(P, stream);
+            case 256: return launch_q4<256>(P, stream);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     const bool two = G > 8;
     switch (a.g.hd) {
-        case 64: return two ? launch_decode_t<64, 2>(P, stream) : launch_decode_t<64, 1>(P, stream);
-        case 128: return two ? launch_decode_t<128, 2>(P, stream) : launch_decode_t<128, 1>(P, stream);
-        case 256: return two ? launch_decode_t<256, 2>(P, stream) : launch_decode_t<256, 1>(P, stream);
+        case 64: return two ? launch_generic<64, 2>(P, stream) : launch_generic<64, 1>(P, stream);
+        case 128: return two ? launch_generic<128, 2>(P, stream) : launch_generic<128, 1>(P, stream);
+        case 256: return two ? launch_generic<256, 2>(P, stream) : launch_generic<256, 1>(P, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t launch_combine(const void *workspace, float *out, int nslots, int n_q_heads,
-                           int head_dim, int max_splits, unsigned *err, cudaStream_t stream) {
+                           int head_dim, int stride, unsigned *err, cudaStream_t stream) {
     DecodeWs ws;
-    decode_ws_carve(const_cast<void *>(workspace), nslots, n_q_heads, head_dim, max_splits, &ws);
+    decode_ws_carve(const_cast<void *>(workspace), nslots, n_q_heads, head_dim, stride, &ws);
     const long long heads = static_cast<long long>(nslots) * n_q_heads;
     const int blocks = static_cast<int>((heads + 3) / 4);
     switch (head_dim) {

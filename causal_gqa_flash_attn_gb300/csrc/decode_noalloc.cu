@@ -85,15 +85,12 @@ extern "C" fa_status fa_decode_noalloc(const float *q, const void *k_planes,
     fa::PlaneGeom g;
     if (!fa::plane_geom(kv_fmt, n_kv_heads, max_seq, head_dim, &g)) return FA_ERR_INVALID;
 
-    // Same plan as fa_decode: runs of plan splits merged inside one block so
-    // that about four blocks per SM cover every (slot, kv head) pair; E
-    // partials per (slot, head), stored with stride E (not max_splits).
-    const long long pairs = static_cast<long long>(nslots) * n_kv_heads;
-    const long long target = 4LL * fa::device_sm_count();
-    long long cpc = (pairs * max_splits + target - 1) / target;
-    if (cpc < 1) cpc = 1;
-    if (cpc > max_splits) cpc = max_splits;
-    const int entries = static_cast<int>((max_splits + cpc - 1) / cpc);
+    // The same work split as fa_decode; the partials are stored with entry
+    // stride equal to the number of entries (not max_splits + 1).
+    const fa::DecodeShape shape = fa::decode_shape(nslots, n_q_heads, n_kv_heads, kv_fmt,
+                                                   shadow_sink, shadow_win, max_splits, max_seq,
+                                                   g.row_bytes);
+    const int entries = shape.entries;
     if (fa::decode_ws_bytes(nslots, n_q_heads, head_dim, entries) > kFaDecodeScratchBytes)
         return FA_ERR_WORKSPACE;
 
@@ -103,8 +100,6 @@ extern "C" fa_status fa_decode_noalloc(const float *q, const void *k_planes,
 
     fa::DecodeWs ws;
     fa::decode_ws_carve(scratch, nslots, n_q_heads, head_dim, entries, &ws);
-    ws.entries = entries;
-    ws.splits_per_cta = static_cast<int>(cpc);
     fa::DecodeArgs a;
     a.q = q;
     a.k_planes = static_cast<const uint8_t *>(k_planes);
@@ -123,7 +118,7 @@ extern "C" fa_status fa_decode_noalloc(const float *q, const void *k_planes,
     a.scale = 1.0f / sqrtf(static_cast<float>(head_dim));
     a.workspace = scratch;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = fa::launch_decode(a, ws, err, s);
+    cudaError_t e = fa::launch_decode(a, ws, shape, err, s);
     // The combine carves the same array with stride `entries`.
     if (e == cudaSuccess)
         e = fa::launch_combine(scratch, out, nslots, n_q_heads, head_dim, entries, err, s);

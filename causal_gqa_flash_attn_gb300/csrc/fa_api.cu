@@ -264,7 +264,7 @@ fa_status fa_prefill(const float *q, const void *k, const void *v, float *out, i
 
 size_t fa_decode_workspace_bytes(int nslots, int n_q_heads, int head_dim, int max_splits) {
     if (nslots < 1 || n_q_heads < 1 || head_dim < 1 || max_splits < 1) return 0;
-    return fa::decode_ws_bytes(nslots, n_q_heads, head_dim, max_splits);
+    return fa::decode_ws_bytes(nslots, n_q_heads, head_dim, max_splits + 1);
 }
 
 fa_status fa_decode(const float *q, const void *k_planes, const void *v_planes,
@@ -283,23 +283,17 @@ fa_status fa_decode(const float *q, const void *k_planes, const void *v_planes,
     if (!aligned16(q) || !aligned16(k_planes) || !aligned16(v_planes) || !aligned16(workspace) ||
         (reinterpret_cast<uintptr_t>(pos) & 3u))
         return FA_ERR_INVALID;
-    if (workspace_bytes < fa::decode_ws_bytes(nslots, n_q_heads, head_dim, max_splits))
+    if (workspace_bytes < fa::decode_ws_bytes(nslots, n_q_heads, head_dim, max_splits + 1))
         return FA_ERR_WORKSPACE;
     fa::PlaneGeom g;
     if (!fa::plane_geom(kv_fmt, n_kv_heads, max_seq, head_dim, &g)) return FA_ERR_INVALID;
     DeviceInfo *d = device_info();
     if (!d || !d->err) return FA_ERR_CUDA;
     fa::DecodeWs ws;
-    fa::decode_ws_carve(workspace, nslots, n_q_heads, head_dim, max_splits, &ws);
-    // Merge runs of plan splits inside one block so that about four blocks per
-    // SM cover every (slot, kv head) pair.
-    const long long pairs = static_cast<long long>(nslots) * n_kv_heads;
-    const long long target = 4LL * fa::device_sm_count();
-    long long cpc = (pairs * max_splits + target - 1) / target;
-    if (cpc < 1) cpc = 1;
-    if (cpc > max_splits) cpc = max_splits;
-    ws.splits_per_cta = static_cast<int>(cpc);
-    ws.entries = static_cast<int>((max_splits + cpc - 1) / cpc);
+    fa::decode_ws_carve(workspace, nslots, n_q_heads, head_dim, max_splits + 1, &ws);
+    const fa::DecodeShape shape = fa::decode_shape(nslots, n_q_heads, n_kv_heads, kv_fmt,
+                                                   shadow_sink, shadow_win, max_splits, max_seq,
+                                                   g.row_bytes);
     fa::DecodeArgs a;
     a.q = q;
     a.k_planes = static_cast<const uint8_t *>(k_planes);
@@ -319,7 +313,7 @@ fa_status fa_decode(const float *q, const void *k_planes, const void *v_planes,
     a.workspace = workspace;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = record_start(s);
-    if (e == cudaSuccess) e = fa::launch_decode(a, ws, d->err, s);
+    if (e == cudaSuccess) e = fa::launch_decode(a, ws, shape, d->err, s);
     if (e == cudaSuccess) e = record_stop(s);
     return from_cuda(e);
 }
@@ -332,8 +326,9 @@ fa_status fa_decode_combine(const void *workspace, float *out, int nslots, int n
     if (!workspace || !out || !aligned16(workspace) || !aligned16(out)) return FA_ERR_INVALID;
     DeviceInfo *d = device_info();
     if (!d || !d->err) return FA_ERR_CUDA;
-    return from_cuda(fa::launch_combine(workspace, out, nslots, n_q_heads, head_dim, max_splits,
-                                        d->err, reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(fa::launch_combine(workspace, out, nslots, n_q_heads, head_dim,
+                                        max_splits + 1, d->err,
+                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
 fa_status fa_set_kernel_events(void *start, void *stop) {

@@ -74,17 +74,27 @@ struct DecodeArgs {
 struct DecodeWs {
     uint32_t *header;
     float *m, *l, *acc;
-    int stride;          // entry stride per (slot, head) = max_splits
-    int entries;         // partials written per (slot, head), <= stride
-    int splits_per_cta;  // plan splits merged inside one block
+    int stride;  // entry stride per (slot, head)
 };
-size_t decode_ws_bytes(int nslots, int n_q_heads, int head_dim, int max_splits);
-void decode_ws_carve(void *ws, int nslots, int n_q_heads, int head_dim, int max_splits,
+// How fa_decode splits the work: runs of splits_per_cta plan splits per block
+// (body_entries blocks per (slot, kv head)), plus one entry for the fp16
+// shadow keys when the Q4_0 fast path is used.
+struct DecodeShape {
+    bool fast;           // Q4_0 kernel (group <= 8, 16-byte aligned K/V rows per head)
+    int splits_per_cta;
+    int body_entries;
+    int shadow_entry;    // -1 if none
+    int entries;         // body_entries + (shadow_entry >= 0)
+};
+DecodeShape decode_shape(int nslots, int n_q_heads, int n_kv_heads, int kv_fmt, int shadow_sink,
+                         int shadow_win, int max_splits, int max_seq, size_t row_bytes);
+size_t decode_ws_bytes(int nslots, int n_q_heads, int head_dim, int stride);
+void decode_ws_carve(void *ws, int nslots, int n_q_heads, int head_dim, int stride,
                      DecodeWs *out);
-cudaError_t launch_decode(const DecodeArgs &a, const DecodeWs &ws, unsigned *err,
-                          cudaStream_t stream);
+cudaError_t launch_decode(const DecodeArgs &a, const DecodeWs &ws, const DecodeShape &d,
+                          unsigned *err, cudaStream_t stream);
 cudaError_t launch_combine(const void *workspace, float *out, int nslots, int n_q_heads,
-                           int head_dim, int max_splits, unsigned *err, cudaStream_t stream);
+                           int head_dim, int stride, unsigned *err, cudaStream_t stream);
 
 constexpr uint32_t kDecodeMagic = 0x46414443u;  // "FADC"
 

@@ -181,9 +181,10 @@ fa_status fa_prefill(const float *q, const void *k, const void *v, float *out, i
  * in ascending order: M = max m_e, w_e = exp(m_e - M),
  * out = sum w_e acc_e / sum w_e l_e.
  *
- * Workspace layout (S = max_splits): a 256-byte header of uint32 words
- * {0x46414443, nslots, n_q_heads, head_dim, E} where E <= S is the number of
- * entries fa_decode wrote per head, then m [nslots*n_q_heads][S] fp32,
+ * A Q4_0 cache's fp16 shadow keys (sinks, recent ring) go to one extra entry
+ * per head. Workspace layout (S = max_splits + 1): a 256-byte header of uint32
+ * words {0x46414443, nslots, n_q_heads, head_dim, E} where E <= S is the
+ * number of entries fa_decode wrote per head, then m [nslots*n_q_heads][S] fp32,
  * l [nslots*n_q_heads][S] fp32 and acc [nslots*n_q_heads][S][head_dim] fp32,
  * each part starting 256-byte aligned; entry e of a head is at index e < E.
  */

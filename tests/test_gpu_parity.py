@@ -295,9 +295,10 @@ def test_combine_on_oracle_partials(oracle_mod):
     ws_bytes = m.decode_workspace_bytes(nslots, hq, hd, max_splits)
     heads = nslots * hq
     up = lambda x: (x + 255) // 256 * 256
-    m_arr = np.full((heads, max_splits), -np.inf, np.float32)
-    l_arr = np.zeros((heads, max_splits), np.float32)
-    acc = np.zeros((heads, max_splits, hd), np.float32)
+    S = max_splits + 1        # entry stride of fa_decode's workspace
+    m_arr = np.full((heads, S), -np.inf, np.float32)
+    l_arr = np.zeros((heads, S), np.float32)
+    acc = np.zeros((heads, S, hd), np.float32)
     want = np.zeros((nslots, hq, hd))
     for u in range(nslots):
         q, k, v = decode_slot_inputs(L, hq, hkv, hd, seed=3, slot=u)
@@ -315,8 +316,8 @@ def test_combine_on_oracle_partials(oracle_mod):
     buf = np.zeros(ws_bytes, np.uint8)
     buf[:20] = np.array([0x46414443, nslots, hq, hd, E], np.uint32).view(np.uint8)
     o_m = 256
-    o_l = o_m + up(heads * max_splits * 4)
-    o_a = o_l + up(heads * max_splits * 4)
+    o_l = o_m + up(heads * S * 4)
+    o_a = o_l + up(heads * S * 4)
     buf[o_m:o_m + m_arr.nbytes] = m_arr.view(np.uint8).ravel()
     buf[o_l:o_l + l_arr.nbytes] = l_arr.view(np.uint8).ravel()
     buf[o_a:o_a + acc.nbytes] = acc.view(np.uint8).ravel()
