@@ -35,7 +35,6 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kChunk = 16;     // keys per step of the generic path
 constexpr int kTileKeys = 32;  // keys per stage of the Q4_0 path
-constexpr int kStages = 3;     // stages per warp of the Q4_0 path
 // Lazy rescale threshold (log2 units) of the running max: O and l keep a
 // stale reference until the max grows past it. In the Q4_0 path P is
 // multiplied by the block scale d in fp16, so P <= 2^2 keeps P*d finite for
@@ -84,8 +83,8 @@ __device__ __forceinline__ void write_empty(const DecodeParams &P, size_t head0,
 // Merge the kWarps per-warp online-softmax states of a block and write the
 // block's partial. Per thread: m_used/m_true/lsum of heads nt*8 + 2t + {0,1}
 // (exp2 domain, lsum already summed over the warp), o[mt][nt][k] of rows
-// 16mt + r (+8 for k >= 2), heads nt*8 + 2t + (k & 1).
-template <int HD, int NT>
+// r (k < 2) and r+8 (k >= 2) of m-tile mt, heads nt*8 + 2t + (k & 1).
+template <int HD, int NT, bool Q4ROWS = false>
 __device__ __forceinline__ void merge_and_write(const DecodeParams &P, uint8_t *dsmem,
                                                 size_t head0, int G, int e,
                                                 const float (&m_used)[NT][2],
@@ -119,7 +118,10 @@ __device__ __forceinline__ void merge_and_write(const DecodeParams &P, uint8_t *
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int head = nt * 8 + 2 * t + (k & 1);
-                const int dim = 16 * mt + r + ((k >> 1) << 3);
+                // Q4_0 path: m-tile 2b (2b+1) rows r, r+8 hold elements 2r, 2r+1
+                // (16 + 2r, 17 + 2r) of block b; generic path: natural order.
+                const int dim = Q4ROWS ? 32 * (mt >> 1) + 16 * (mt & 1) + 2 * r + (k >> 1)
+                                       : 16 * mt + r + ((k >> 1) << 3);
                 sm_o[(warp * 16 + head) * HD + dim] = o[mt][nt][k];
             }
     __syncthreads();
@@ -449,32 +451,37 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(const DecodeParams 
 
 // ============================================================== Q4_0 path
 
+// The Q4_0 path's pipeline depth and residency (stages per warp, blocks per
+// SM); shared memory per block is 4 warps x stages x 2 tiles of 32 keys.
+#ifndef FA_Q4_STAGES
+#define FA_Q4_STAGES 2
+#endif
+#ifndef FA_Q4_MIN_BLOCKS
+#define FA_Q4_MIN_BLOCKS 3
+#endif
+
 template <int HD>
 struct Q4Cfg {
+    static constexpr int NST = FA_Q4_STAGES;
     static constexpr int NB = HD / kQ4Block;                  // blocks per row
     static constexpr int MT = HD / 16;                        // m16 tiles of head_dim
     static constexpr int ROWB = NB * kQ4BlockBytes;           // bytes per row
     static constexpr int TILE = kTileKeys * ROWB;             // bytes of K (or V) per stage
     static constexpr int TILE_ALLOC = (TILE + 127) / 128 * 128;
-    static constexpr int WARP_BYTES = kStages * 2 * TILE_ALLOC;
+    static constexpr int WARP_BYTES = NST * 2 * TILE_ALLOC;
     static constexpr int BAR_OFF = kWarps * WARP_BYTES;
-    static constexpr int SMEM_PIPE = BAR_OFF + kWarps * kStages * 8 + 16;
+    static constexpr int SMEM_PIPE = BAR_OFF + kWarps * NST * 8 + 16;
     static constexpr int SMEM_GENERIC = kWarps * 2 * kChunk * (HD + 8) * 2;
     static constexpr int SMEM_MERGE = kWarps * 16 * (4 + HD) * 4;
     static constexpr int SMEM = SMEM_PIPE > SMEM_GENERIC
                                     ? (SMEM_PIPE > SMEM_MERGE ? SMEM_PIPE : SMEM_MERGE)
                                     : (SMEM_GENERIC > SMEM_MERGE ? SMEM_GENERIC : SMEM_MERGE);
+    static_assert(NB % 2 == 0, "head_dim must be a multiple of 64");
 };
 
-__device__ __forceinline__ uint32_t nib_lo(uint32_t x) {  // fp16 1024 + c, two lanes
-    return (x & 0x000F000Fu) | 0x64006400u;
-}
-__device__ __forceinline__ uint32_t nib_hi(uint32_t x) {
-    return ((x >> 4) & 0x000F000Fu) | 0x64006400u;
-}
-__device__ __forceinline__ uint32_t hsub1032(uint32_t x) {  // (1024 + c) - 1032 = c - 8, exact
+__device__ __forceinline__ uint32_t h2sub(uint32_t x, uint16_t c_bits) {
     __half2 h = *reinterpret_cast<__half2 *>(&x);
-    h = __hsub2(h, __half2half2(__ushort_as_half(0x6408u)));  // 1032.0
+    h = __hsub2(h, __half2half2(__ushort_as_half(c_bits)));
     return *reinterpret_cast<uint32_t *>(&h);
 }
 __device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
@@ -482,23 +489,37 @@ __device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
     x = __hmul2(x, y);
     return *reinterpret_cast<uint32_t *>(&x);
 }
+constexpr uint32_t kMagic = 0x64006400u;    // fp16 pair (1024, 1024)
+constexpr uint32_t kHNeg1032 = 0xE408E408u;  // fp16 pair (-1032, -1032)
+constexpr uint32_t kHNeg1152 = 0xE480E480u;  // fp16 pair (-1152, -1152)
+constexpr uint16_t kH1032 = 0x6408u;        // fp16 1032 = 1024 + 8
+constexpr uint16_t kH1152 = 0x6480u;        // fp16 1152 = 1024 + 16 * 8
+
+// Code bytes of block b that thread t (of 4 per row) turns into its K operand
+// halves: a 32-bit word read at an aligned offset. Element order within the
+// block is permuted per thread (and mirrored in Q): odd blocks give thread t
+// bytes 4t..4t+3; even blocks, whose codes start 2 bytes off a word, give
+// threads 0-2 bytes 2+4t..5+4t and thread 3 bytes 14, 15, 0, 1.
+__host__ __device__ constexpr int q4k_elem(int b, int t, int i) {
+    return (b & 1) ? 4 * t + i : (t < 3 ? 2 + 4 * t + i : (i < 2 ? 14 + i : i - 2));
+}
 
 template <int HD>
 __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, int e, int g,
                                         int u, int p, int k_lo, int k_hi) {
     using C = Q4Cfg<HD>;
-    constexpr int NB = C::NB, MT = C::MT, ROWB = C::ROWB;
+    constexpr int NB = C::NB, MT = C::MT, ROWB = C::ROWB, NST = C::NST;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = lane >> 2, t = lane & 3;
     const int G = P.Hq / P.Hkv;
     const size_t head0 = static_cast<size_t>(u) * P.Hq + static_cast<size_t>(g) * G;
     uint8_t *wbase = dsmem + warp * C::WARP_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(dsmem + C::BAR_OFF) + warp * kStages;
-    volatile int *abort = reinterpret_cast<volatile int *>(dsmem + C::BAR_OFF + kWarps * kStages * 8);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(dsmem + C::BAR_OFF) + warp * NST;
+    volatile int *abort = reinterpret_cast<volatile int *>(dsmem + C::BAR_OFF + kWarps * NST * 8);
 
     if (threadIdx.x == 0) *abort = 0;
     if (lane == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+        for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
         mbar_fence_init();
     }
     __syncthreads();
@@ -533,40 +554,37 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
                       vbody + static_cast<size_t>(t0) * ROWB, bytes, &bars[s]);
     };
 
-    // Q^T B fragments (natural head_dim order) and the per-block bias
-    // -1032 * sum of the fp16-rounded q over the block, for heads 2t, 2t+1.
+    // Q^T B fragments in the permuted order of q4k_elem: lo k-step of block b
+    // (elements 0..15) takes q as is, the hi k-step (elements 16..31) q / 16,
+    // because the K operand there is 1024 + 16 c. bias[b] = -(1032 sum_lo q +
+    // 1152 sum_hi q/16) over the fp16 values, for heads 2t, 2t+1, so that the
+    // accumulator ends at sum q (c - 8).
     uint32_t qb[MT][2];
     float bias[NB][2];
     {
         const int hh = r;
         const float *qr = P.q + (head0 + (hh < G ? hh : 0)) * HD;
-#pragma unroll
-        for (int kk = 0; kk < MT; ++kk) {
-            const int d0 = 16 * kk + 2 * t;
-            if (hh < G) {
-                const float2 a = *reinterpret_cast<const float2 *>(qr + d0);
-                const float2 b = *reinterpret_cast<const float2 *>(qr + d0 + 8);
-                qb[kk][0] = pack_half2(a.x, a.y);
-                qb[kk][1] = pack_half2(b.x, b.y);
-            } else {
-                qb[kk][0] = 0u;
-                qb[kk][1] = 0u;
-            }
-        }
+        const float sc = (hh < G) ? 1.0f : 0.0f;
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
             float ps = 0.0f;
 #pragma unroll
-            for (int kk = 2 * b; kk < 2 * b + 2; ++kk)
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&qb[kk][j]));
-                    ps += f.x + f.y;
-                }
+            for (int hi = 0; hi < 2; ++hi) {
+                const float f = hi ? 0.0625f : 1.0f;
+                const float *qb0 = qr + 32 * b + 16 * hi;
+                const __half2 x0 = __floats2half2_rn(sc * f * qb0[q4k_elem(b, t, 0)],
+                                                     sc * f * qb0[q4k_elem(b, t, 2)]);
+                const __half2 x1 = __floats2half2_rn(sc * f * qb0[q4k_elem(b, t, 1)],
+                                                     sc * f * qb0[q4k_elem(b, t, 3)]);
+                qb[2 * b + hi][0] = *reinterpret_cast<const uint32_t *>(&x0);
+                qb[2 * b + hi][1] = *reinterpret_cast<const uint32_t *>(&x1);
+                const float2 f0 = __half22float2(x0), f1 = __half22float2(x1);
+                ps += (hi ? -1152.0f : -1032.0f) * ((f0.x + f0.y) + (f1.x + f1.y));
+            }
             ps += __shfl_xor_sync(0xffffffffu, ps, 1);
-            ps += __shfl_xor_sync(0xffffffffu, ps, 2);  // head r's block sum
-            bias[b][0] = -1032.0f * __shfl_sync(0xffffffffu, ps, (2 * t) * 4);
-            bias[b][1] = -1032.0f * __shfl_sync(0xffffffffu, ps, (2 * t + 1) * 4);
+            ps += __shfl_xor_sync(0xffffffffu, ps, 2);  // head r's block bias
+            bias[b][0] = __shfl_sync(0xffffffffu, ps, (2 * t) * 4);
+            bias[b][1] = __shfl_sync(0xffffffffu, ps, (2 * t + 1) * 4);
         }
     }
 
@@ -578,11 +596,12 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
     float m_used[1][2] = {{-INFINITY, -INFINITY}}, m_true[1][2] = {{-INFINITY, -INFINITY}};
     float lsum[1][2] = {{0.0f, 0.0f}};
 
-    // pipeline: stage s holds tile tiles[s] (ntiles = none)
-    int tiles[kStages];
+    // stage s holds tile tiles[s] of this warp's sequence (ntiles = none);
+    // the sequence is consumed in order, stage after stage
+    int tiles[NST];
     int issued = next_tile(warp);
 #pragma unroll
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < NST; ++s) {
         tiles[s] = issued;
         if (issued < ntiles) {
             if (lane == 0) issue(issued, s);
@@ -590,8 +609,9 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
         }
     }
     uint32_t phase = 0;
-    int s = 0;
     bool ok = true;
+    int s = 0;
+#pragma unroll 1
     while (tiles[s] < ntiles) {
         const int i = tiles[s];
         ok = mbar_wait(&bars[s], (phase >> s) & 1u, abort, P.err);
@@ -602,25 +622,41 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
         const uint8_t *Vs = Ks + C::TILE_ALLOC;
         const int t0 = k_lo + kTileKeys * i;
 
-        // ---- scores of the 32 keys: half h2 holds keys t0 + 16 h2 + {r, r+8}
-        float sc[2][4];
-#pragma unroll
+        // ---- scores: half h2 holds keys t0 + 16 h2 + {r, r+8}
+        float sc0[4], sc1[4];
+#pragma unroll 1
         for (int h2 = 0; h2 < 2; ++h2) {
             const uint8_t *KA = Ks + (16 * h2 + r) * ROWB;
             const uint8_t *KB = KA + 8 * ROWB;
             float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
-                const uint32_t dA = lds_u16(KA + kQ4BlockBytes * b);
-                const uint32_t dB = lds_u16(KB + kQ4BlockBytes * b);
-                const uint32_t xA0 = __byte_perm(lds_u16(KA + kQ4BlockBytes * b + 2 + 2 * t), 0u, 0x4140);
-                const uint32_t xA1 = __byte_perm(lds_u16(KA + kQ4BlockBytes * b + 10 + 2 * t), 0u, 0x4140);
-                const uint32_t xB0 = __byte_perm(lds_u16(KB + kQ4BlockBytes * b + 2 + 2 * t), 0u, 0x4140);
-                const uint32_t xB1 = __byte_perm(lds_u16(KB + kQ4BlockBytes * b + 10 + 2 * t), 0u, 0x4140);
-                const uint32_t alo[4] = {nib_lo(xA0), nib_lo(xB0), nib_lo(xA1), nib_lo(xB1)};
-                const uint32_t ahi[4] = {nib_hi(xA0), nib_hi(xB0), nib_hi(xA1), nib_hi(xB1)};
-                float acc[4] = {bias[b][0], bias[b][1], bias[b][0], bias[b][1]};
-                mma_16816(acc, alo, qb[2 * b]);
+                const int o18 = kQ4BlockBytes * b;
+                uint32_t wA, wB, dA, dB;
+                if ((b & 1) == 0) {
+                    const uint32_t a0 = *reinterpret_cast<const uint32_t *>(KA + o18 + 4 + 4 * t);
+                    const uint32_t a1 = *reinterpret_cast<const uint32_t *>(KA + o18);
+                    const uint32_t b0 = *reinterpret_cast<const uint32_t *>(KB + o18 + 4 + 4 * t);
+                    const uint32_t b1 = *reinterpret_cast<const uint32_t *>(KB + o18);
+                    const uint32_t sel = (t == 3) ? 0x7610u : 0x3210u;
+                    wA = __byte_perm(a0, a1, sel);
+                    wB = __byte_perm(b0, b1, sel);
+                    dA = a1 & 0xFFFFu;
+                    dB = b1 & 0xFFFFu;
+                } else {
+                    wA = *reinterpret_cast<const uint32_t *>(KA + o18 + 2 + 4 * t);
+                    wB = *reinterpret_cast<const uint32_t *>(KB + o18 + 2 + 4 * t);
+                    dA = *reinterpret_cast<const uint16_t *>(KA + o18);
+                    dB = *reinterpret_cast<const uint16_t *>(KB + o18);
+                }
+                const uint32_t wA8 = wA >> 8, wB8 = wB >> 8;
+                const uint32_t alo[4] = {(wA & 0x000F000Fu) | kMagic, (wB & 0x000F000Fu) | kMagic,
+                                         (wA8 & 0x000F000Fu) | kMagic, (wB8 & 0x000F000Fu) | kMagic};
+                const uint32_t ahi[4] = {(wA & 0x00F000F0u) | kMagic, (wB & 0x00F000F0u) | kMagic,
+                                         (wA8 & 0x00F000F0u) | kMagic, (wB8 & 0x00F000F0u) | kMagic};
+                const float cb[4] = {bias[b][0], bias[b][1], bias[b][0], bias[b][1]};
+                float acc[4];
+                mma_16816_c(acc, alo, qb[2 * b], cb);
                 mma_16816(acc, ahi, qb[2 * b + 1]);
                 const float fA = __half2float(__ushort_as_half(static_cast<uint16_t>(dA)));
                 const float fB = __half2float(__ushort_as_half(static_cast<uint16_t>(dB)));
@@ -630,55 +666,84 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
                 s4[3] = fmaf(fB, acc[3], s4[3]);
             }
 #pragma unroll
-            for (int k = 0; k < 4; ++k) sc[h2][k] = s4[k];
+            for (int k = 0; k < 4; ++k) {
+                if (h2 == 0) sc0[k] = s4[k];
+                else sc1[k] = s4[k];
+            }
         }
-        // ---- mask and fold: key of score sc[h2][k] is t0 + 16 h2 + r + 8 (k >> 1)
+        // ---- mask and fold: sv[hh][2 h2 + half] is key t0 + 16 h2 + r + 8 half.
+        // Most tiles are wholly in range, visible and free of shadow keys.
+        const int t1 = t0 + kTileKeys - 1;
+        const bool whole = t1 < k_hi && t0 >= ss && (sw <= 0 || t1 <= p - sw) &&
+                           (P.win <= 0 || t0 >= p - P.win + 1);
         float sv[2][4], pv[2][4];
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 const int key = t0 + 16 * h2 + r + 8 * half;
-                const bool vis = key < k_hi && key_visible(p, key, P.sink, P.win) &&
-                                 !(key < ss || (sw > 0 && key > p - sw));
+                const bool vis = whole || (key < k_hi && key_visible(p, key, P.sink, P.win) &&
+                                           !(key < ss || (sw > 0 && key > p - sw)));
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh)
-                    sv[hh][2 * h2 + half] = vis ? sc[h2][2 * half + hh] : -INFINITY;
+                    sv[hh][2 * h2 + half] = vis ? (h2 ? sc1 : sc0)[2 * half + hh] : -INFINITY;
             }
         fold_scores<MT, 1, 4>(sv, P.sl2, kRescaleQ4, m_used[0][0], m_used[0][1], m_true[0][0],
                               m_true[0][1], lsum[0][0], lsum[0][1], o, 0, pv);
+        // P^T B fragments of both halves: keys 2t,2t+1 (b0) and 2t+8,2t+9 (b1) of head r
+        const uint32_t pbA0 = movmatrix_trans(pack_half2(pv[0][0], pv[1][0]));
+        const uint32_t pbA1 = movmatrix_trans(pack_half2(pv[0][1], pv[1][1]));
+        const uint32_t pbB0 = movmatrix_trans(pack_half2(pv[0][2], pv[1][2]));
+        const uint32_t pbB1 = movmatrix_trans(pack_half2(pv[0][3], pv[1][3]));
 
-        // ---- O^T += V^T P'^T per 16-key half
-#pragma unroll
+        // ---- O^T += V^T P'^T per 16-key half; thread group r owns elements
+        // 2r, 2r+1 (m-tile 2b) and 16+2r, 17+2r (m-tile 2b+1) of block b.
+#pragma unroll 1
         for (int h2 = 0; h2 < 2; ++h2) {
-            // P^T B fragments: keys 2t,2t+1 (b0) and 2t+8,2t+9 (b1) of head r
-            const uint32_t pb0 = movmatrix_trans(pack_half2(pv[0][2 * h2], pv[1][2 * h2]));
-            const uint32_t pb1 = movmatrix_trans(pack_half2(pv[0][2 * h2 + 1], pv[1][2 * h2 + 1]));
-            const uint8_t *V0 = Vs + (16 * h2 + 2 * t) * ROWB;   // key 2t
-            const uint8_t *V1 = V0 + ROWB;                       // key 2t+1
-            const uint8_t *V2 = V0 + 8 * ROWB;                   // key 2t+8
-            const uint8_t *V3 = V2 + ROWB;                       // key 2t+9
+            const uint32_t pb0 = h2 ? pbB0 : pbA0;
+            const uint32_t pb1 = h2 ? pbB1 : pbA1;
+            const uint8_t *R0 = Vs + (16 * h2 + 2 * t) * ROWB;   // key 2t
+            const uint8_t *R1 = R0 + ROWB;                       // key 2t+1
+            const uint8_t *R2 = R0 + 8 * ROWB;                   // key 2t+8
+            const uint8_t *R3 = R2 + ROWB;                       // key 2t+9
             const int kb = t0 + 16 * h2 + 2 * t;
             // a key past the range has P = 0; force its scale to 0 so that no
             // stale or uninitialised bytes can turn 0 * d into NaN
-            const uint32_t mask01 = (kb < k_hi ? 0x0000FFFFu : 0u) | (kb + 1 < k_hi ? 0xFFFF0000u : 0u);
-            const uint32_t mask23 = (kb + 8 < k_hi ? 0x0000FFFFu : 0u) | (kb + 9 < k_hi ? 0xFFFF0000u : 0u);
+            const uint32_t mask01 =
+                (kb < k_hi ? 0x0000FFFFu : 0u) | (kb + 1 < k_hi ? 0xFFFF0000u : 0u);
+            const uint32_t mask23 =
+                (kb + 8 < k_hi ? 0x0000FFFFu : 0u) | (kb + 9 < k_hi ? 0xFFFF0000u : 0u);
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
-                const int off = kQ4BlockBytes * b;
-                const uint32_t d01 = __byte_perm(lds_u16(V0 + off), lds_u16(V1 + off), 0x5410) & mask01;
-                const uint32_t d23 = __byte_perm(lds_u16(V2 + off), lds_u16(V3 + off), 0x5410) & mask23;
+                const int o18 = kQ4BlockBytes * b;
+                const uint32_t d01 = __byte_perm(*reinterpret_cast<const uint16_t *>(R0 + o18),
+                                                 *reinterpret_cast<const uint16_t *>(R1 + o18),
+                                                 0x5410) & mask01;
+                const uint32_t d23 = __byte_perm(*reinterpret_cast<const uint16_t *>(R2 + o18),
+                                                 *reinterpret_cast<const uint16_t *>(R3 + o18),
+                                                 0x5410) & mask23;
                 const uint32_t bb[2] = {hmul2u(pb0, d01), hmul2u(pb1, d23)};
-                const uint32_t x01 = __byte_perm(lds_u8(V0 + off + 2 + r), lds_u8(V1 + off + 2 + r), 0x5410);
-                const uint32_t x23 = __byte_perm(lds_u8(V2 + off + 2 + r), lds_u8(V3 + off + 2 + r), 0x5410);
-                const uint32_t y01 = __byte_perm(lds_u8(V0 + off + 10 + r), lds_u8(V1 + off + 10 + r), 0x5410);
-                const uint32_t y23 = __byte_perm(lds_u8(V2 + off + 10 + r), lds_u8(V3 + off + 10 + r), 0x5410);
-                const uint32_t alo[4] = {hsub1032(nib_lo(x01)), hsub1032(nib_lo(y01)),
-                                         hsub1032(nib_lo(x23)), hsub1032(nib_lo(y23))};
-                const uint32_t ahi[4] = {hsub1032(nib_hi(x01)), hsub1032(nib_hi(y01)),
-                                         hsub1032(nib_hi(x23)), hsub1032(nib_hi(y23))};
+                const int oc = o18 + 2 + 2 * r;
+                const uint32_t z01 = __byte_perm(*reinterpret_cast<const uint16_t *>(R0 + oc),
+                                                 *reinterpret_cast<const uint16_t *>(R1 + oc),
+                                                 0x5410);
+                const uint32_t z23 = __byte_perm(*reinterpret_cast<const uint16_t *>(R2 + oc),
+                                                 *reinterpret_cast<const uint16_t *>(R3 + oc),
+                                                 0x5410);
+                const uint32_t y01 = z01 >> 8, y23 = z23 >> 8;
+                // operands 1024 + c (lo nibbles) and 1024 + 16 c (hi nibbles); the
+                // constant operand right after removes 1032 (1152) times the sum of
+                // the block's P' from every row, leaving c - 8 (16 (c - 8)).
+                const uint32_t alo[4] = {(z01 & 0x000F000Fu) | kMagic, (y01 & 0x000F000Fu) | kMagic,
+                                         (z23 & 0x000F000Fu) | kMagic, (y23 & 0x000F000Fu) | kMagic};
+                const uint32_t ahi[4] = {(z01 & 0x00F000F0u) | kMagic, (y01 & 0x00F000F0u) | kMagic,
+                                         (z23 & 0x00F000F0u) | kMagic, (y23 & 0x00F000F0u) | kMagic};
+                const uint32_t nlo[4] = {kHNeg1032, kHNeg1032, kHNeg1032, kHNeg1032};
+                const uint32_t nhi[4] = {kHNeg1152, kHNeg1152, kHNeg1152, kHNeg1152};
                 mma_16816(o[2 * b][0], alo, bb);
-                mma_16816(o[2 * b + 1][0], ahi, bb);
+                mma_16816(o[2 * b][0], nlo, bb);
+                mma_16816(o[2 * b + 1][0], ahi, bb);  // 16 (c - 8): scaled back at the end
+                mma_16816(o[2 * b + 1][0], nhi, bb);
             }
         }
         __syncwarp();
@@ -688,20 +753,23 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
             if (lane == 0) issue(issued, s);
             issued = next_tile(issued + kWarps);
         }
-        s = (s + 1 == kStages) ? 0 : s + 1;
+        s = (s + 1 == NST) ? 0 : s + 1;
     }
     if (!ok) {
         // let the copies already issued land before the shared memory is reused
-        for (int k = 0; k < kStages; ++k) {
-            const int st = (s + k) % kStages;
+#pragma unroll
+        for (int st = 0; st < NST; ++st) {
             if (tiles[st] < ntiles) {
                 const long long c0 = clock64();
                 while (!mbar_try_wait(&bars[st], (phase >> st) & 1u) && clock64() - c0 < kSpinCycles) {
                 }
-                phase ^= 1u << st;
             }
         }
     }
+#pragma unroll
+    for (int mt = 1; mt < MT; mt += 2)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o[mt][0][k] *= 0.0625f;
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
         float v = lsum[0][hh];
@@ -710,11 +778,12 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
         v += __shfl_xor_sync(0xffffffffu, v, 16);
         lsum[0][hh] = v;
     }
-    merge_and_write<HD, 1>(P, dsmem, head0, G, e, m_used, m_true, lsum, o);
+    merge_and_write<HD, 1, true>(P, dsmem, head0, G, e, m_used, m_true, lsum, o);
 }
 
 template <int HD>
-__global__ void __launch_bounds__(kWarps * 32, 2) decode_q4_kernel(const DecodeParams P) {
+__global__ void __launch_bounds__(kWarps * 32, FA_Q4_MIN_BLOCKS)
+    decode_q4_kernel(const DecodeParams P) {
     extern __shared__ __align__(128) uint8_t dsmem[];
     const int e = blockIdx.x, g = blockIdx.y, u = blockIdx.z;
     const int G = P.Hq / P.Hkv;
