@@ -427,8 +427,7 @@ def main():
     value = world * flops_step / (ms * 1e-3) / 1e12
     kms = statistics.mean(kern_ms)
     achieved = flops_step / (kms * 1e-3) / 1e12
-    traffic = profiled_traffic("prefill_tc_kernel<256>", src_hash("prefill_tc.cu",
-                                                                   "fa_device.cuh"))
+    traffic = profiled_traffic("prefill_tc_kernel<256>", src_hash("prefill_tc.cu"))
     roofline = {"kernel": "prefill_tc_kernel<256>", "bound": "tensor", "achieved": achieved,
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
