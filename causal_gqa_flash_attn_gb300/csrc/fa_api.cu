@@ -80,14 +80,16 @@ fa_status check_shadow(int kv_fmt, int shadow_sink, int shadow_win) {
     return FA_OK;
 }
 
-// fp16 staging for prefill: Q [n][Hq][hd], K and V [Hkv][n][hd].
+// Prefill workspace: a 256-byte header holding the kernel's work counter,
+// then the fp16 staging of Q [n][Hq][hd], K and V [Hkv][n][hd].
 struct PrefillWs {
-    size_t q_off, k_off, v_off, bytes;
+    size_t ctr_off, q_off, k_off, v_off, bytes;
 };
 PrefillWs prefill_ws(int n, int hq, int hkv, int hd) {
     PrefillWs w;
-    w.q_off = 0;
-    w.k_off = up256(static_cast<size_t>(n) * hq * hd * 2);
+    w.ctr_off = 0;
+    w.q_off = 256;
+    w.k_off = w.q_off + up256(static_cast<size_t>(n) * hq * hd * 2);
     const size_t kv = up256(static_cast<size_t>(hkv) * n * hd * 2);
     w.v_off = w.k_off + kv;
     w.bytes = w.v_off + kv;
@@ -234,8 +236,9 @@ fa_status fa_prefill(const float *q, const void *k, const void *v, float *out, i
     __half *qh = reinterpret_cast<__half *>(ws + w.q_off);
     __half *kh = reinterpret_cast<__half *>(ws + w.k_off);
     __half *vh = reinterpret_cast<__half *>(ws + w.v_off);
+    unsigned *ctr = reinterpret_cast<unsigned *>(ws + w.ctr_off);
     cudaError_t e =
-        fa::launch_stage_q(q, qh, static_cast<size_t>(n) * n_q_heads * head_dim, s);
+        fa::launch_stage_q(q, qh, static_cast<size_t>(n) * n_q_heads * head_dim, ctr, s);
     if (e == cudaSuccess)
         e = fa::launch_stage_kv(static_cast<const uint8_t *>(k), kh, n, g, shadow_sink,
                                 shadow_win, s);
@@ -249,6 +252,7 @@ fa_status fa_prefill(const float *q, const void *k, const void *v, float *out, i
     a.vh = vh;
     a.out = out;
     a.tile_map = tile_map;
+    a.work_counter = ctr;
     a.n = n;
     a.n_q_heads = n_q_heads;
     a.n_kv_heads = n_kv_heads;

@@ -41,7 +41,9 @@ cudaError_t launch_kv_append(const float *k_new, const float *v_new, uint8_t *k_
                              unsigned *err, cudaStream_t stream);
 
 // ---- prefill_stage.cu: fp16 staging of Q and of the K/V rows a prefill reads
-cudaError_t launch_stage_q(const float *q, __half *qh, size_t count, cudaStream_t stream);
+// Converts q and zeroes *counter (the prefill kernel's work queue).
+cudaError_t launch_stage_q(const float *q, __half *qh, size_t count, unsigned *counter,
+                           cudaStream_t stream);
 cudaError_t launch_stage_kv(const uint8_t *plane, __half *dst, int n, const PlaneGeom &g,
                             int shadow_sink, int shadow_win, cudaStream_t stream);
 
@@ -52,6 +54,7 @@ struct PrefillArgs {
     const __half *vh;   // [Hkv][n][hd] fp16
     float *out;         // [n][Hq][hd] fp32
     uint8_t *tile_map;  // optional
+    unsigned *work_counter;  // prefill work queue, zeroed by launch_stage_q
     int n, n_q_heads, n_kv_heads, head_dim, sink, win;
     float scale;
 };

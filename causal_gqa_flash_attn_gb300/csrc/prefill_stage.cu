@@ -22,7 +22,9 @@ namespace {
 constexpr int kThreads = 256;
 
 __global__ void __launch_bounds__(kThreads)
-    stage_q_kernel(const float4 *__restrict__ q, uint2 *__restrict__ qh, long long count4) {
+    stage_q_kernel(const float4 *__restrict__ q, uint2 *__restrict__ qh, long long count4,
+                   unsigned *counter) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) *counter = 0u;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < count4;
          i += static_cast<long long>(gridDim.x) * blockDim.x) {
         const float4 x = __ldg(q + i);
@@ -111,10 +113,12 @@ int grid_for(long long items) {
 
 }  // namespace
 
-cudaError_t launch_stage_q(const float *q, __half *qh, size_t count, cudaStream_t stream) {
+cudaError_t launch_stage_q(const float *q, __half *qh, size_t count, unsigned *counter,
+                           cudaStream_t stream) {
     const long long c4 = static_cast<long long>(count / 4);
     stage_q_kernel<<<grid_for(c4), kThreads, 0, stream>>>(reinterpret_cast<const float4 *>(q),
-                                                           reinterpret_cast<uint2 *>(qh), c4);
+                                                           reinterpret_cast<uint2 *>(qh), c4,
+                                                           counter);
     return cudaGetLastError();
 }
 

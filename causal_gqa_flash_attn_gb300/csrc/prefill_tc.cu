@@ -45,7 +45,10 @@ struct Cfg {
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_K = TILE_BYTES;
     static constexpr uint32_t OFF_V = OFF_K + NS * TILE_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_V + NS * TILE_BYTES;
+    // epilogue staging: per softmax warp two boxes of [32 rows][32 fp32]
+    static constexpr uint32_t OFF_OST = OFF_V + NS * TILE_BYTES;
+    static constexpr uint32_t OST_BYTES = 32 * 128;
+    static constexpr uint32_t OFF_BAR = OFF_OST + 4 * 2 * OST_BYTES;
     static constexpr uint32_t USED = OFF_BAR + 256;
     // at least 120 KB so that one block owns an SM (and all 512 TMEM columns)
     static constexpr uint32_t SMEM = (USED + 1024 > 120u * 1024u) ? USED + 1024 : 120u * 1024u;
@@ -58,8 +61,13 @@ struct Cfg {
     static_assert(USED + 1024 <= 227u * 1024u, "shared memory");
 };
 
+constexpr int kUnitRing = 4;
+
 struct Bars {
-    uint64_t q_full;
+    uint64_t q_full, q_empty;
+    uint64_t o_free;
+    uint64_t unit_full[kUnitRing], unit_empty[kUnitRing];
+    int unit_id[kUnitRing];
     uint64_t k_full[2], k_empty[2];
     uint64_t v_full[2], v_empty[2];
     uint64_t s_full[2], p_full[2];
@@ -111,13 +119,24 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
         if (clock64() - t0 > kSpinCycles) return;
 }
 
+// Work unit w (heaviest first): query tile nqt-1-w/Hq of q head w%Hq. Block b
+// starts with unit b; afterwards its producer warp takes the next unit from a
+// global counter (zeroed by the staging kernel that runs first) and hands the
+// id to the MMA and softmax warps through a small ring in shared memory. Each
+// unit is computed by exactly one block, so the result does not depend on the
+// schedule.
+struct Unit {
+    int qt, h;
+};
+
 template <int HD>
 __global__ void __launch_bounds__(256, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, float *__restrict__ out,
-                      uint8_t *__restrict__ tile_map, int n, int Hq, int Hkv, int sink, int win,
-                      float sl2, unsigned *err) {
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_o, uint8_t *__restrict__ tile_map,
+                      unsigned *__restrict__ work_counter, int n, int Hq, int Hkv, int sink,
+                      int win, float sl2, unsigned *err) {
     using C = Cfg<HD>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -128,16 +147,22 @@ __global__ void __launch_bounds__(256, 1)
 
     const int nqt = (n + C::BQ - 1) / C::BQ;
     const int nkt = (n + C::BK - 1) / C::BK;
-    const int qt = nqt - 1 - static_cast<int>(blockIdx.x / Hq);  // heaviest first
-    const int h = static_cast<int>(blockIdx.x % Hq);
-    const int g = h / (Hq / Hkv);
-    const int p0 = qt * C::BQ;
-    const int p1 = min(n, p0 + C::BQ) - 1;
-    const TilePlan plan = tile_plan(p0, p1, sink, win, C::BK);
-    const int count = plan.count;
+    const int n_units = nqt * Hq;
+    const int G = gridDim.x;
+    volatile int *abort_flag = nullptr;  // set below
+    // j-th unit of this block, read from the ring (consumers) after the
+    // producer published it; false at the end of the work (or on abort).
+    auto to_unit = [&](int w, Unit *u) -> bool {
+        if (w < 0 || w >= n_units) return false;
+        u->qt = nqt - 1 - w / Hq;
+        u->h = w % Hq;
+        return true;
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, 1);
+        mbar_init(&bars->q_empty, 1);
+        mbar_init(&bars->o_free, 128);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars->k_full[s], 1);
             mbar_init(&bars->k_empty[s], 1);
@@ -148,11 +173,16 @@ __global__ void __launch_bounds__(256, 1)
         }
         mbar_init(&bars->o_done, 1);
         mbar_init(&bars->drain, 1);
+        for (int k = 0; k < kUnitRing; ++k) {
+            mbar_init(&bars->unit_full[k], 1);
+            mbar_init(&bars->unit_empty[k], 1 + 4);  // MMA thread + 4 softmax warps
+        }
         bars->abort = 0;
         mbar_fence_init();
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_o);
     }
     if (warp == 1) {
         tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
@@ -163,54 +193,83 @@ __global__ void __launch_bounds__(256, 1)
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     volatile int *abort = &bars->abort;
+    abort_flag = abort;
+    // consumer side of the unit ring: wait for slot j and read the unit id
+    auto next_unit = [&](int j, Unit *u, bool arrive_one) -> bool {
+        const int slot = j % kUnitRing;
+        if (!mbar_wait(&bars->unit_full[slot], (j / kUnitRing) & 1, abort_flag, err)) return false;
+        const int w = *reinterpret_cast<volatile int *>(&bars->unit_id[slot]);
+        if (arrive_one) mbar_arrive(&bars->unit_empty[slot]);
+        return to_unit(w, u);
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------- TMA producer
         if (lane == 0) {
-            int k_arms[2] = {0, 0}, v_arms[2] = {0, 0};
-            mbar_arrive_expect_tx(&bars->q_full, C::TILE_BYTES);
-            for (int c = 0; c < C::NCHUNK; ++c)
-                tma_load_3d(smem + C::OFF_Q + c * C::CHUNK_BYTES, &tm_q, &bars->q_full, c * 64, h,
-                            p0);
+            int k_arms[2] = {0, 0}, v_arms[2] = {0, 0}, q_arms = 0;
+            int t = 0;  // global tile index of this block
             bool ok = true;
-            auto load_k = [&](int i) -> bool {
-                const int st = i % C::NS;
-                if (i >= C::NS &&
-                    !mbar_wait(&bars->k_empty[st], ((i / C::NS) - 1) & 1, abort, err))
-                    return false;
-                const int kt = plan.kt(i);
-                mbar_arrive_expect_tx(&bars->k_full[st], C::TILE_BYTES);
+            Unit u;
+            for (int j = 0; ok; ++j) {
+                // take the next unit and publish it to the other warps
+                const int w = (j == 0) ? static_cast<int>(blockIdx.x)
+                                       : G + static_cast<int>(atomicAdd(work_counter, 1u));
+                const int slot = j % kUnitRing;
+                if (j >= kUnitRing &&
+                    !mbar_wait(&bars->unit_empty[slot], ((j / kUnitRing) - 1) & 1, abort, err)) {
+                    ok = false;
+                    break;
+                }
+                bars->unit_id[slot] = w;
+                mbar_arrive(&bars->unit_full[slot]);
+                if (!to_unit(w, &u)) break;
+                const int p0 = u.qt * C::BQ, p1 = min(n, p0 + C::BQ) - 1;
+                const int g = u.h / (Hq / Hkv);
+                const TilePlan plan = tile_plan(p0, p1, sink, win, C::BK);
+                // the Q buffer is free once the previous unit's last QK^T completed
+                if (j > 0 && !mbar_wait(&bars->q_empty, (j - 1) & 1, abort, err)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&bars->q_full, C::TILE_BYTES);
                 for (int c = 0; c < C::NCHUNK; ++c)
-                    tma_load_3d(smem + C::OFF_K + st * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k,
-                                &bars->k_full[st], c * 64, kt * C::BK, g);
-                ++k_arms[st];
-                if (tile_map) tile_map[static_cast<size_t>(qt) * nkt + kt] = 1;
-                return true;
-            };
-            auto load_v = [&](int i) -> bool {
-                const int st = i % C::NS;
-                if (i >= C::NS &&
-                    !mbar_wait(&bars->v_empty[st], ((i / C::NS) - 1) & 1, abort, err))
-                    return false;
-                const int kt = plan.kt(i);
-                mbar_arrive_expect_tx(&bars->v_full[st], C::TILE_BYTES);
-                for (int c = 0; c < C::NCHUNK; ++c)
-                    tma_load_3d(smem + C::OFF_V + st * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v,
-                                &bars->v_full[st], c * 64, kt * C::BK, g);
-                ++v_arms[st];
-                return true;
-            };
-            // Consumption order of the MMA warp: K0, K1, V0, K2, V1, ...
-            for (int i = 0; i < count && ok; ++i) {
-                ok = load_k(i);
-                if (ok && i >= 1) ok = load_v(i - 1);
+                    tma_load_3d(smem + C::OFF_Q + c * C::CHUNK_BYTES, &tm_q, &bars->q_full, c * 64,
+                                u.h, p0);
+                ++q_arms;
+                auto load = [&](int i, bool is_k) -> bool {
+                    const int tt = t + i;
+                    const int st = tt % C::NS;
+                    uint64_t *empty = is_k ? &bars->k_empty[st] : &bars->v_empty[st];
+                    uint64_t *full = is_k ? &bars->k_full[st] : &bars->v_full[st];
+                    if (tt >= C::NS && !mbar_wait(empty, ((tt / C::NS) - 1) & 1, abort, err))
+                        return false;
+                    const int kt = plan.kt(i);
+                    mbar_arrive_expect_tx(full, C::TILE_BYTES);
+                    const uint32_t base = (is_k ? C::OFF_K : C::OFF_V) + st * C::TILE_BYTES;
+                    for (int c = 0; c < C::NCHUNK; ++c)
+                        tma_load_3d(smem + base + c * C::CHUNK_BYTES, is_k ? &tm_k : &tm_v, full,
+                                    c * 64, kt * C::BK, g);
+                    if (is_k) {
+                        ++k_arms[st];
+                        if (tile_map) tile_map[static_cast<size_t>(u.qt) * nkt + kt] = 1;
+                    } else {
+                        ++v_arms[st];
+                    }
+                    return true;
+                };
+                // consumption order of the MMA warp: K0, K1, V0, K2, V1, ..., V(n-1)
+                for (int i = 0; i < plan.count && ok; ++i) {
+                    ok = load(i, true);
+                    if (ok && i >= 1) ok = load(i - 1, false);
+                }
+                if (ok) ok = load(plan.count - 1, false);
+                t += plan.count;
             }
-            if (ok) ok = load_v(count - 1);
             if (!ok) {  // let every copy already issued land before exit
-                drain_wait(&bars->q_full, 0);
-                for (int s = 0; s < 2; ++s) {
-                    if (k_arms[s]) drain_wait(&bars->k_full[s], (k_arms[s] - 1) & 1);
-                    if (v_arms[s]) drain_wait(&bars->v_full[s], (v_arms[s] - 1) & 1);
+                if (q_arms) drain_wait(&bars->q_full, (q_arms - 1) & 1);
+                for (int s2 = 0; s2 < 2; ++s2) {
+                    if (k_arms[s2]) drain_wait(&bars->k_full[s2], (k_arms[s2] - 1) & 1);
+                    if (v_arms[s2]) drain_wait(&bars->v_full[s2], (v_arms[s2] - 1) & 1);
                 }
             }
         }
@@ -220,164 +279,221 @@ __global__ void __launch_bounds__(256, 1)
             const uint32_t sQ = smem_u32(smem + C::OFF_Q);
             const uint32_t sK = smem_u32(smem + C::OFF_K);
             const uint32_t sV = smem_u32(smem + C::OFF_V);
-            auto issue_qk = [&](int i) -> bool {
-                const int st = i % C::NS;
-                if (!mbar_wait(&bars->k_full[st], (i / C::NS) & 1, abort, err)) return false;
+            auto issue_qk = [&](int tt) -> bool {
+                const int st = tt % C::NS;
+                if (!mbar_wait(&bars->k_full[st], (tt / C::NS) & 1, abort, err)) return false;
                 tc_fence_after();
-                const uint32_t d = tmem + ((i & 1) ? C::S_COL1 : C::S_COL0);
+                const uint32_t d = tmem + ((tt & 1) ? C::S_COL1 : C::S_COL0);
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
                     const uint64_t a = desc_sw128(sQ + off, 16, 1024);
-                    const uint64_t b = desc_sw128(sK + st * C::TILE_BYTES + off, 16, 1024);
-                    mma_ss(d, a, b, C::IDESC_QK, kk > 0 ? 1u : 0u);
+                    const uint64_t bd = desc_sw128(sK + st * C::TILE_BYTES + off, 16, 1024);
+                    mma_ss(d, a, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(&bars->k_empty[st]);
-                tc_commit(&bars->s_full[i & 1]);
+                tc_commit(&bars->s_full[tt & 1]);
                 return true;
             };
-            auto issue_pv = [&](int j) -> bool {
-                const int st = j % C::NS;
-                if (!mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1, abort, err)) return false;
-                if (!mbar_wait(&bars->v_full[st], (j / C::NS) & 1, abort, err)) return false;
+            // PV of global tile tt; `first` starts a fresh O for the unit
+            auto issue_pv = [&](int tt, bool first) -> bool {
+                const int st = tt % C::NS;
+                if (!mbar_wait(&bars->p_full[tt & 1], (tt >> 1) & 1, abort, err)) return false;
+                if (!mbar_wait(&bars->v_full[st], (tt / C::NS) & 1, abort, err)) return false;
                 tc_fence_after();
-                const uint32_t pcol = tmem + ((j & 1) ? C::S_COL1 : C::S_COL0);
+                const uint32_t pcol = tmem + ((tt & 1) ? C::S_COL1 : C::S_COL0);
 #pragma unroll
                 for (int kk = 0; kk < C::BK / 16; ++kk) {
                     // V tile: [128 keys][64 dims] per 16-KB chunk; 16 keys per k-step,
                     // next 64 dims of N one chunk further (LBO), 8-key atoms 1 KB apart (SBO).
-                    const uint64_t b = desc_sw128(sV + st * C::TILE_BYTES + kk * 2048,
-                                                  C::CHUNK_BYTES, 1024);
-                    mma_ts(tmem + C::O_COL, pcol + kk * 8, b, C::IDESC_PV,
-                           (j > 0 || kk > 0) ? 1u : 0u);
+                    const uint64_t bd = desc_sw128(sV + st * C::TILE_BYTES + kk * 2048,
+                                                   C::CHUNK_BYTES, 1024);
+                    mma_ts(tmem + C::O_COL, pcol + kk * 8, bd, C::IDESC_PV,
+                           (!first || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(&bars->v_empty[st]);
                 tc_commit(&bars->o_done);
                 return true;
             };
-            bool ok = mbar_wait(&bars->q_full, 0, abort, err);
-            if (ok) tc_fence_after();
-            for (int i = 0; i < count && ok; ++i) {
-                ok = issue_qk(i);
-                if (ok && i >= 1) ok = issue_pv(i - 1);
+            int t = 0;
+            bool ok = true;
+            Unit u;
+            for (int j = 0; ok && next_unit(j, &u, true); ++j) {
+                const int p0 = u.qt * C::BQ, p1 = min(n, p0 + C::BQ) - 1;
+                const int count = tile_plan(p0, p1, sink, win, C::BK).count;
+                ok = mbar_wait(&bars->q_full, j & 1, abort, err);
+                if (!ok) break;
+                tc_fence_after();
+                for (int i = 0; i < count && ok; ++i) {
+                    ok = issue_qk(t + i);
+                    if (ok && i == count - 1) tc_commit(&bars->q_empty);  // Q read for the last time
+                    if (ok && i >= 1) {
+                        // the first P.V of a unit overwrites O: the epilogue of the
+                        // previous unit must have read it
+                        if (i == 1 && j > 0) {
+                            ok = mbar_wait(&bars->o_free, (j - 1) & 1, abort, err);
+                            if (ok) tc_fence_after();
+                        }
+                        if (ok) ok = issue_pv(t + i - 1, i == 1);
+                    }
+                }
+                if (ok && count == 1 && j > 0) {
+                    ok = mbar_wait(&bars->o_free, (j - 1) & 1, abort, err);
+                    if (ok) tc_fence_after();
+                }
+                if (ok) ok = issue_pv(t + count - 1, count == 1);
+                t += count;
             }
-            if (ok) ok = issue_pv(count - 1);
             // every MMA issued must complete before TMEM is released
             tc_commit(&bars->drain);
             drain_wait(&bars->drain, 0);
         }
     } else if (warp >= 4) {
-        // ----------------------------------------------------------- softmax
+        // ----------------------------------------------- softmax and epilogue
         const int r = threadIdx.x - 128;  // tile row == TMEM lane
-        const int p = p0 + r;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        float m_used = -INFINITY;  // exp2-domain reference shared by O and l
-        float l = 0.0f;
+        int t = 0;
+        int stores = 0;  // TMA stores issued by this warp's lane 0
         bool ok = true;
-        for (int i = 0; i < count; ++i) {
-            const int b = i & 1;
-            ok = mbar_wait(&bars->s_full[b], (i >> 1) & 1, abort, err);
+        Unit u;
+        for (int j = 0; ok; ++j) {
+            const bool have = next_unit(j, &u, false);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->unit_empty[j % kUnitRing]);
+            if (!__all_sync(0xffffffffu, have)) break;
+            const int p0 = u.qt * C::BQ, p1 = min(n, p0 + C::BQ) - 1;
+            const int p = p0 + r;
+            const TilePlan plan = tile_plan(p0, p1, sink, win, C::BK);
+            float m_used = -INFINITY;  // exp2-domain reference shared by O and l
+            float l = 0.0f;
+            for (int i = 0; i < plan.count; ++i) {
+                const int tt = t + i;
+                const int bsel = tt & 1;
+                ok = mbar_wait(&bars->s_full[bsel], (tt >> 1) & 1, abort, err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t scol = tmem + lane_base + (bsel ? C::S_COL1 : C::S_COL0);
+                uint32_t s[128];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(scol + 32 * c, s + 32 * c);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) reg_fence32(s + 32 * c);
+
+                const int kt = plan.kt(i);
+                const int j0 = kt * C::BK;
+                float mx = -INFINITY;
+                if (tile_full(kt, p0, p1, sink, win, C::BK)) {
+#pragma unroll
+                    for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+                } else {
+                    // key j0 + c is visible iff c <= hi and (c >= lo or c < sk)
+                    const int hi = p - j0;
+                    const int lo = win > 0 ? p - win + 1 - j0 : -1;
+                    const int sk = win > 0 ? sink - j0 : -1;
+#pragma unroll
+                    for (int c = 0; c < 128; ++c) {
+                        const bool vis = (c <= hi) & ((c >= lo) | (c < sk));
+                        const float v = vis ? __uint_as_float(s[c]) : -INFINITY;
+                        s[c] = __float_as_uint(v);
+                        mx = fmaxf(mx, v);
+                    }
+                }
+                const float m_new = fmaxf(m_used, mx * sl2);
+                float corr = 1.0f;
+                bool resc = false;
+                if (m_new > m_used + 8.0f) {
+                    if (m_used != -INFINITY) {
+                        corr = ex2(m_used - m_new);
+                        resc = true;
+                        l *= corr;
+                    }
+                    m_used = m_new;
+                }
+                const float mref = (m_used == -INFINITY) ? 0.0f : m_used;
+                uint32_t pk[64];
+                float rs = 0.0f;
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    const float a = ex2(fmaf(__uint_as_float(s[2 * c]), sl2, -mref));
+                    const float bq = ex2(fmaf(__uint_as_float(s[2 * c + 1]), sl2, -mref));
+                    rs += a + bq;
+                    pk[c] = pack_half2(a, bq);
+                }
+                l += rs;
+                if (i > 0) {  // O must hold PV(tt-1) before it is rescaled and before P lands
+                    ok = mbar_wait(&bars->o_done, (tt - 1) & 1, abort, err);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                }
+                tc_fence_after();
+                __syncwarp();
+                if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+                    for (int c = 0; c < HD / 32; ++c) {
+                        uint32_t o[32];
+                        const uint32_t oc = tmem + lane_base + C::O_COL + 32 * c;
+                        tmem_ld32(oc, o);
+                        tmem_wait_ld();
+                        reg_fence32(o);
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            o[k] = __float_as_uint(__uint_as_float(o[k]) * corr);
+                        tmem_st32(oc, o);
+                    }
+                }
+                tmem_st32(scol, pk);
+                tmem_st32(scol + 32, pk + 32);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&bars->p_full[bsel]);
+            }
+            if (!ok) break;
+            t += plan.count;
+            // ---- epilogue of the unit: wait for its last P.V, then O / l leaves
+            // through this warp's two staging boxes [32 rows][32 fp32] (128-byte
+            // swizzle) by TMA bulk-tensor stores; rows past n are dropped.
+            ok = mbar_wait(&bars->o_done, (t - 1) & 1, abort, err);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t scol = tmem + lane_base + (b ? C::S_COL1 : C::S_COL0);
-            uint32_t s[128];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(scol + 32 * c, s + 32 * c);
-            tmem_wait_ld();
-#pragma unroll
-            for (int c = 0; c < 4; ++c) reg_fence32(s + 32 * c);
-
-            const int kt = plan.kt(i);
-            const int j0 = kt * C::BK;
-            float mx = -INFINITY;
-            if (tile_full(kt, p0, p1, sink, win, C::BK)) {
-#pragma unroll
-                for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
-            } else {
-#pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    float v = __uint_as_float(s[c]);
-                    if (!key_visible(p, j0 + c, sink, win)) v = -INFINITY;
-                    s[c] = __float_as_uint(v);
-                    mx = fmaxf(mx, v);
-                }
-            }
-            const float m_new = fmaxf(m_used, mx * sl2);
-            float corr = 1.0f;
-            bool resc = false;
-            if (m_new > m_used + 8.0f) {
-                if (m_used != -INFINITY) {
-                    corr = ex2(m_used - m_new);
-                    resc = true;
-                    l *= corr;
-                }
-                m_used = m_new;
-            }
-            const float mref = (m_used == -INFINITY) ? 0.0f : m_used;
-            uint32_t pk[64];
-            float rs = 0.0f;
-#pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const float a = ex2(fmaf(__uint_as_float(s[2 * c]), sl2, -mref));
-                const float bq = ex2(fmaf(__uint_as_float(s[2 * c + 1]), sl2, -mref));
-                rs += a + bq;
-                pk[c] = pack_half2(a, bq);
-            }
-            l += rs;
-            if (i > 0) {  // O must hold PV_{i-1} before it is rescaled and before P_i lands
-                ok = mbar_wait(&bars->o_done, (i - 1) & 1, abort, err);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-            }
-            tc_fence_after();
-            __syncwarp();
-            if (__any_sync(0xffffffffu, resc)) {
-#pragma unroll 1
-                for (int c = 0; c < HD / 32; ++c) {
-                    uint32_t o[32];
-                    const uint32_t oc = tmem + lane_base + C::O_COL + 32 * c;
-                    tmem_ld32(oc, o);
-                    tmem_wait_ld();
-                    reg_fence32(o);
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * corr);
-                    tmem_st32(oc, o);
-                }
-            }
-            tmem_st32(scol, pk);
-            tmem_st32(scol + 32, pk + 32);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&bars->p_full[b]);
-        }
-        if (ok) {
-            ok = mbar_wait(&bars->o_done, (count - 1) & 1, abort, err);
-            ok = __all_sync(0xffffffffu, ok);
-        }
-        if (ok) {
-            tc_fence_after();
             const float inv = 1.0f / l;
-            float *orow = out + (static_cast<size_t>(p) * Hq + h) * HD;
+            const int wr = warp & 3;  // rows 32 wr .. 32 wr + 31 of the tile
 #pragma unroll 1
             for (int c = 0; c < HD / 32; ++c) {
                 uint32_t o[32];
                 tmem_ld32(tmem + lane_base + C::O_COL + 32 * c, o);
                 tmem_wait_ld();
                 reg_fence32(o);
-                if (p < n) {
+                if (c == HD / 32 - 1) {  // O fully read: the next unit may overwrite it
+                    tc_fence_before();
+                    mbar_arrive(&bars->o_free);
+                }
+                // this box was last used by the store issued two chunks ago
+                if (lane == 0 && stores >= 2) bulk_wait_group_read<1>();
+                __syncwarp();
+                uint8_t *box = smem + C::OFF_OST + (wr * 2 + (c & 1)) * C::OST_BYTES;
+                uint8_t *rowp = box + lane * 128;
 #pragma unroll
-                    for (int k = 0; k < 32; k += 4) {
-                        float4 v;
-                        v.x = __uint_as_float(o[k]) * inv;
-                        v.y = __uint_as_float(o[k + 1]) * inv;
-                        v.z = __uint_as_float(o[k + 2]) * inv;
-                        v.w = __uint_as_float(o[k + 3]) * inv;
-                        *reinterpret_cast<float4 *>(orow + 32 * c + k) = v;
-                    }
+                for (int k = 0; k < 8; ++k) {
+                    float4 v;
+                    v.x = __uint_as_float(o[4 * k]) * inv;
+                    v.y = __uint_as_float(o[4 * k + 1]) * inv;
+                    v.z = __uint_as_float(o[4 * k + 2]) * inv;
+                    v.w = __uint_as_float(o[4 * k + 3]) * inv;
+                    *reinterpret_cast<float4 *>(rowp + ((k ^ (lane & 7)) << 4)) = v;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && p0 + 32 * wr < n) {  // rows past n are not stored
+                    tma_store_3d(&tm_o, box, 32 * c, u.h, p0 + 32 * wr);
+                    bulk_commit_group();
+                    ++stores;
                 }
             }
         }
+        if (lane == 0) bulk_wait_group_read<0>();
     }
     tc_fence_before();
     __syncthreads();
@@ -408,17 +524,17 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// fp16 3-D tensor, 128-byte swizzle, zero fill outside the tensor.
+// 3-D tensor (fp16 or fp32), 128-byte swizzle, zero fill outside the tensor.
 bool encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
                uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1,
-               uint32_t b2) {
+               uint32_t b2, CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_FLOAT16) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[3] = {d0, d1, d2};
     const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
     const cuuint32_t box[3] = {b0, b1, b2};
     const cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+    return fn(m, dtype, 3, const_cast<void *>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -427,19 +543,24 @@ bool encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint6
 template <int HD>
 cudaError_t launch_hd(const PrefillArgs &a, unsigned *err, cudaStream_t stream) {
     using C = Cfg<HD>;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     const uint64_t n = a.n, Hq = a.n_q_heads, Hkv = a.n_kv_heads;
     if (!encode_3d(&tq, a.qh, HD, Hq, n, HD * 2, Hq * HD * 2, 64, 1, C::BQ) ||
         !encode_3d(&tk, a.kh, HD, n, Hkv, HD * 2, n * HD * 2, 64, C::BK, 1) ||
-        !encode_3d(&tv, a.vh, HD, n, Hkv, HD * 2, n * HD * 2, 64, C::BK, 1))
+        !encode_3d(&tv, a.vh, HD, n, Hkv, HD * 2, n * HD * 2, 64, C::BK, 1) ||
+        !encode_3d(&to, a.out, HD, Hq, n, HD * 4, Hq * HD * 4, 32, 1, 32,
+                   CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<HD>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     const int nqt = (a.n + C::BQ - 1) / C::BQ;
+    const int units = nqt * a.n_q_heads;
+    const int grid = units < device_sm_count() ? units : device_sm_count();
     const float sl2 = a.scale * 1.4426950408889634f;
-    prefill_tc_kernel<HD><<<nqt * a.n_q_heads, 256, C::SMEM, stream>>>(
-        tq, tk, tv, a.out, a.tile_map, a.n, a.n_q_heads, a.n_kv_heads, a.sink, a.win, sl2, err);
+    prefill_tc_kernel<HD><<<grid, 256, C::SMEM, stream>>>(
+        tq, tk, tv, to, a.tile_map, a.work_counter, a.n, a.n_q_heads, a.n_kv_heads, a.sink, a.win,
+        sl2, err);
     return cudaGetLastError();
 }
 
