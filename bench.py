@@ -135,6 +135,25 @@ class ClockSampler:
                 "samples": len(self.samples)}
 
 
+# ------------------------------------------------- multi-rank (replicas)
+
+def reduce_max_over_ranks(x, dist=None, device="cpu"):
+    """Largest value of x over all ranks of the default process group (x
+    itself when running alone). The job time is the slowest rank's time."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(work_per_rank, ms_max, world):
+    """Whole-job throughput when every rank runs the same workload on its own
+    GPU (replicas, weak scaling): all ranks' work over the slowest rank's time."""
+    return world * work_per_rank / (ms_max * 1e-3)
+
+
 # ------------------------------------------------------------ GPU arm
 
 class GpuBench:
@@ -409,11 +428,7 @@ def main():
         torch.cuda.synchronize(dev)
 
     def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max_over_ranks(x, torch.distributed if world > 1 else None, dev)
 
     # ---------------- headline: prefill n=8192 fp32 KV, full causal
     S = B.prefill_setup(headline)
@@ -424,7 +439,7 @@ def main():
     barrier()
     wall = time.perf_counter() - t_wall
     ms = max_over_ranks(statistics.mean(step_ms))
-    value = world * flops_step / (ms * 1e-3) / 1e12
+    value = job_throughput(flops_step, ms, world) / 1e12
     kms = statistics.mean(kern_ms)
     achieved = flops_step / (kms * 1e-3) / 1e12
     traffic = profiled_traffic("prefill_tc_kernel<256>", src_hash("prefill_tc.cu"))
@@ -434,7 +449,7 @@ def main():
                 "peak_source": f"{peaks['source']} bf16 dense (fp16 has the same nominal rate), "
                                "burst", "kernel_ms": kms}
     e2e_ms, h2d, d2h = B.prefill_e2e(S, args.warmup, max(3, args.steps // 2))
-    e2e_val = world * flops_step / (max_over_ranks(statistics.mean(e2e_ms)) * 1e-3) / 1e12
+    e2e_val = job_throughput(flops_step, max_over_ranks(statistics.mean(e2e_ms)), world) / 1e12
     launches_per_step = 5  # append, stage Q, stage K, stage V, tensor-core kernel
 
     cpu = None

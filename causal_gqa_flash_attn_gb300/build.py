@@ -43,8 +43,8 @@ def _stale() -> bool:
     return any(os.path.getmtime(p) > t for p in _deps())
 
 
-def _compile(src: str, extra) -> str:
-    obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+def _compile(src: str, extra, out_dir: str = OUT_DIR) -> str:
+    obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
     cmd = [nvcc()] + ARCH + CFLAGS + list(extra) + ["-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -52,22 +52,25 @@ def _compile(src: str, extra) -> str:
     return obj
 
 
-def build(force: bool = False, extra=(), verbose: bool = False) -> str:
-    if not force and not extra and not _stale():
+def build(force: bool = False, extra=(), verbose: bool = False, out_dir: str = OUT_DIR) -> str:
+    """Build libfa.so into out_dir (the default in-tree _build, or another
+    directory for a variant built with extra nvcc flags)."""
+    lib = os.path.join(out_dir, "libfa.so")
+    if out_dir == OUT_DIR and not force and not extra and not _stale():
         return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+    os.makedirs(out_dir, exist_ok=True)
     srcs = sources()
     with concurrent.futures.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), srcs))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, extra, out_dir), srcs))
+    tmp = lib + ".tmp"
     cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     if verbose:
-        print(LIB)
-    return LIB
+        print(lib)
+    return lib
 
 
 if __name__ == "__main__":
