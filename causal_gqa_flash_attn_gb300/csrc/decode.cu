@@ -16,13 +16,15 @@
 // by the dequantisation, not by the MMA rate.
 //
 // Two kernels write the same partials (m, l, acc per slot, q head, entry):
-//  * decode_q4_kernel (Q4_0 cache, group <= 8): per warp a 3-stage ring of raw
-//    Q4_0 K/V tiles (32 keys) filled by one bulk copy each; nibbles become fp16
-//    MMA operands in registers. For K the operand is 1024 + c (one LOP3) and the
+//  * decode_q4_kernel (Q4_0 cache, group <= 8): 4 pairs of warps per block,
+//    each pair a QK warp and a PV warp with their own rings of raw Q4_0 K and
+//    V tiles (32 keys, one bulk copy each); nibbles become fp16 MMA operands in
+//    registers. For K the operand is 1024 + c (one LOP3) and the
 //    -1032 * sum(q) bias of each 32-element block is preloaded into a fresh
-//    accumulator, then scaled by the block's d; for V the operand is c - 8
-//    and d is folded into P. Keys held as fp16 shadows (sinks, recent ring)
-//    are left to one extra entry per (slot, kv head), run by the generic path.
+//    accumulator, then scaled by the block's d; for V the operand is 1024 + c
+//    (or + 16 c) with a constant-operand MMA removing the offset, and d is
+//    folded into P. Keys held as fp16 shadows (sinks, recent ring) are left to
+//    one extra entry per (slot, kv head), run by the generic path.
 //  * decode_kernel (fp32 caches, group 16, and that shadow entry): stages
 //    16-key fp16 tiles in shared memory, reads fragments with ldmatrix.
 // Each block merges its warps; fa_decode_combine merges the entries.
@@ -34,7 +36,6 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kChunk = 16;     // keys per step of the generic path
-constexpr int kTileKeys = 32;  // keys per stage of the Q4_0 path
 // Lazy rescale threshold (log2 units) of the running max: O and l keep a
 // stale reference until the max grows past it. In the Q4_0 path P is
 // multiplied by the block scale d in fp16, so P <= 2^2 keeps P*d finite for
@@ -80,37 +81,41 @@ __device__ __forceinline__ void write_empty(const DecodeParams &P, size_t head0,
     }
 }
 
-// Merge the kWarps per-warp online-softmax states of a block and write the
-// block's partial. Per thread: m_used/m_true/lsum of heads nt*8 + 2t + {0,1}
-// (exp2 domain, lsum already summed over the warp), o[mt][nt][k] of rows
-// r (k < 2) and r+8 (k >= 2) of m-tile mt, heads nt*8 + 2t + (k & 1).
-template <int HD, int NT, bool Q4ROWS = false>
-__device__ __forceinline__ void merge_and_write(const DecodeParams &P, uint8_t *dsmem,
-                                                size_t head0, int G, int e,
-                                                const float (&m_used)[NT][2],
-                                                const float (&m_true)[NT][2],
-                                                const float (&lsum)[NT][2],
-                                                const float (&o)[HD / 16][NT][4]) {
-    constexpr int MT = HD / 16;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = lane >> 2, t = lane & 3;
-    __syncthreads();
-    float *sm_mu = reinterpret_cast<float *>(dsmem);  // [kWarps][16]
-    float *sm_mt = sm_mu + kWarps * 16;
-    float *sm_l = sm_mt + kWarps * 16;
-    float *sm_f = sm_l + kWarps * 16;
-    float *sm_o = sm_f + kWarps * 16;  // [kWarps][16][HD]
+// Merge of a block's kWarps online-softmax states ("slots") into the block's
+// partial. Slot w holds m_used, m_true, lsum of heads nt*8 + 2t + {0,1}
+// (exp2 domain; lsum summed over the warp) and O^T rows r (k < 2) and r+8
+// (k >= 2) of m-tile mt, heads nt*8 + 2t + (k & 1). The stats and O of a slot
+// may come from different warps; merge_finish is called by every thread.
+__device__ __forceinline__ float *merge_buf(uint8_t *dsmem) { return reinterpret_cast<float *>(dsmem); }
+
+template <int NT>
+__device__ __forceinline__ void merge_write_stats(uint8_t *dsmem, int slot,
+                                                  const float (&m_used)[NT][2],
+                                                  const float (&m_true)[NT][2],
+                                                  const float (&lsum)[NT][2]) {
+    const int lane = threadIdx.x & 31, r = lane >> 2, t = lane & 3;
+    float *sm_mu = merge_buf(dsmem), *sm_mt = sm_mu + kWarps * 16, *sm_l = sm_mt + kWarps * 16;
     if (r == 0) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const int head = nt * 8 + 2 * t + hh;
-                sm_mu[warp * 16 + head] = m_used[nt][hh];
-                sm_mt[warp * 16 + head] = m_true[nt][hh];
-                sm_l[warp * 16 + head] = lsum[nt][hh];
+                sm_mu[slot * 16 + head] = m_used[nt][hh];
+                sm_mt[slot * 16 + head] = m_true[nt][hh];
+                sm_l[slot * 16 + head] = lsum[nt][hh];
             }
     }
+}
+
+// Q4ROWS: the Q4_0 path's m-tile 2b + j rows r, r+8 hold elements 2r + j,
+// 16 + 2r + j of block b; otherwise rows are in natural order.
+template <int HD, int NT, bool Q4ROWS>
+__device__ __forceinline__ void merge_write_o(uint8_t *dsmem, int slot,
+                                              const float (&o)[HD / 16][NT][4]) {
+    constexpr int MT = HD / 16;
+    const int lane = threadIdx.x & 31, r = lane >> 2, t = lane & 3;
+    float *sm_o = merge_buf(dsmem) + 4 * kWarps * 16;  // [kWarps][16][HD]
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -118,12 +123,17 @@ __device__ __forceinline__ void merge_and_write(const DecodeParams &P, uint8_t *
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int head = nt * 8 + 2 * t + (k & 1);
-                // Q4_0 path: m-tile 2b (2b+1) rows r, r+8 hold elements 2r, 2r+1
-                // (16 + 2r, 17 + 2r) of block b; generic path: natural order.
-                const int dim = Q4ROWS ? 32 * (mt >> 1) + 16 * (mt & 1) + 2 * r + (k >> 1)
+                const int dim = Q4ROWS ? 32 * (mt >> 1) + 16 * (k >> 1) + 2 * r + (mt & 1)
                                        : 16 * mt + r + ((k >> 1) << 3);
-                sm_o[(warp * 16 + head) * HD + dim] = o[mt][nt][k];
+                sm_o[(slot * 16 + head) * HD + dim] = o[mt][nt][k];
             }
+}
+
+template <int HD>
+__device__ __forceinline__ void merge_finish(const DecodeParams &P, uint8_t *dsmem, size_t head0,
+                                             int G, int e) {
+    float *sm_mu = merge_buf(dsmem), *sm_mt = sm_mu + kWarps * 16, *sm_l = sm_mt + kWarps * 16;
+    float *sm_f = sm_l + kWarps * 16, *sm_o = sm_f + kWarps * 16;
     __syncthreads();
     if (threadIdx.x < G) {
         const int head = threadIdx.x;
@@ -144,9 +154,9 @@ __device__ __forceinline__ void merge_and_write(const DecodeParams &P, uint8_t *
     __syncthreads();
     for (int idx = threadIdx.x; idx < G * HD; idx += blockDim.x) {
         const int head = idx / HD, dim = idx % HD;
-        if (sm_mt[head] == -INFINITY && sm_mt[16 + head] == -INFINITY &&
-            sm_mt[32 + head] == -INFINITY && sm_mt[48 + head] == -INFINITY)
-            continue;  // empty for this head: acc is never read
+        bool any = false;
+        for (int w = 0; w < kWarps; ++w) any |= sm_mt[w * 16 + head] != -INFINITY;
+        if (!any) continue;  // empty for this head: acc is never read
         float a = 0.0f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) a += sm_f[w * 16 + head] * sm_o[(w * 16 + head) * HD + dim];
@@ -307,7 +317,8 @@ __device__ __forceinline__ void generic_body(const DecodeParams &P, uint8_t *dsm
     const uint32_t tk_s = smem_u32(tk), tv_s = smem_u32(tv);
     const int n0 = max(0, hi0 - lo0 + kChunk - 1) / kChunk;
     const int n1 = max(0, hi1 - lo1 + kChunk - 1) / kChunk;
-    for (int ci = warp; ci < n0 + n1; ci += kWarps) {
+    // blocks with more than kWarps warps: the extra warps only join the merge
+    for (int ci = warp; warp < kWarps && ci < n0 + n1; ci += kWarps) {
         const bool first = ci < n0;
         const int c0 = first ? lo0 + kChunk * ci : lo1 + kChunk * (ci - n0);
         const int k_hi = first ? hi0 : hi1;
@@ -380,7 +391,12 @@ __device__ __forceinline__ void generic_body(const DecodeParams &P, uint8_t *dsm
             v += __shfl_xor_sync(0xffffffffu, v, 16);
             lsum[nt][hh] = v;
         }
-    merge_and_write<HD, NT>(P, dsmem, head0, G, e, m_used, m_true, lsum, o);
+    __syncthreads();  // the merge buffer overlaps the staging tiles
+    if (warp < kWarps) {
+        merge_write_stats<NT>(dsmem, warp, m_used, m_true, lsum);
+        merge_write_o<HD, NT, false>(dsmem, warp, o);
+    }
+    merge_finish<HD>(P, dsmem, head0, G, e);
 }
 
 __device__ __forceinline__ void write_header(const DecodeParams &P, int hd) {
@@ -450,50 +466,85 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(const DecodeParams 
 }
 
 // ============================================================== Q4_0 path
-
-// The Q4_0 path's pipeline depth and residency (stages per warp, blocks per
-// SM); shared memory per block is 4 warps x stages x 2 tiles of 32 keys.
-#ifndef FA_Q4_STAGES
-#define FA_Q4_STAGES 2
+//
+// The block's 8 warps form 4 pairs; pair w walks 32-key tiles w, w+4, ... of
+// the entry's key range through its own rings of raw Q4_0 K tiles and V tiles
+// (one bulk copy each). Warp w (QK) scores a tile, folds it into the online
+// softmax and hands P^T fragments plus the O rescale factor of that tile to
+// warp w+4 (PV) through a ring of P records; warp w+4 multiplies them into O.
+// The QK warp's lane 0 issues every copy: a K tile as soon as the QK warp
+// itself has scored the tile before it in that stage, a V tile as soon as the
+// PV warp has released that stage, so that the two warps overlap.
+constexpr int kTileKeys = 32;  // keys per tile
+constexpr int kPairs = 4;      // warp pairs per block
+constexpr int kPRing = 2;      // P records in flight per pair
+// Pipeline depths (K tiles and V tiles per pair) and residency (blocks per SM).
+#ifndef FA_Q4_KSTAGES
+#define FA_Q4_KSTAGES 2
+#endif
+#ifndef FA_Q4_VSTAGES
+#define FA_Q4_VSTAGES 3
 #endif
 #ifndef FA_Q4_MIN_BLOCKS
-#define FA_Q4_MIN_BLOCKS 3
+#define FA_Q4_MIN_BLOCKS 2
 #endif
 
 template <int HD>
 struct Q4Cfg {
-    static constexpr int NST = FA_Q4_STAGES;
+    static constexpr int NK = FA_Q4_KSTAGES;
+    static constexpr int NV = FA_Q4_VSTAGES;
     static constexpr int NB = HD / kQ4Block;                  // blocks per row
     static constexpr int MT = HD / 16;                        // m16 tiles of head_dim
     static constexpr int ROWB = NB * kQ4BlockBytes;           // bytes per row
     static constexpr int TILE = kTileKeys * ROWB;             // bytes of K (or V) per stage
     static constexpr int TILE_ALLOC = (TILE + 127) / 128 * 128;
-    static constexpr int WARP_BYTES = NST * 2 * TILE_ALLOC;
-    static constexpr int BAR_OFF = kWarps * WARP_BYTES;
-    static constexpr int SMEM_PIPE = BAR_OFF + kWarps * NST * 8 + 16;
+    // P record: [32 lanes] {P^T b0, b1 of keys 0-15, b0, b1 of keys 16-31},
+    // then [32 lanes] {rescale of head 2t, of head 2t+1, tile index, 0}
+    static constexpr int PREC = 2 * 32 * 16;
+    static constexpr int K_OFF = 0;
+    static constexpr int V_OFF = NK * TILE_ALLOC;
+    static constexpr int P_OFF = (NK + NV) * TILE_ALLOC;
+    static constexpr int PAIR_BYTES = P_OFF + kPRing * PREC;
+    // Q^T fragments [NB][32 lanes] uint4 and block biases [NB][32 lanes]
+    // float4, shared by the block's QK warps (one slot, one kv head)
+    static constexpr int QF_OFF = kPairs * PAIR_BYTES;
+    static constexpr int QB_OFF = QF_OFF + NB * 32 * 16;
+    static constexpr int BAR_OFF = QB_OFF + NB * 32 * 16;
+    // per pair: kfull[NK], vfull[NV], vempty[NV], pfull[kPRing], pempty[kPRing]
+    static constexpr int BARS_PER_PAIR = NK + 2 * NV + 2 * kPRing;
+    static constexpr int SMEM_PIPE = BAR_OFF + kPairs * BARS_PER_PAIR * 8 + 16;
     static constexpr int SMEM_GENERIC = kWarps * 2 * kChunk * (HD + 8) * 2;
     static constexpr int SMEM_MERGE = kWarps * 16 * (4 + HD) * 4;
     static constexpr int SMEM = SMEM_PIPE > SMEM_GENERIC
                                     ? (SMEM_PIPE > SMEM_MERGE ? SMEM_PIPE : SMEM_MERGE)
                                     : (SMEM_GENERIC > SMEM_MERGE ? SMEM_GENERIC : SMEM_MERGE);
     static_assert(NB % 2 == 0, "head_dim must be a multiple of 64");
+    static_assert(NK >= 1 && NV >= 2, "pipeline depths");
+    static_assert(TILE_ALLOC % 128 == 0 && PAIR_BYTES % 16 == 0 && BAR_OFF % 8 == 0, "alignment");
 };
 
-__device__ __forceinline__ uint32_t h2sub(uint32_t x, uint16_t c_bits) {
-    __half2 h = *reinterpret_cast<__half2 *>(&x);
-    h = __hsub2(h, __half2half2(__ushort_as_half(c_bits)));
-    return *reinterpret_cast<uint32_t *>(&h);
-}
 __device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
     __half2 x = *reinterpret_cast<__half2 *>(&a), y = *reinterpret_cast<__half2 *>(&b);
     x = __hmul2(x, y);
     return *reinterpret_cast<uint32_t *>(&x);
 }
-constexpr uint32_t kMagic = 0x64006400u;    // fp16 pair (1024, 1024)
+
+// (x & MASK) | magic in one LOP3; magic is passed in a register so that the
+// two constants need not both be encoded in the instruction.
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t magic) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(x), "n"(MASK), "r"(magic));
+    return d;
+}
+// A value the compiler must keep in a register rather than re-materialise.
+__device__ __forceinline__ uint32_t opaque(uint32_t x) {
+    asm volatile("" : "+r"(x));
+    return x;
+}
+constexpr uint32_t kMagic = 0x64006400u;     // fp16 pair (1024, 1024)
 constexpr uint32_t kHNeg1032 = 0xE408E408u;  // fp16 pair (-1032, -1032)
 constexpr uint32_t kHNeg1152 = 0xE480E480u;  // fp16 pair (-1152, -1152)
-constexpr uint16_t kH1032 = 0x6408u;        // fp16 1032 = 1024 + 8
-constexpr uint16_t kH1152 = 0x6480u;        // fp16 1152 = 1024 + 16 * 8
 
 // Code bytes of block b that thread t (of 4 per row) turns into its K operand
 // halves: a 32-bit word read at an aligned offset. Element order within the
@@ -504,30 +555,84 @@ __host__ __device__ constexpr int q4k_elem(int b, int t, int i) {
     return (b & 1) ? 4 * t + i : (t < 3 ? 2 + 4 * t + i : (i < 2 ? 14 + i : i - 2));
 }
 
+
+// Q^T B fragments of kv head group head0 for blocks b = first, first + step,
+// ... in the permuted order of q4k_elem: lo k-step of block b (elements
+// 0..15) takes q, the hi k-step (16..31) q / 16, because the K operand there
+// is 1024 + 16 c. bias = -(1032 sum_lo q + 1152 sum_hi q/16) over the fp16
+// values, for heads 2t, 2t+1 (twice: the accumulator input of rows r and
+// r + 8), so that a block's accumulator ends at sum q (c - 8). Heads >= G get
+// q = 0.
+template <int HD>
+__device__ __forceinline__ void build_q_frags(const DecodeParams &P, size_t head0, int G,
+                                              int first, int step, uint4 *qfrag, float4 *qbias) {
+    constexpr int NB = HD / kQ4Block;
+    const int lane = threadIdx.x & 31, r = lane >> 2, t = lane & 3;
+    for (int b = first; b < NB; b += step) {
+        const int hh = r;
+        const float *qr = P.q + (head0 + (hh < G ? hh : 0)) * HD + 32 * b;
+        const float sc = (hh < G) ? 1.0f : 0.0f;
+        uint32_t w[4];
+        float ps = 0.0f;
+#pragma unroll
+        for (int hi = 0; hi < 2; ++hi) {
+            const float f = hi ? 0.0625f : 1.0f;
+            const float *qb0 = qr + 16 * hi;
+            const __half2 x0 = __floats2half2_rn(sc * f * qb0[q4k_elem(b, t, 0)],
+                                                 sc * f * qb0[q4k_elem(b, t, 2)]);
+            const __half2 x1 = __floats2half2_rn(sc * f * qb0[q4k_elem(b, t, 1)],
+                                                 sc * f * qb0[q4k_elem(b, t, 3)]);
+            w[2 * hi] = *reinterpret_cast<const uint32_t *>(&x0);
+            w[2 * hi + 1] = *reinterpret_cast<const uint32_t *>(&x1);
+            const float2 f0 = __half22float2(x0), f1 = __half22float2(x1);
+            ps += (hi ? -1152.0f : -1032.0f) * ((f0.x + f0.y) + (f1.x + f1.y));
+        }
+        ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 2);  // head r's block bias
+        const float b0 = __shfl_sync(0xffffffffu, ps, (2 * t) * 4);
+        const float b1 = __shfl_sync(0xffffffffu, ps, (2 * t + 1) * 4);
+        qfrag[b * 32 + lane] = make_uint4(w[0], w[1], w[2], w[3]);
+        qbias[b * 32 + lane] = make_float4(b0, b1, b0, b1);
+    }
+}
+
 template <int HD>
 __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, int e, int g,
                                         int u, int p, int k_lo, int k_hi) {
     using C = Q4Cfg<HD>;
-    constexpr int NB = C::NB, MT = C::MT, ROWB = C::ROWB, NST = C::NST;
+    constexpr int NB = C::NB, MT = C::MT, ROWB = C::ROWB, NK = C::NK, NV = C::NV;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = lane >> 2, t = lane & 3;
+    const int pair = warp & (kPairs - 1);
+    const bool qk_role = warp < kPairs;
     const int G = P.Hq / P.Hkv;
     const size_t head0 = static_cast<size_t>(u) * P.Hq + static_cast<size_t>(g) * G;
-    uint8_t *wbase = dsmem + warp * C::WARP_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(dsmem + C::BAR_OFF) + warp * NST;
-    volatile int *abort = reinterpret_cast<volatile int *>(dsmem + C::BAR_OFF + kWarps * NST * 8);
+    uint8_t *pbase = dsmem + pair * C::PAIR_BYTES;
+    uint8_t *prec = pbase + C::P_OFF;  // P record ring
+    uint4 *qfrag = reinterpret_cast<uint4 *>(dsmem + C::QF_OFF);
+    float4 *qbias = reinterpret_cast<float4 *>(dsmem + C::QB_OFF);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(dsmem + C::BAR_OFF) + pair * C::BARS_PER_PAIR;
+    uint64_t *kfull = bars, *vfull = bars + NK, *vempty = bars + NK + NV,
+             *pfull = bars + NK + 2 * NV, *pempty = bars + NK + 2 * NV + kPRing;
+    volatile int *abort =
+        reinterpret_cast<volatile int *>(dsmem + C::BAR_OFF + kPairs * C::BARS_PER_PAIR * 8);
 
+    build_q_frags<HD>(P, head0, G, warp, 2 * kPairs, qfrag, qbias);
     if (threadIdx.x == 0) *abort = 0;
-    if (lane == 0) {
-        for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
+    if (qk_role && lane == 0) {
+        for (int s = 0; s < NK; ++s) mbar_init(&kfull[s], 1);
+        for (int s = 0; s < NV; ++s) {
+            mbar_init(&vfull[s], 1);
+            mbar_init(&vempty[s], 1);
+        }
+        for (int s = 0; s < kPRing; ++s) {
+            mbar_init(&pfull[s], 1);
+            mbar_init(&pempty[s], 1);
+        }
         mbar_fence_init();
     }
     __syncthreads();
 
-    const uint8_t *kbody = P.k_planes + static_cast<size_t>(u) * P.plane_bytes + P.body_off +
-                           static_cast<size_t>(g) * P.max_seq * ROWB;
-    const uint8_t *vbody = P.v_planes + static_cast<size_t>(u) * P.plane_bytes + P.body_off +
-                           static_cast<size_t>(g) * P.max_seq * ROWB;
     const int ss = P.shadow_sink, sw = P.shadow_win;
     const int ntiles = (k_hi - k_lo + kTileKeys - 1) / kTileKeys;
     // A tile is worth loading if some key in it is visible and not a shadow key.
@@ -540,249 +645,303 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
         return true;
     };
     auto next_tile = [&](int i) -> int {
-        while (i < ntiles && !tile_ok(i)) i += kWarps;
+        while (i < ntiles && !tile_ok(i)) i += kPairs;
         return i;
     };
-    auto issue = [&](int i, int s) {
-        const int t0 = k_lo + kTileKeys * i;
-        const int nk = min(kTileKeys, k_hi - t0);
-        const uint32_t bytes = (static_cast<uint32_t>(nk * ROWB) + 15u) & ~15u;
-        mbar_arrive_expect_tx(&bars[s], 2 * bytes);
-        bulk_copy_g2s(wbase + s * 2 * C::TILE_ALLOC, kbody + static_cast<size_t>(t0) * ROWB, bytes,
-                      &bars[s]);
-        bulk_copy_g2s(wbase + s * 2 * C::TILE_ALLOC + C::TILE_ALLOC,
-                      vbody + static_cast<size_t>(t0) * ROWB, bytes, &bars[s]);
-    };
-
-    // Q^T B fragments in the permuted order of q4k_elem: lo k-step of block b
-    // (elements 0..15) takes q as is, the hi k-step (elements 16..31) q / 16,
-    // because the K operand there is 1024 + 16 c. bias[b] = -(1032 sum_lo q +
-    // 1152 sum_hi q/16) over the fp16 values, for heads 2t, 2t+1, so that the
-    // accumulator ends at sum q (c - 8).
-    uint32_t qb[MT][2];
-    float bias[NB][2];
-    {
-        const int hh = r;
-        const float *qr = P.q + (head0 + (hh < G ? hh : 0)) * HD;
-        const float sc = (hh < G) ? 1.0f : 0.0f;
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            float ps = 0.0f;
-#pragma unroll
-            for (int hi = 0; hi < 2; ++hi) {
-                const float f = hi ? 0.0625f : 1.0f;
-                const float *qb0 = qr + 32 * b + 16 * hi;
-                const __half2 x0 = __floats2half2_rn(sc * f * qb0[q4k_elem(b, t, 0)],
-                                                     sc * f * qb0[q4k_elem(b, t, 2)]);
-                const __half2 x1 = __floats2half2_rn(sc * f * qb0[q4k_elem(b, t, 1)],
-                                                     sc * f * qb0[q4k_elem(b, t, 3)]);
-                qb[2 * b + hi][0] = *reinterpret_cast<const uint32_t *>(&x0);
-                qb[2 * b + hi][1] = *reinterpret_cast<const uint32_t *>(&x1);
-                const float2 f0 = __half22float2(x0), f1 = __half22float2(x1);
-                ps += (hi ? -1152.0f : -1032.0f) * ((f0.x + f0.y) + (f1.x + f1.y));
-            }
-            ps += __shfl_xor_sync(0xffffffffu, ps, 1);
-            ps += __shfl_xor_sync(0xffffffffu, ps, 2);  // head r's block bias
-            bias[b][0] = __shfl_sync(0xffffffffu, ps, (2 * t) * 4);
-            bias[b][1] = __shfl_sync(0xffffffffu, ps, (2 * t + 1) * 4);
-        }
-    }
-
-    float o[MT][1][4];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) o[mt][0][k] = 0.0f;
-    float m_used[1][2] = {{-INFINITY, -INFINITY}}, m_true[1][2] = {{-INFINITY, -INFINITY}};
-    float lsum[1][2] = {{0.0f, 0.0f}};
-
-    // stage s holds tile tiles[s] of this warp's sequence (ntiles = none);
-    // the sequence is consumed in order, stage after stage
-    int tiles[NST];
-    int issued = next_tile(warp);
-#pragma unroll
-    for (int s = 0; s < NST; ++s) {
-        tiles[s] = issued;
-        if (issued < ntiles) {
-            if (lane == 0) issue(issued, s);
-            issued = next_tile(issued + kWarps);
-        }
-    }
-    uint32_t phase = 0;
     bool ok = true;
-    int s = 0;
-#pragma unroll 1
-    while (tiles[s] < ntiles) {
-        const int i = tiles[s];
-        ok = mbar_wait(&bars[s], (phase >> s) & 1u, abort, P.err);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        phase ^= 1u << s;
-        const uint8_t *Ks = wbase + s * 2 * C::TILE_ALLOC;
-        const uint8_t *Vs = Ks + C::TILE_ALLOC;
-        const int t0 = k_lo + kTileKeys * i;
 
-        // ---- scores: half h2 holds keys t0 + 16 h2 + {r, r+8}
-        float sc0[4], sc1[4];
+    if (qk_role) {
+        // ================================================= QK + softmax warp
+        const uint8_t *kbody = P.k_planes + static_cast<size_t>(u) * P.plane_bytes + P.body_off +
+                               static_cast<size_t>(g) * P.max_seq * ROWB;
+        const uint8_t *vbody = P.v_planes + static_cast<size_t>(u) * P.plane_bytes + P.body_off +
+                               static_cast<size_t>(g) * P.max_seq * ROWB;
+        // one bulk copy of tile i's rows (rounded up to 16 bytes) into dst
+        auto issue = [&](const uint8_t *body, int i, uint8_t *dst, uint64_t *bar) {
+            const int t0 = k_lo + kTileKeys * i;
+            const int nk = min(kTileKeys, k_hi - t0);
+            const uint32_t bytes = (static_cast<uint32_t>(nk * ROWB) + 15u) & ~15u;
+            mbar_arrive_expect_tx(bar, bytes);
+            bulk_copy_g2s(dst, body + static_cast<size_t>(t0) * ROWB, bytes, bar);
+        };
+        float mu0 = -INFINITY, mu1 = -INFINITY, mt0 = -INFINITY, mt1 = -INFINITY;
+        float ls0 = 0.0f, ls1 = 0.0f;
+        // Prologue: the first NK K tiles and the first NV - 1 V tiles. V stays
+        // one tile behind so that refilling a V stage waits on the PV warp's
+        // previous tile, not on the one just handed over.
+        int kt = next_tile(pair), vt = kt;  // next tile index to copy
+        int kn = 0, vn = 0;                 // copies issued so far
+        for (; kn < NK && kt < ntiles; ++kn) {
+            if (lane == 0) issue(kbody, kt, pbase + C::K_OFF + kn * C::TILE_ALLOC, &kfull[kn]);
+            kt = next_tile(kt + kPairs);
+        }
+        for (; vn < NV - 1 && vt < ntiles; ++vn) {
+            if (lane == 0) issue(vbody, vt, pbase + C::V_OFF + vn * C::TILE_ALLOC, &vfull[vn]);
+            vt = next_tile(vt + kPairs);
+        }
+        const uint32_t magic = opaque(kMagic);
+        int seq = 0;  // position of the tile in this pair's sequence
+        for (int i = next_tile(pair); i < ntiles; i = next_tile(i + kPairs), ++seq) {
+            const int s = seq % NK;
+            ok = __all_sync(0xffffffffu, mbar_wait(&kfull[s], (seq / NK) & 1, abort, P.err));
+            if (!ok) break;
+            const uint8_t *Ks = pbase + C::K_OFF + s * C::TILE_ALLOC;
+            const int t0 = k_lo + kTileKeys * i;
+            // ---- scores: half h2 holds keys t0 + 16 h2 + {r, r+8}
+            float sc0[4], sc1[4];
 #pragma unroll 1
-        for (int h2 = 0; h2 < 2; ++h2) {
-            const uint8_t *KA = Ks + (16 * h2 + r) * ROWB;
-            const uint8_t *KB = KA + 8 * ROWB;
-            float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const uint8_t *KA = Ks + (16 * h2 + r) * ROWB;
+                const uint8_t *KB = KA + 8 * ROWB;
+                float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                const int o18 = kQ4BlockBytes * b;
-                uint32_t wA, wB, dA, dB;
-                if ((b & 1) == 0) {
-                    const uint32_t a0 = *reinterpret_cast<const uint32_t *>(KA + o18 + 4 + 4 * t);
-                    const uint32_t a1 = *reinterpret_cast<const uint32_t *>(KA + o18);
-                    const uint32_t b0 = *reinterpret_cast<const uint32_t *>(KB + o18 + 4 + 4 * t);
-                    const uint32_t b1 = *reinterpret_cast<const uint32_t *>(KB + o18);
-                    const uint32_t sel = (t == 3) ? 0x7610u : 0x3210u;
-                    wA = __byte_perm(a0, a1, sel);
-                    wB = __byte_perm(b0, b1, sel);
-                    dA = a1 & 0xFFFFu;
-                    dB = b1 & 0xFFFFu;
-                } else {
-                    wA = *reinterpret_cast<const uint32_t *>(KA + o18 + 2 + 4 * t);
-                    wB = *reinterpret_cast<const uint32_t *>(KB + o18 + 2 + 4 * t);
-                    dA = *reinterpret_cast<const uint16_t *>(KA + o18);
-                    dB = *reinterpret_cast<const uint16_t *>(KB + o18);
+                for (int b = 0; b < NB; ++b) {
+                    const int o18 = kQ4BlockBytes * b;
+                    uint32_t wA, wB, dA, dB;
+                    if ((b & 1) == 0) {
+                        const uint32_t a0 = *reinterpret_cast<const uint32_t *>(KA + o18 + 4 + 4 * t);
+                        const uint32_t a1 = *reinterpret_cast<const uint32_t *>(KA + o18);
+                        const uint32_t b0 = *reinterpret_cast<const uint32_t *>(KB + o18 + 4 + 4 * t);
+                        const uint32_t b1 = *reinterpret_cast<const uint32_t *>(KB + o18);
+                        const uint32_t sel = (t == 3) ? 0x7610u : 0x3210u;
+                        wA = __byte_perm(a0, a1, sel);
+                        wB = __byte_perm(b0, b1, sel);
+                        dA = a1 & 0xFFFFu;
+                        dB = b1 & 0xFFFFu;
+                    } else {
+                        wA = *reinterpret_cast<const uint32_t *>(KA + o18 + 2 + 4 * t);
+                        wB = *reinterpret_cast<const uint32_t *>(KB + o18 + 2 + 4 * t);
+                        dA = *reinterpret_cast<const uint16_t *>(KA + o18);
+                        dB = *reinterpret_cast<const uint16_t *>(KB + o18);
+                    }
+                    const uint32_t wA8 = wA >> 8, wB8 = wB >> 8;
+                    const uint32_t alo[4] = {and_or<0x000F000Fu>(wA, magic), and_or<0x000F000Fu>(wB, magic),
+                                             and_or<0x000F000Fu>(wA8, magic), and_or<0x000F000Fu>(wB8, magic)};
+                    const uint32_t ahi[4] = {and_or<0x00F000F0u>(wA, magic), and_or<0x00F000F0u>(wB, magic),
+                                             and_or<0x00F000F0u>(wA8, magic), and_or<0x00F000F0u>(wB8, magic)};
+                    const uint4 qv = lds_v4(qfrag + b * 32 + lane);
+                    const float4 bv = lds_f4(qbias + b * 32 + lane);
+                    const float cb[4] = {bv.x, bv.y, bv.z, bv.w};
+                    const uint32_t qlo[2] = {qv.x, qv.y}, qhi[2] = {qv.z, qv.w};
+                    float acc[4];
+                    mma_16816_c(acc, alo, qlo, cb);
+                    mma_16816(acc, ahi, qhi);
+                    const float fA = __half2float(__ushort_as_half(static_cast<uint16_t>(dA)));
+                    const float fB = __half2float(__ushort_as_half(static_cast<uint16_t>(dB)));
+                    s4[0] = fmaf(fA, acc[0], s4[0]);
+                    s4[1] = fmaf(fA, acc[1], s4[1]);
+                    s4[2] = fmaf(fB, acc[2], s4[2]);
+                    s4[3] = fmaf(fB, acc[3], s4[3]);
                 }
-                const uint32_t wA8 = wA >> 8, wB8 = wB >> 8;
-                const uint32_t alo[4] = {(wA & 0x000F000Fu) | kMagic, (wB & 0x000F000Fu) | kMagic,
-                                         (wA8 & 0x000F000Fu) | kMagic, (wB8 & 0x000F000Fu) | kMagic};
-                const uint32_t ahi[4] = {(wA & 0x00F000F0u) | kMagic, (wB & 0x00F000F0u) | kMagic,
-                                         (wA8 & 0x00F000F0u) | kMagic, (wB8 & 0x00F000F0u) | kMagic};
-                const float cb[4] = {bias[b][0], bias[b][1], bias[b][0], bias[b][1]};
-                float acc[4];
-                mma_16816_c(acc, alo, qb[2 * b], cb);
-                mma_16816(acc, ahi, qb[2 * b + 1]);
-                const float fA = __half2float(__ushort_as_half(static_cast<uint16_t>(dA)));
-                const float fB = __half2float(__ushort_as_half(static_cast<uint16_t>(dB)));
-                s4[0] = fmaf(fA, acc[0], s4[0]);
-                s4[1] = fmaf(fA, acc[1], s4[1]);
-                s4[2] = fmaf(fB, acc[2], s4[2]);
-                s4[3] = fmaf(fB, acc[3], s4[3]);
-            }
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                if (h2 == 0) sc0[k] = s4[k];
-                else sc1[k] = s4[k];
-            }
-        }
-        // ---- mask and fold: sv[hh][2 h2 + half] is key t0 + 16 h2 + r + 8 half.
-        // Most tiles are wholly in range, visible and free of shadow keys.
-        const int t1 = t0 + kTileKeys - 1;
-        const bool whole = t1 < k_hi && t0 >= ss && (sw <= 0 || t1 <= p - sw) &&
-                           (P.win <= 0 || t0 >= p - P.win + 1);
-        float sv[2][4], pv[2][4];
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2)
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const int key = t0 + 16 * h2 + r + 8 * half;
-                const bool vis = whole || (key < k_hi && key_visible(p, key, P.sink, P.win) &&
-                                           !(key < ss || (sw > 0 && key > p - sw)));
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
-                    sv[hh][2 * h2 + half] = vis ? (h2 ? sc1 : sc0)[2 * half + hh] : -INFINITY;
-            }
-        fold_scores<MT, 1, 4>(sv, P.sl2, kRescaleQ4, m_used[0][0], m_used[0][1], m_true[0][0],
-                              m_true[0][1], lsum[0][0], lsum[0][1], o, 0, pv);
-        // P^T B fragments of both halves: keys 2t,2t+1 (b0) and 2t+8,2t+9 (b1) of head r
-        const uint32_t pbA0 = movmatrix_trans(pack_half2(pv[0][0], pv[1][0]));
-        const uint32_t pbA1 = movmatrix_trans(pack_half2(pv[0][1], pv[1][1]));
-        const uint32_t pbB0 = movmatrix_trans(pack_half2(pv[0][2], pv[1][2]));
-        const uint32_t pbB1 = movmatrix_trans(pack_half2(pv[0][3], pv[1][3]));
-
-        // ---- O^T += V^T P'^T per 16-key half; thread group r owns elements
-        // 2r, 2r+1 (m-tile 2b) and 16+2r, 17+2r (m-tile 2b+1) of block b.
-#pragma unroll 1
-        for (int h2 = 0; h2 < 2; ++h2) {
-            const uint32_t pb0 = h2 ? pbB0 : pbA0;
-            const uint32_t pb1 = h2 ? pbB1 : pbA1;
-            const uint8_t *R0 = Vs + (16 * h2 + 2 * t) * ROWB;   // key 2t
-            const uint8_t *R1 = R0 + ROWB;                       // key 2t+1
-            const uint8_t *R2 = R0 + 8 * ROWB;                   // key 2t+8
-            const uint8_t *R3 = R2 + ROWB;                       // key 2t+9
-            const int kb = t0 + 16 * h2 + 2 * t;
-            // a key past the range has P = 0; force its scale to 0 so that no
-            // stale or uninitialised bytes can turn 0 * d into NaN
-            const uint32_t mask01 =
-                (kb < k_hi ? 0x0000FFFFu : 0u) | (kb + 1 < k_hi ? 0xFFFF0000u : 0u);
-            const uint32_t mask23 =
-                (kb + 8 < k_hi ? 0x0000FFFFu : 0u) | (kb + 9 < k_hi ? 0xFFFF0000u : 0u);
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                const int o18 = kQ4BlockBytes * b;
-                const uint32_t d01 = __byte_perm(*reinterpret_cast<const uint16_t *>(R0 + o18),
-                                                 *reinterpret_cast<const uint16_t *>(R1 + o18),
-                                                 0x5410) & mask01;
-                const uint32_t d23 = __byte_perm(*reinterpret_cast<const uint16_t *>(R2 + o18),
-                                                 *reinterpret_cast<const uint16_t *>(R3 + o18),
-                                                 0x5410) & mask23;
-                const uint32_t bb[2] = {hmul2u(pb0, d01), hmul2u(pb1, d23)};
-                const int oc = o18 + 2 + 2 * r;
-                const uint32_t z01 = __byte_perm(*reinterpret_cast<const uint16_t *>(R0 + oc),
-                                                 *reinterpret_cast<const uint16_t *>(R1 + oc),
-                                                 0x5410);
-                const uint32_t z23 = __byte_perm(*reinterpret_cast<const uint16_t *>(R2 + oc),
-                                                 *reinterpret_cast<const uint16_t *>(R3 + oc),
-                                                 0x5410);
-                const uint32_t y01 = z01 >> 8, y23 = z23 >> 8;
-                // operands 1024 + c (lo nibbles) and 1024 + 16 c (hi nibbles); the
-                // constant operand right after removes 1032 (1152) times the sum of
-                // the block's P' from every row, leaving c - 8 (16 (c - 8)).
-                const uint32_t alo[4] = {(z01 & 0x000F000Fu) | kMagic, (y01 & 0x000F000Fu) | kMagic,
-                                         (z23 & 0x000F000Fu) | kMagic, (y23 & 0x000F000Fu) | kMagic};
-                const uint32_t ahi[4] = {(z01 & 0x00F000F0u) | kMagic, (y01 & 0x00F000F0u) | kMagic,
-                                         (z23 & 0x00F000F0u) | kMagic, (y23 & 0x00F000F0u) | kMagic};
-                const uint32_t nlo[4] = {kHNeg1032, kHNeg1032, kHNeg1032, kHNeg1032};
-                const uint32_t nhi[4] = {kHNeg1152, kHNeg1152, kHNeg1152, kHNeg1152};
-                mma_16816(o[2 * b][0], alo, bb);
-                mma_16816(o[2 * b][0], nlo, bb);
-                mma_16816(o[2 * b + 1][0], ahi, bb);  // 16 (c - 8): scaled back at the end
-                mma_16816(o[2 * b + 1][0], nhi, bb);
-            }
-        }
-        __syncwarp();
-        // refill this stage with the warp's next tile
-        tiles[s] = issued;
-        if (issued < ntiles) {
-            if (lane == 0) issue(issued, s);
-            issued = next_tile(issued + kWarps);
-        }
-        s = (s + 1 == NST) ? 0 : s + 1;
-    }
-    if (!ok) {
-        // let the copies already issued land before the shared memory is reused
-#pragma unroll
-        for (int st = 0; st < NST; ++st) {
-            if (tiles[st] < ntiles) {
-                const long long c0 = clock64();
-                while (!mbar_try_wait(&bars[st], (phase >> st) & 1u) && clock64() - c0 < kSpinCycles) {
+                for (int k = 0; k < 4; ++k) {
+                    if (h2 == 0) sc0[k] = s4[k];
+                    else sc1[k] = s4[k];
                 }
             }
+            // The scores consumed every byte this warp read from the stage, so
+            // the stage can take the K tile NK places further on.
+            __syncwarp();
+            if (kt < ntiles) {
+                if (lane == 0) issue(kbody, kt, pbase + C::K_OFF + s * C::TILE_ALLOC, &kfull[s]);
+                kt = next_tile(kt + kPairs);
+                ++kn;
+            }
+            // ---- mask and fold: sv[hh][2 h2 + half] is key t0 + 16 h2 + r + 8 half.
+            const int t1 = t0 + kTileKeys - 1;
+            const bool whole = t1 < k_hi && t0 >= ss && (sw <= 0 || t1 <= p - sw) &&
+                               (P.win <= 0 || t0 >= p - P.win + 1);
+            float sv[2][4], pv[2][4];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int key = t0 + 16 * h2 + r + 8 * half;
+                    const bool vis = whole || (key < k_hi && key_visible(p, key, P.sink, P.win) &&
+                                               !(key < ss || (sw > 0 && key > p - sw)));
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh)
+                        sv[hh][2 * h2 + half] = vis ? (h2 ? sc1 : sc0)[2 * half + hh] : -INFINITY;
+                }
+            const float old0 = mu0, old1 = mu1;
+            float o_none[1][1][4] = {};  // O lives in the PV warp
+            fold_scores<1, 1, 4>(sv, P.sl2, kRescaleQ4, mu0, mu1, mt0, mt1, ls0, ls1, o_none, 0, pv);
+            // factor the PV warp applies to O before adding this tile (1: none)
+            const float c0 = (mu0 != old0) ? ex2(old0 - mu0) : 1.0f;
+            const float c1 = (mu1 != old1) ? ex2(old1 - mu1) : 1.0f;
+            // ---- hand P^T (both halves) and the rescale to the PV warp
+            const int ps = seq % kPRing;
+            if (seq >= kPRing) {
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(&pempty[ps], ((seq / kPRing) - 1) & 1, abort, P.err));
+                if (!ok) break;
+            }
+            uint4 *rec = reinterpret_cast<uint4 *>(prec + ps * C::PREC);
+            rec[lane] = make_uint4(movmatrix_trans(pack_half2(pv[0][0], pv[1][0])),
+                                   movmatrix_trans(pack_half2(pv[0][1], pv[1][1])),
+                                   movmatrix_trans(pack_half2(pv[0][2], pv[1][2])),
+                                   movmatrix_trans(pack_half2(pv[0][3], pv[1][3])));
+            rec[32 + lane] = make_uint4(__float_as_uint(c0), __float_as_uint(c1),
+                                        static_cast<uint32_t>(i), 0u);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pfull[ps]);  // release: the record is visible
+            // ---- V tile NV - 1 places ahead, into the stage the PV warp frees
+            // when it finishes the tile before this one
+            if (vt < ntiles) {
+                const int sv_ = vn % NV;
+                if (vn >= NV) {
+                    ok = __all_sync(0xffffffffu,
+                                    mbar_wait(&vempty[sv_], ((vn / NV) - 1) & 1, abort, P.err));
+                    if (!ok) break;
+                }
+                if (lane == 0) issue(vbody, vt, pbase + C::V_OFF + sv_ * C::TILE_ALLOC, &vfull[sv_]);
+                vt = next_tile(vt + kPairs);
+                ++vn;
+            }
         }
+        // end of the sequence for the PV warp
+        if (ok) {
+            const int ps = seq % kPRing;
+            if (seq >= kPRing)
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(&pempty[ps], ((seq / kPRing) - 1) & 1, abort, P.err));
+            if (ok) {
+                uint4 *rec = reinterpret_cast<uint4 *>(prec + ps * C::PREC);
+                rec[32 + lane] = make_uint4(0u, 0u, 0xFFFFFFFFu, 0u);  // tile index: none
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&pfull[ps]);
+            }
+        }
+        if (!ok) {
+            // let the copies already issued land before the shared memory is
+            // reused: wait (bounded) for the last phase of every stage used
+            for (int st = 0; st < NK; ++st)
+                if (kn > st) {
+                    const long long c0 = clock64();
+                    while (!mbar_try_wait(&kfull[st], ((kn - 1 - st) / NK) & 1) &&
+                           clock64() - c0 < kSpinCycles) {
+                    }
+                }
+            for (int st = 0; st < NV; ++st)
+                if (vn > st) {
+                    const long long c0 = clock64();
+                    while (!mbar_try_wait(&vfull[st], ((vn - 1 - st) / NV) & 1) &&
+                           clock64() - c0 < kSpinCycles) {
+                    }
+                }
+        }
+        float m_used[1][2] = {{mu0, mu1}}, m_true[1][2] = {{mt0, mt1}}, lsum[1][2] = {{ls0, ls1}};
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            float v = lsum[0][hh];
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            v += __shfl_xor_sync(0xffffffffu, v, 8);
+            v += __shfl_xor_sync(0xffffffffu, v, 16);
+            lsum[0][hh] = v;
+        }
+        __syncthreads();  // both warps of every pair are done with the stages
+        merge_write_stats<1>(dsmem, pair, m_used, m_true, lsum);
+    } else {
+        // ================================================================ PV warp
+        float o[MT][1][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) o[mt][0][k] = 0.0f;
+        const uint32_t magic = opaque(kMagic);
+        const uint32_t ncorr[4] = {opaque(kHNeg1032), opaque(kHNeg1152), opaque(kHNeg1032),
+                                   opaque(kHNeg1152)};
+        for (int seq = 0;; ++seq) {
+            const int ps = seq % kPRing;
+            ok = __all_sync(0xffffffffu, mbar_wait(&pfull[ps], (seq / kPRing) & 1, abort, P.err));
+            if (!ok) break;
+            const uint4 *rec = reinterpret_cast<const uint4 *>(prec + ps * C::PREC);
+            const uint4 w0 = rec[lane];
+            const uint4 w1 = rec[32 + lane];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pempty[ps]);
+            if (w1.z == 0xFFFFFFFFu) break;  // end of the sequence
+            const int s = seq % NV;
+            ok = __all_sync(0xffffffffu, mbar_wait(&vfull[s], (seq / NV) & 1, abort, P.err));
+            if (!ok) break;
+            const float c0 = __uint_as_float(w1.x), c1 = __uint_as_float(w1.y);
+            if (__any_sync(0xffffffffu, c0 != 1.0f || c1 != 1.0f)) {
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    o[mt][0][0] *= c0;
+                    o[mt][0][2] *= c0;
+                    o[mt][0][1] *= c1;
+                    o[mt][0][3] *= c1;
+                }
+            }
+            uint8_t *Vs = pbase + C::V_OFF + s * C::TILE_ALLOC;
+            const int nk = k_hi - (k_lo + kTileKeys * static_cast<int>(w1.z));
+            if (nk < kTileKeys) {
+                // Rows past the range hold bytes of earlier tiles, bytes the copy
+                // rounded up into, or nothing written yet. Their P is 0; zero
+                // their scales so that 0 * d stays 0 whatever the bytes are.
+                for (int idx = lane; idx < (kTileKeys - nk) * NB; idx += 32)
+                    *reinterpret_cast<uint16_t *>(Vs + (nk + idx / NB) * ROWB +
+                                                  (idx % NB) * kQ4BlockBytes) = 0;
+                fence_proxy_async_smem();  // the next copy into this stage comes after
+                __syncwarp();
+            }
+#pragma unroll 1
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const uint32_t pb0 = h2 ? w0.z : w0.x;
+                const uint32_t pb1 = h2 ? w0.w : w0.y;
+                const uint8_t *R0 = Vs + (16 * h2 + 2 * t) * ROWB;  // key 2t
+                const uint8_t *R1 = R0 + ROWB;                      // key 2t+1
+                const uint8_t *R2 = R0 + 8 * ROWB;                  // key 2t+8
+                const uint8_t *R3 = R2 + ROWB;                      // key 2t+9
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    const int o18 = kQ4BlockBytes * b;
+                    const uint32_t d01 = __byte_perm(*reinterpret_cast<const uint16_t *>(R0 + o18),
+                                                     *reinterpret_cast<const uint16_t *>(R1 + o18),
+                                                     0x5410);
+                    const uint32_t d23 = __byte_perm(*reinterpret_cast<const uint16_t *>(R2 + o18),
+                                                     *reinterpret_cast<const uint16_t *>(R3 + o18),
+                                                     0x5410);
+                    const uint32_t bb[2] = {hmul2u(pb0, d01), hmul2u(pb1, d23)};
+                    const int oc = o18 + 2 + 2 * r;
+                    const uint32_t z01 = __byte_perm(*reinterpret_cast<const uint16_t *>(R0 + oc),
+                                                     *reinterpret_cast<const uint16_t *>(R1 + oc),
+                                                     0x5410);
+                    const uint32_t z23 = __byte_perm(*reinterpret_cast<const uint16_t *>(R2 + oc),
+                                                     *reinterpret_cast<const uint16_t *>(R3 + oc),
+                                                     0x5410);
+                    const uint32_t y01 = z01 >> 8, y23 = z23 >> 8;
+                    // m-tile 2b + j: row r is element 2r + j (operand 1024 + c),
+                    // row r + 8 element 16 + 2r + j (operand 1024 + 16 c). The
+                    // constant operand right after removes 1032 (row r) or 1152
+                    // (row r + 8) times the sum of the block's P' from the rows.
+                    const uint32_t ax[4] = {and_or<0x000F000Fu>(z01, magic), and_or<0x00F000F0u>(z01, magic),
+                                            and_or<0x000F000Fu>(z23, magic), and_or<0x00F000F0u>(z23, magic)};
+                    const uint32_t ay[4] = {and_or<0x000F000Fu>(y01, magic), and_or<0x00F000F0u>(y01, magic),
+                                            and_or<0x000F000Fu>(y23, magic), and_or<0x00F000F0u>(y23, magic)};
+                    mma_16816(o[2 * b][0], ax, bb);
+                    mma_16816(o[2 * b][0], ncorr, bb);
+                    mma_16816(o[2 * b + 1][0], ay, bb);
+                    mma_16816(o[2 * b + 1][0], ncorr, bb);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&vempty[s]);
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {  // rows r + 8 carry 16 (c - 8)
+            o[mt][0][2] *= 0.0625f;
+            o[mt][0][3] *= 0.0625f;
+        }
+        __syncthreads();  // pairs with the QK warps' barrier above
+        merge_write_o<HD, 1, true>(dsmem, pair, o);
     }
-#pragma unroll
-    for (int mt = 1; mt < MT; mt += 2)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) o[mt][0][k] *= 0.0625f;
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-        float v = lsum[0][hh];
-        v += __shfl_xor_sync(0xffffffffu, v, 4);
-        v += __shfl_xor_sync(0xffffffffu, v, 8);
-        v += __shfl_xor_sync(0xffffffffu, v, 16);
-        lsum[0][hh] = v;
-    }
-    merge_and_write<HD, 1, true>(P, dsmem, head0, G, e, m_used, m_true, lsum, o);
+    merge_finish<HD>(P, dsmem, head0, G, e);
 }
 
 template <int HD>
-__global__ void __launch_bounds__(kWarps * 32, FA_Q4_MIN_BLOCKS)
+__global__ void __launch_bounds__(2 * kPairs * 32, FA_Q4_MIN_BLOCKS)
     decode_q4_kernel(const DecodeParams P) {
     extern __shared__ __align__(128) uint8_t dsmem[];
     const int e = blockIdx.x, g = blockIdx.y, u = blockIdx.z;
@@ -885,7 +1044,7 @@ cudaError_t launch_q4(const DecodeParams &P, cudaStream_t stream) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid(P.entries, P.Hkv, P.nslots);
-    decode_q4_kernel<HD><<<grid, kWarps * 32, C::SMEM, stream>>>(P);
+    decode_q4_kernel<HD><<<grid, 2 * kPairs * 32, C::SMEM, stream>>>(P);
     return cudaGetLastError();
 }
 
@@ -895,11 +1054,11 @@ DecodeShape decode_shape(int nslots, int n_q_heads, int n_kv_heads, int kv_fmt, 
                          int shadow_win, int max_splits, int max_seq, size_t row_bytes) {
     DecodeShape d;
     const int G = n_q_heads / n_kv_heads;
-    // The Q4_0 path bulk-copies rows [t0, t0+32) of a kv head; the copy must
-    // start 16-byte aligned, so every head's body must start 16-byte aligned.
+    // The Q4_0 path bulk-copies rows of a kv head; a copy must start 16-byte
+    // aligned, so every head's body must start 16-byte aligned.
     d.fast = kv_fmt == 1 && G <= 8 && (static_cast<size_t>(max_seq) * row_bytes) % 16 == 0;
-    // Blocks per wave: the Q4_0 path keeps 2 blocks per SM; aim at about four
-    // waves so the last one is short.
+    // Blocks to aim at: the Q4_0 path keeps 2 blocks per SM, so 8 per SM is
+    // about four waves and the last one is short; the generic path, 4 per SM.
     const long long pairs = static_cast<long long>(nslots) * n_kv_heads;
     const long long target = (d.fast ? 8LL : 4LL) * device_sm_count();
     long long cpc = (pairs * max_splits + target - 1) / target;

@@ -19,6 +19,22 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Shared-memory loads the compiler keeps where they are written (not hoisted
+// into registers across a loop), for operands re-read every iteration.
+__device__ __forceinline__ uint4 lds_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_u32(p)));
+    return v;
+}
+__device__ __forceinline__ float4 lds_f4(const void *p) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(smem_u32(p)));
+    return v;
+}
 __device__ __forceinline__ void flag_error(unsigned *err, unsigned bit) {
     if (err) atomicOr(err, bit);
 }
