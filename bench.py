@@ -487,9 +487,11 @@ def main():
         extra[w.name] = {"value": kvb / (statistics.mean(sm) * 1e-3) / 1e9, "unit": "GB/s",
                          "ms_per_step": statistics.mean(sm), "kv_bytes_per_step": kvb,
                          "step": "append 1 row/slot + split decode + combine",
-                         "roofline": {"kernel": "decode_kernel<256,1>", "bound": "hbm",
+                         "roofline": {"kernel": "decode_q4_kernel<256>", "bound": "hbm",
                                       "achieved": a, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                       "frac": a / peaks["hbm_gbs"], "frac_of_8tbs": a / 8000.0,
+                                      "traffic": profiled_traffic("decode_q4_kernel<256>",
+                                                                  src_hash("decode.cu")),
                                       "kernel_ms": statistics.mean(km)}}
         del S
         torch.cuda.empty_cache()
