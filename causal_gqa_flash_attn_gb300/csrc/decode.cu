@@ -488,6 +488,17 @@ constexpr int kPRing = 2;      // P records in flight per pair
 #ifndef FA_Q4_MIN_BLOCKS
 #define FA_Q4_MIN_BLOCKS 2
 #endif
+// Unroll factors (1 or 2) of the loops over a tile's two 16-key halves in the
+// QK and PV warps: 2 interleaves the halves' dependency chains, 1 keeps the
+// registers and the code small.
+#ifndef FA_Q4_QK_HALVES
+#define FA_Q4_QK_HALVES 2
+#endif
+#ifndef FA_Q4_PV_HALVES
+#define FA_Q4_PV_HALVES 1
+#endif
+constexpr int kQKHalves = FA_Q4_QK_HALVES;
+constexpr int kPVHalves = FA_Q4_PV_HALVES;
 
 template <int HD>
 struct Q4Cfg {
@@ -689,7 +700,7 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
             const int t0 = k_lo + kTileKeys * i;
             // ---- scores: half h2 holds keys t0 + 16 h2 + {r, r+8}
             float sc0[4], sc1[4];
-#pragma unroll 1
+#pragma unroll kQKHalves
             for (int h2 = 0; h2 < 2; ++h2) {
                 const uint8_t *KA = Ks + (16 * h2 + r) * ROWB;
                 const uint8_t *KB = KA + 8 * ROWB;
@@ -886,7 +897,7 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
                 fence_proxy_async_smem();  // the next copy into this stage comes after
                 __syncwarp();
             }
-#pragma unroll 1
+#pragma unroll kPVHalves
             for (int h2 = 0; h2 < 2; ++h2) {
                 const uint32_t pb0 = h2 ? w0.z : w0.x;
                 const uint32_t pb1 = h2 ? w0.w : w0.y;
