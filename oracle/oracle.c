@@ -243,13 +243,15 @@ static const double *oracle_key_row(const double *body, const double *f16, int p
     return body + off;
 }
 
-/* out[r][h][:] for query rows r at positions qpos[r] (q: [nq][Hq][hd] float).
- * Returns 0, or -1 if a position is out of range, -2 if a query has no
- * visible key (impossible: p always sees itself). */
+/* out[r][h][:] for query rows r at positions qpos[r] (q: [nq][Hq][hd] float),
+ * and, when lse is not NULL, lse[r][h] = log(sum_j exp(s_j)) = m + log(sum_j
+ * exp(s_j - m)), the log-sum-exp of the row's scores ([B] MergeAttnStates
+ * consumes it). Returns 0, or -1 if a position is out of range, -2 if a query
+ * has no visible key (impossible: p always sees itself). */
 int oracle_attention(const float *q, const int *qpos, int nq, int Hq, int Hkv, int hd, int L,
                      const double *kbody, const double *vbody, const double *kf16,
                      const double *vf16, int shadow_sink, int shadow_win, int sink, int win,
-                     double scale, double *out) {
+                     double scale, double *out, double *lse) {
     if (Hkv <= 0 || Hq % Hkv != 0)
         return -1;
     const int G = Hq / Hkv;
@@ -303,9 +305,54 @@ int oracle_attention(const float *q, const int *qpos, int nq, int Hq, int Hkv, i
         }
         for (int e = 0; e < hd; e++)
             o[e] /= den;
+        if (lse)
+            lse[rh] = m + log(den);
         free(sc);
     }
     return status;
+}
+
+/* [B] MergeAttnStates: two attention results over disjoint key sets, each with
+ * its log-sum-exp, combined into the result over the union. Per token t and
+ * head h (outputs [T][H][D], lses [H][T]):
+ *   - tokens t >= with_context (when with_context >= 0) take the suffix output
+ *     and its lse unchanged;
+ *   - an lse of +inf counts as -inf;
+ *   - if both lses are -inf (no key on either side) the output is the prefix
+ *     output and the lse is -inf;
+ *   - otherwise m = max(lp, ls), wp = exp(lp - m), ws = exp(ls - m),
+ *     out = prefix * wp/(wp+ws) + suffix * ws/(wp+ws), lse = log(wp+ws) + m.
+ * Inputs are float (the tensors' type), arithmetic fp64. */
+void oracle_merge_attn_states(const float *prefix, const float *prefix_lse, const float *suffix,
+                              const float *suffix_lse, int T, int H, int D, int with_context,
+                              double *out, double *out_lse) {
+    for (int t = 0; t < T; t++)
+        for (int h = 0; h < H; h++) {
+            const int64_t row = ((int64_t)t * H + h) * D;
+            const int64_t li = (int64_t)h * T + t;
+            if (with_context >= 0 && t >= with_context) {
+                for (int d = 0; d < D; d++)
+                    out[row + d] = suffix[row + d];
+                out_lse[li] = suffix_lse[li];
+                continue;
+            }
+            double lp = prefix_lse[li], ls = suffix_lse[li];
+            if (lp == INFINITY)
+                lp = -INFINITY;
+            if (ls == INFINITY)
+                ls = -INFINITY;
+            const double m = lp > ls ? lp : ls;
+            if (m == -INFINITY) {
+                for (int d = 0; d < D; d++)
+                    out[row + d] = prefix[row + d];
+                out_lse[li] = -INFINITY;
+                continue;
+            }
+            const double wp = exp(lp - m), ws = exp(ls - m), tot = wp + ws;
+            for (int d = 0; d < D; d++)
+                out[row + d] = prefix[row + d] * (wp / tot) + suffix[row + d] * (ws / tot);
+            out_lse[li] = log(tot) + m;
+        }
 }
 
 /* -------------------------------------------------- split-KV decode + merge */

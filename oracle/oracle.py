@@ -59,7 +59,9 @@ def lib():
         L.oracle_reads_fp16.argtypes = [i32, i32, i32, i32, i32]
         L.oracle_attention.restype = i32
         L.oracle_attention.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P,
-                                       i32, i32, i32, i32, f64, P]
+                                       i32, i32, i32, i32, f64, P, P]
+        L.oracle_merge_attn_states.restype = None
+        L.oracle_merge_attn_states.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P]
         L.oracle_dec_plan.restype = i32
         L.oracle_dec_plan.argtypes = [i32, i32, i32, ctypes.POINTER(i32)]
         L.oracle_partial.argtypes = [P, i32, i32, i32, i32, i32, i32, i32, P, P, P, P,
@@ -166,8 +168,9 @@ class KVValues:
 
 def attention(q, qpos, kv_k: KVValues, kv_v: KVValues, *, sink: int, win: int,
               shadow_sink: int = 0, shadow_win: int = 0, scale: float | None = None,
-              L: int | None = None) -> np.ndarray:
-    """out [nq][Hq][hd] float64 for query rows q [nq][Hq][hd] at positions qpos.
+              L: int | None = None, with_lse: bool = False):
+    """out [nq][Hq][hd] float64 for query rows q [nq][Hq][hd] at positions qpos;
+    with with_lse, also lse [nq][Hq] = log sum_j exp(s_j) of each row's scores.
 
     L is the number of rows in the cache (last appended row L-1), which decides
     the fp16 ring liveness of a Q4_0 cache; it defaults to the cache size."""
@@ -181,29 +184,51 @@ def attention(q, qpos, kv_k: KVValues, kv_v: KVValues, *, sink: int, win: int,
     if scale is None:
         scale = 1.0 / math.sqrt(hd)
     out = np.empty((nq, Hq, hd), np.float64)
+    lse = np.empty((nq, Hq), np.float64) if with_lse else None
     kf = kv_k.f16 if kv_k.f16 is not None else None
     vf = kv_v.f16 if kv_v.f16 is not None else None
     st = lib().oracle_attention(
         _ptr(q), _ptr(qpos), nq, Hq, Hkv, hd, L, _ptr(kv_k.body), _ptr(kv_v.body),
         _ptr(kf) if kf is not None else None, _ptr(vf) if vf is not None else None,
-        shadow_sink, shadow_win, sink, win, float(scale), _ptr(out))
+        shadow_sink, shadow_win, sink, win, float(scale), _ptr(out),
+        _ptr(lse) if lse is not None else None)
     if st != 0:
         raise ValueError(f"oracle_attention failed with status {st}")
-    return out
+    return (out, lse) if with_lse else out
 
 
 def prefill(q, k, v, *, kv_fmt: str, sink: int, win: int, shadow_sink: int = 0,
-            shadow_win: int = 0, rows=None) -> np.ndarray:
+            shadow_win: int = 0, rows=None, with_lse: bool = False):
     """Prefill with pos0 = 0: query t at position t over the n appended rows.
 
-    rows selects query rows (default all); returns [len(rows)][Hq][hd]."""
+    rows selects query rows (default all); returns [len(rows)][Hq][hd], and
+    with with_lse also the rows' lse [len(rows)][Hq]."""
     n = q.shape[0]
     if rows is None:
         rows = np.arange(n, dtype=np.int32)
     rows = np.asarray(rows, dtype=np.int32)
     kk, vv = KVValues(k, kv_fmt), KVValues(v, kv_fmt)
     return attention(q[rows], rows, kk, vv, sink=sink, win=win, shadow_sink=shadow_sink,
-                     shadow_win=shadow_win, L=n)
+                     shadow_win=shadow_win, L=n, with_lse=with_lse)
+
+
+def merge_attn_states(prefix, prefix_lse, suffix, suffix_lse, with_context: int = -1):
+    """[B] MergeAttnStates on float32 inputs: outputs [T][H][D], lses [H][T].
+
+    Returns (out [T][H][D], out_lse [H][T]) in float64; tokens t >=
+    with_context (when >= 0) take the suffix unchanged."""
+    prefix = np.ascontiguousarray(prefix, dtype=np.float32)
+    suffix = np.ascontiguousarray(suffix, dtype=np.float32)
+    prefix_lse = np.ascontiguousarray(prefix_lse, dtype=np.float32)
+    suffix_lse = np.ascontiguousarray(suffix_lse, dtype=np.float32)
+    T, H, D = prefix.shape
+    assert suffix.shape == (T, H, D) and prefix_lse.shape == (H, T) == suffix_lse.shape
+    out = np.empty((T, H, D), np.float64)
+    out_lse = np.empty((H, T), np.float64)
+    lib().oracle_merge_attn_states(_ptr(prefix), _ptr(prefix_lse), _ptr(suffix),
+                                   _ptr(suffix_lse), T, H, D, int(with_context), _ptr(out),
+                                   _ptr(out_lse))
+    return out, out_lse
 
 
 # ------------------------------------------------- split-KV decode + merge

@@ -388,3 +388,95 @@ def test_combine_closed_form(oracle_mod):
     np.testing.assert_allclose(oracle_mod.combine(m, l, acc), want, rtol=1e-15)
     with pytest.raises(ValueError):
         oracle_mod.combine(np.array([-np.inf]), np.array([0.0]), np.zeros((1, 2)))
+
+
+# ------------------------------------------- log-sum-exp and state merging
+
+def test_lse_of_a_single_key(oracle_mod):
+    """Causal row 0 sees key 0 only: its lse is that one score, scale q.k0."""
+    from workloads import prefill_inputs
+    q, k, v = prefill_inputs(5, 4, 2, 32, seed=41)
+    _, lse = oracle_mod.prefill(q, k, v, kv_fmt="f32", sink=0, win=0, with_lse=True)
+    for h in range(4):
+        want = (1.0 / math.sqrt(32)) * float(np.dot(q[0, h].astype(np.float64),
+                                                    k[0, h // 2].astype(np.float64)))
+        assert lse[0, h] == pytest.approx(want, rel=1e-13, abs=1e-13)
+
+
+def test_lse_of_equal_scores_counts_the_visible_keys(oracle_mod):
+    """With every key row equal, all visible scores are one value s, so
+    lse = s + log |S(p)|, which counts the attended set."""
+    from workloads import prefill_inputs
+    n, hd = 60, 32
+    q, k, v = prefill_inputs(n, 2, 1, hd, seed=42)
+    k[:] = k[7]
+    for sink, win in ((0, 0), (3, 10), (0, 1)):
+        _, lse = oracle_mod.prefill(q, k, v, kv_fmt="f32", sink=sink, win=win, with_lse=True)
+        for p in (0, 1, 9, 30, n - 1):
+            count = sum(oracle_mod.visible(p, j, sink, win) for j in range(p + 1))
+            for h in range(2):
+                s = (1.0 / math.sqrt(hd)) * float(np.dot(q[p, h].astype(np.float64),
+                                                         k[0, 0].astype(np.float64)))
+                assert lse[p, h] == pytest.approx(s + math.log(count), rel=1e-12, abs=1e-12)
+
+
+def test_merge_of_disjoint_states_is_the_union(oracle_mod):
+    """Attention over keys [0, c) and over [c, p] (each normalised, with its
+    lse) merge into attention over [0, p] and its lse."""
+    from workloads import decode_slot_inputs
+    L, H, D = 300, 4, 64
+    q, k, v = decode_slot_inputs(L, H, 2, D, seed=43, slot=1)
+    p = L - 1
+    kk, vv = oracle_mod.KVValues(k, "f32"), oracle_mod.KVValues(v, "f32")
+    full, full_lse = oracle_mod.attention(q[None], np.array([p], np.int32), kk, vv, sink=0,
+                                          win=0, with_lse=True)
+    for c in (1, 17, 150, 299):
+        states = []
+        for lo, hi in ((0, c), (c, L)):
+            m, l, acc = oracle_mod.partial(q, p, lo, hi, kk, vv, sink=0, win=0)
+            states.append((acc / l[:, None], m + np.log(l)))
+        (po, pl), (so, sl) = states
+        out, lse = oracle_mod.merge_attn_states(po[None], pl[:, None], so[None], sl[:, None])
+        np.testing.assert_allclose(out[0], full[0], rtol=2e-6, atol=2e-6)
+        np.testing.assert_allclose(lse[:, 0], full_lse[0], rtol=1e-6, atol=1e-6)
+
+
+def test_merge_edge_cases_stated_by_the_pages(oracle_mod):
+    """"vt/ops.h" MergeAttnStates: +inf lse counts as -inf; both -inf gives
+    the prefix output and -inf; tokens from with_context on take the suffix."""
+    T, H, D = 4, 2, 8
+    rng = np.random.default_rng(5)
+    po = rng.standard_normal((T, H, D)).astype(np.float32)
+    so = rng.standard_normal((T, H, D)).astype(np.float32)
+    pl = np.array([[np.inf, -np.inf, 0.5, -np.inf], [1.0, 2.0, np.inf, 0.0]], np.float32)
+    sl = np.array([[0.25, -np.inf, 0.5, 3.0], [1.0, np.inf, np.inf, -np.inf]], np.float32)
+    out, lse = oracle_mod.merge_attn_states(po, pl, so, sl)
+    # token 0, head 0: prefix +inf -> -inf, so the suffix alone
+    np.testing.assert_array_equal(out[0, 0], so[0, 0])
+    assert lse[0, 0] == np.float32(0.25)
+    # token 1, head 0: both -inf -> prefix output, lse -inf
+    np.testing.assert_array_equal(out[1, 0], po[1, 0])
+    assert lse[0, 1] == -np.inf
+    # token 2, head 0: equal lses -> the mean, lse + log 2
+    np.testing.assert_allclose(out[2, 0], (po[2, 0].astype(np.float64) + so[2, 0]) / 2,
+                               rtol=1e-15)
+    assert lse[0, 2] == pytest.approx(0.5 + math.log(2.0), rel=1e-15)
+    # token 3, head 0: prefix -inf -> the suffix alone
+    np.testing.assert_array_equal(out[3, 0], so[3, 0])
+    # token 0, head 1: equal finite lses
+    np.testing.assert_allclose(out[0, 1], (po[0, 1].astype(np.float64) + so[0, 1]) / 2,
+                               rtol=1e-15)
+    # token 1, head 1: suffix +inf -> -inf, the prefix alone, its lse
+    np.testing.assert_array_equal(out[1, 1], po[1, 1])
+    assert lse[1, 1] == np.float32(2.0)
+    # token 2, head 1: both +inf -> both -inf -> prefix output, -inf
+    np.testing.assert_array_equal(out[2, 1], po[2, 1])
+    assert lse[1, 2] == -np.inf
+    # token 3, head 1: weights 1 and e^-inf = 0 -> the prefix
+    np.testing.assert_array_equal(out[3, 1], po[3, 1])
+    assert lse[1, 3] == 0.0
+    # tokens from with_context = 2 on take the suffix output and lse verbatim
+    out2, lse2 = oracle_mod.merge_attn_states(po, pl, so, sl, with_context=2)
+    np.testing.assert_array_equal(out2[2:], so[2:])
+    np.testing.assert_array_equal(lse2[:, 2:], sl[:, 2:])
+    np.testing.assert_array_equal(out2[:2], out[:2])
