@@ -496,6 +496,30 @@ def main():
         del S
         torch.cuda.empty_cache()
 
+    if not args.no_decode:
+        # merge of two attention states (fp32 outputs [T][H][D], lses [H][T]):
+        # the context-chunk + new-tokens combination of chunked prefill
+        T, H, D = 8192, 16, 256
+        g = torch.Generator(device=dev).manual_seed(20261202)
+        po = torch.randn(T, H, D, device=dev, generator=g)
+        so = torch.randn(T, H, D, device=dev, generator=g)
+        pl = torch.randn(H, T, device=dev, generator=g) * 4
+        sl = torch.randn(H, T, device=dev, generator=g) * 4
+        mo = torch.empty_like(po)
+        ml = torch.empty_like(pl)
+        mbytes = 3 * T * H * D * 4 + 3 * H * T * 4
+        sm, _ = B.timed_steps(lambda: B.fa.merge_attn_states(mo, ml, po, pl, so, sl),
+                              args.warmup, args.steps, kernel_events=False)
+        a = mbytes / (statistics.mean(sm) * 1e-3) / 1e9
+        extra["merge_attn_states_t8192_h16_d256"] = {
+            "value": a, "unit": "GB/s", "ms_per_step": statistics.mean(sm),
+            "bytes_per_step": mbytes, "step": "fa_merge_attn_states",
+            "roofline": {"kernel": "merge_attn_states_kernel", "bound": "hbm", "achieved": a,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": a / peaks["hbm_gbs"],
+                         "kernel_ms": statistics.mean(sm)}}
+        del po, so, pl, sl, mo, ml
+        torch.cuda.empty_cache()
+
     if rank == 0:
         print(json.dumps({
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,

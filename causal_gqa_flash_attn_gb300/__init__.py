@@ -35,6 +35,9 @@ SIGNATURES = {
     "fa_prefill_tile_shape": (_I, [_I, _P, _P]),
     "fa_prefill": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _SZ, _P,
                         _P]),
+    "fa_prefill_lse": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _SZ,
+                            _P, _P]),
+    "fa_merge_attn_states": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "fa_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "fa_decode": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _SZ,
                        _P]),
@@ -152,14 +155,31 @@ def prefill_tile_shape(head_dim: int):
 
 def prefill(q, k, v, out, n: int, n_q_heads: int, n_kv_heads: int, head_dim: int, sink: int,
             win: int, kv_fmt: int, *, max_seq: int, shadow_sink: int = 0, shadow_win: int = 0,
-            workspace: torch.Tensor, tile_map: torch.Tensor | None = None, stream=None):
-    """fa_prefill: q/out [n][Hq][hd] fp32, k/v one plane each (uint8 tensors)."""
-    _check(lib().fa_prefill(
-        _dev(q, torch.float32, "q"), _dev(k, torch.uint8, "k"), _dev(v, torch.uint8, "v"),
-        _dev(out, torch.float32, "out"), n, n_q_heads, n_kv_heads, head_dim, sink, win, kv_fmt,
-        max_seq, shadow_sink, shadow_win, _dev(workspace, torch.uint8, "workspace"),
-        workspace.numel(), _dev(tile_map, torch.uint8, "tile_map"), _stream(stream)),
-        "fa_prefill")
+            workspace: torch.Tensor, tile_map: torch.Tensor | None = None,
+            lse: torch.Tensor | None = None, stream=None):
+    """fa_prefill (fa_prefill_lse when lse [Hq][n] fp32 is given): q/out
+    [n][Hq][hd] fp32, k/v one plane each (uint8 tensors)."""
+    args = (_dev(q, torch.float32, "q"), _dev(k, torch.uint8, "k"), _dev(v, torch.uint8, "v"),
+            _dev(out, torch.float32, "out"))
+    rest = (n, n_q_heads, n_kv_heads, head_dim, sink, win, kv_fmt, max_seq, shadow_sink,
+            shadow_win, _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+            _dev(tile_map, torch.uint8, "tile_map"), _stream(stream))
+    if lse is None:
+        _check(lib().fa_prefill(*args, *rest), "fa_prefill")
+    else:
+        _check(lib().fa_prefill_lse(*args, _dev(lse, torch.float32, "lse"), *rest),
+               "fa_prefill_lse")
+
+
+def merge_attn_states(out, out_lse, prefix, prefix_lse, suffix, suffix_lse, *,
+                      prefill_tokens_with_context: int = -1, stream=None):
+    """fa_merge_attn_states: outputs [T][H][D] fp32, lses [H][T] fp32 (out_lse may be None)."""
+    T, H, D = prefix.shape
+    _check(lib().fa_merge_attn_states(
+        _dev(out, torch.float32, "out"), _dev(out_lse, torch.float32, "out_lse"),
+        _dev(prefix, torch.float32, "prefix"), _dev(prefix_lse, torch.float32, "prefix_lse"),
+        _dev(suffix, torch.float32, "suffix"), _dev(suffix_lse, torch.float32, "suffix_lse"),
+        T, H, D, prefill_tokens_with_context, _stream(stream)), "fa_merge_attn_states")
 
 
 # ------------------------------------------------------------------ decode

@@ -213,6 +213,16 @@ fa_status fa_prefill(const float *q, const void *k, const void *v, float *out, i
                      int n_q_heads, int n_kv_heads, int head_dim, int sink, int win, int kv_fmt,
                      int max_seq, int shadow_sink, int shadow_win, void *workspace,
                      size_t workspace_bytes, uint8_t *tile_map, fa_stream_t stream) {
+    return fa_prefill_lse(q, k, v, out, nullptr, n, n_q_heads, n_kv_heads, head_dim, sink, win,
+                          kv_fmt, max_seq, shadow_sink, shadow_win, workspace, workspace_bytes,
+                          tile_map, stream);
+}
+
+fa_status fa_prefill_lse(const float *q, const void *k, const void *v, float *out, float *lse,
+                         int n, int n_q_heads, int n_kv_heads, int head_dim, int sink, int win,
+                         int kv_fmt, int max_seq, int shadow_sink, int shadow_win,
+                         void *workspace, size_t workspace_bytes, uint8_t *tile_map,
+                         fa_stream_t stream) {
     fa_status st = check_heads(n_q_heads, n_kv_heads, head_dim);
     if (st != FA_OK) return st;
     if (n < 0 || sink < 0 || max_seq < 1 || n > max_seq) return FA_ERR_INVALID;
@@ -223,7 +233,7 @@ fa_status fa_prefill(const float *q, const void *k, const void *v, float *out, i
     if (n == 0) return FA_OK;
     if (!q || !k || !v || !out || !workspace) return FA_ERR_INVALID;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
-        !aligned16(workspace))
+        !aligned16(workspace) || (reinterpret_cast<uintptr_t>(lse) & 3u))
         return FA_ERR_INVALID;
     const PrefillWs w = prefill_ws(n, n_q_heads, n_kv_heads, head_dim);
     if (workspace_bytes < w.bytes) return FA_ERR_WORKSPACE;
@@ -253,6 +263,7 @@ fa_status fa_prefill(const float *q, const void *k, const void *v, float *out, i
     a.out = out;
     a.tile_map = tile_map;
     a.work_counter = ctr;
+    a.lse = lse;
     a.n = n;
     a.n_q_heads = n_q_heads;
     a.n_kv_heads = n_kv_heads;
@@ -357,3 +368,20 @@ fa_status fa_get_device_error(fa_stream_t stream) {
 }
 
 }  // extern "C"
+
+fa_status fa_merge_attn_states(float *out, float *out_lse, const float *prefix,
+                               const float *prefix_lse, const float *suffix,
+                               const float *suffix_lse, int num_tokens, int n_heads, int head_dim,
+                               int prefill_tokens_with_context, fa_stream_t stream) {
+    if (num_tokens < 0 || n_heads < 1 || head_dim < 4 || head_dim % 4) return FA_ERR_INVALID;
+    if (num_tokens == 0) return FA_OK;
+    if (!out || !prefix || !prefix_lse || !suffix || !suffix_lse) return FA_ERR_INVALID;
+    if (!aligned16(out) || !aligned16(prefix) || !aligned16(suffix) ||
+        (reinterpret_cast<uintptr_t>(prefix_lse) & 3u) ||
+        (reinterpret_cast<uintptr_t>(suffix_lse) & 3u) ||
+        (reinterpret_cast<uintptr_t>(out_lse) & 3u))
+        return FA_ERR_INVALID;
+    return from_cuda(fa::launch_merge_attn_states(
+        out, out_lse, prefix, prefix_lse, suffix, suffix_lse, num_tokens, n_heads, head_dim,
+        prefill_tokens_with_context, reinterpret_cast<cudaStream_t>(stream)));
+}

@@ -55,12 +55,19 @@ struct PrefillArgs {
     float *out;         // [n][Hq][hd] fp32
     uint8_t *tile_map;  // optional
     unsigned *work_counter;  // prefill work queue, zeroed by launch_stage_q
+    float *lse;              // optional [Hq][n] fp32: log sum_j exp(s_j) per row
     int n, n_q_heads, n_kv_heads, head_dim, sink, win;
     float scale;
 };
 constexpr int kPrefillBQ = 128;
 constexpr int kPrefillBK = 128;
 cudaError_t launch_prefill_tc(const PrefillArgs &a, unsigned *err, cudaStream_t stream);
+
+// ---- merge.cu
+cudaError_t launch_merge_attn_states(float *out, float *out_lse, const float *prefix,
+                                     const float *prefix_lse, const float *suffix,
+                                     const float *suffix_lse, int T, int H, int D,
+                                     int with_context, cudaStream_t stream);
 
 // ---- decode.cu
 struct DecodeArgs {

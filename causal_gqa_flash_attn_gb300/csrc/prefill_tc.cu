@@ -129,14 +129,16 @@ struct Unit {
     int qt, h;
 };
 
-template <int HD>
+// LSE: also write each row's log-sum-exp (a separate instantiation, so that
+// the plain prefill keeps its own register allocation).
+template <int HD, bool LSE>
 __global__ void __launch_bounds__(256, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_o, uint8_t *__restrict__ tile_map,
-                      unsigned *__restrict__ work_counter, int n, int Hq, int Hkv, int sink,
-                      int win, float sl2, unsigned *err) {
+                      unsigned *__restrict__ work_counter, float *__restrict__ lse, int n,
+                      int Hq, int Hkv, int sink, int win, float sl2, unsigned *err) {
     using C = Cfg<HD>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -467,6 +469,9 @@ __global__ void __launch_bounds__(256, 1)
             if (!ok) break;
             tc_fence_after();
             const float inv = 1.0f / l;
+            // log sum_j exp(s_j) = ln 2 * m_used + ln l (l is relative to 2^m_used)
+            if (LSE && p < n)
+                lse[static_cast<size_t>(u.h) * n + p] = m_used * 0.69314718055994531f + logf(l);
             const int wr = warp & 3;  // rows 32 wr .. 32 wr + 31 of the tile
 #pragma unroll 1
             for (int c = 0; c < HD / 32; ++c) {
@@ -559,16 +564,17 @@ cudaError_t launch_hd(const PrefillArgs &a, unsigned *err, cudaStream_t stream) 
         !encode_3d(&to, a.out, HD, Hq, n, HD * 4, Hq * HD * 4, 32, 1, 32,
                    CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<HD>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    auto kernel = a.lse ? prefill_tc_kernel<HD, true> : prefill_tc_kernel<HD, false>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     const int nqt = (a.n + C::BQ - 1) / C::BQ;
     const int units = nqt * a.n_q_heads;
     const int grid = units < device_sm_count() ? units : device_sm_count();
     const float sl2 = a.scale * 1.4426950408889634f;
-    prefill_tc_kernel<HD><<<grid, 256, C::SMEM, stream>>>(
-        tq, tk, tv, to, a.tile_map, a.work_counter, a.n, a.n_q_heads, a.n_kv_heads, a.sink, a.win,
-        sl2, err);
+    kernel<<<grid, 256, C::SMEM, stream>>>(
+        tq, tk, tv, to, a.tile_map, a.work_counter, a.lse, a.n, a.n_q_heads, a.n_kv_heads, a.sink,
+        a.win, sl2, err);
     return cudaGetLastError();
 }
 

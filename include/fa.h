@@ -164,6 +164,44 @@ fa_status fa_prefill(const float *q, const void *k, const void *v, float *out, i
                      void *workspace, size_t workspace_bytes, uint8_t *tile_map,
                      fa_stream_t stream);
 
+/* fa_prefill that also writes the log-sum-exp of every query row's scores,
+ * the second input of fa_merge_attn_states ("vt/ops.h" MergeAttnStates):
+ *   lse[h][t] = log sum_{j in S(t)} exp(scale * q[t][h] . k[j])   (natural log)
+ *   lse        [n_q_heads][n] fp32 (device, 4-byte aligned), written; NULL
+ *              makes this call fa_prefill.
+ * Every other argument, requirement and status is fa_prefill's. */
+fa_status fa_prefill_lse(const float *q, const void *k, const void *v, float *out, float *lse,
+                         int n, int n_q_heads, int n_kv_heads, int head_dim, int sink, int win,
+                         int kv_fmt, int max_seq, int shadow_sink, int shadow_win,
+                         void *workspace, size_t workspace_bytes, uint8_t *tile_map,
+                         fa_stream_t stream);
+
+/* ------------------------------------------------------- attention-state merge
+ *
+ * Merge of two attention results over disjoint key sets by their log-sum-exps
+ * ("vt/ops.h" (vllm-cpp-sys), MergeAttnStates, after section 2.2 of the paper
+ * it cites): for token t and head h, with lp = prefix_lse[h][t] and
+ * ls = suffix_lse[h][t],
+ *   - t >= prefill_tokens_with_context (when that is >= 0): out and out_lse
+ *     are the suffix's, unchanged;
+ *   - an lse of +inf counts as -inf;
+ *   - lp = ls = -inf (no key on either side): out = the prefix output,
+ *     out_lse = -inf;
+ *   - otherwise m = max(lp, ls), wp = exp(lp - m), ws = exp(ls - m):
+ *     out = prefix * wp/(wp+ws) + suffix * ws/(wp+ws), out_lse = log(wp+ws) + m.
+ * Arithmetic is fp32.
+ *   out, prefix, suffix   [num_tokens][n_heads][head_dim] fp32 (device,
+ *                         16-byte aligned); out must not overlap the inputs.
+ *   out_lse               [n_heads][num_tokens] fp32 (device) or NULL.
+ *   prefix_lse, suffix_lse [n_heads][num_tokens] fp32 (device).
+ *   head_dim              a multiple of 4.
+ * FA_ERR_INVALID for a bad size, a NULL input or a misaligned pointer, before
+ * any launch. */
+fa_status fa_merge_attn_states(float *out, float *out_lse, const float *prefix,
+                               const float *prefix_lse, const float *suffix,
+                               const float *suffix_lse, int num_tokens, int n_heads, int head_dim,
+                               int prefill_tokens_with_context, fa_stream_t stream);
+
 /* ------------------------------------------------------------------- decode
  *
  * Multi-slot split-KV decode ("attention.cu", "Decode-mode flash attention"

@@ -123,3 +123,28 @@ def test_decode_and_append_validation(fa):
     assert L.fa_kv_append(16, 16, 16, 16, 16, 1, 8, 2, 96, 16, 1, 0, 0, None) == fa.ERR_UNSUPPORTED
     assert L.fa_kv_append(None, 16, 16, 16, 16, 1, 8, 2, 64, 16, 1, 0, 0, None) == fa.ERR_INVALID
     assert L.fa_kv_append(16, 16, 16, 16, 16, 0, 8, 2, 64, 16, 1, 0, 0, None) == fa.OK
+
+
+def test_prefill_lse_and_merge_reject_bad_arguments(fa):
+    L = fa.lib()
+    # fa_prefill_lse: a misaligned lse pointer, and fa_prefill's own checks
+    base = (16, 16, 16, 16)
+    rest = (16, 8, 2, 64, 0, 0, 0, 16, 0, 0, 16, 1 << 30, None, None)
+    assert L.fa_prefill_lse(*base, 18, *rest) == fa.ERR_INVALID
+    bad_heads = (16, 8, 3, 64) + rest[4:]
+    assert L.fa_prefill_lse(*base, None, *bad_heads) == fa.ERR_INVALID
+    # n = 0 is a no-op
+    assert L.fa_prefill_lse(*base, 16, 0, *rest[1:]) == fa.OK
+    # fa_merge_attn_states: sizes, NULL inputs and alignment, before any launch
+    def merge(out=16, out_lse=16, pre=16, pl=16, suf=16, sl=16, T=4, H=2, D=64, wc=-1):
+        return L.fa_merge_attn_states(out, out_lse, pre, pl, suf, sl, T, H, D, wc, None)
+    assert merge(D=6) == fa.ERR_INVALID
+    assert merge(D=0) == fa.ERR_INVALID
+    assert merge(H=0) == fa.ERR_INVALID
+    assert merge(T=-1) == fa.ERR_INVALID
+    assert merge(T=0) == fa.OK
+    assert merge(pre=None) == fa.ERR_INVALID
+    assert merge(sl=None) == fa.ERR_INVALID
+    assert merge(out=8) == fa.ERR_INVALID
+    assert merge(pl=18) == fa.ERR_INVALID
+    assert merge(out_lse=2) == fa.ERR_INVALID
