@@ -203,16 +203,19 @@ int oracle_visible(int p, int j, int sink, int win) {
     return (j < sink) || (j >= p - win + 1);
 }
 
-/* Tile map by brute force: map[qt][kt] = 1 iff some query p in
- * [qt*bq, min(n, qt*bq+bq)) sees some key j in [kt*bk, min(n, kt*bk+bk)). */
-void oracle_tile_map(int n, int bq, int bk, int sink, int win, uint8_t *map) {
-    const int nqt = (n + bq - 1) / bq, nkt = (n + bk - 1) / bk;
+/* Tile map by brute force for n queries at positions pos0 .. pos0+n-1 over
+ * keys 0 .. pos0+n-1: map[qt][kt] = 1 iff some query row t in
+ * [qt*bq, min(n, qt*bq+bq)), at position pos0 + t, sees some key j in
+ * [kt*bk, min(L, kt*bk+bk)), L = pos0 + n. */
+void oracle_tile_map(int pos0, int n, int bq, int bk, int sink, int win, uint8_t *map) {
+    const int L = pos0 + n;
+    const int nqt = (n + bq - 1) / bq, nkt = (L + bk - 1) / bk;
     for (int qt = 0; qt < nqt; qt++)
         for (int kt = 0; kt < nkt; kt++) {
             int any = 0;
-            for (int p = qt * bq; p < n && p < qt * bq + bq && !any; p++)
-                for (int j = kt * bk; j < n && j < kt * bk + bk; j++)
-                    if (oracle_visible(p, j, sink, win)) {
+            for (int t = qt * bq; t < n && t < qt * bq + bq && !any; t++)
+                for (int j = kt * bk; j < L && j < kt * bk + bk; j++)
+                    if (oracle_visible(pos0 + t, j, sink, win)) {
                         any = 1;
                         break;
                     }

@@ -54,7 +54,7 @@ def lib():
         L.oracle_q4_decode_rows.argtypes = [P, i64, i32, P]
         L.oracle_visible.restype = i32
         L.oracle_visible.argtypes = [i32, i32, i32, i32]
-        L.oracle_tile_map.argtypes = [i32, i32, i32, i32, i32, P]
+        L.oracle_tile_map.argtypes = [i32, i32, i32, i32, i32, i32, P]
         L.oracle_reads_fp16.restype = i32
         L.oracle_reads_fp16.argtypes = [i32, i32, i32, i32, i32]
         L.oracle_attention.restype = i32
@@ -131,10 +131,12 @@ def visible(p: int, j: int, sink: int, win: int) -> bool:
     return bool(lib().oracle_visible(p, j, sink, win))
 
 
-def tile_map(n: int, bq: int, bk: int, sink: int, win: int) -> np.ndarray:
-    nqt, nkt = -(-n // bq), -(-n // bk)
+def tile_map(n: int, bq: int, bk: int, sink: int, win: int, pos0: int = 0) -> np.ndarray:
+    """[ceil(n/bq)][ceil((pos0+n)/bk)] visited (query tile, key tile) pairs of n
+    queries at positions pos0.. over keys 0..pos0+n-1."""
+    nqt, nkt = -(-n // bq), -(-(pos0 + n) // bk)
     out = np.zeros((nqt, nkt), np.uint8)
-    lib().oracle_tile_map(n, bq, bk, sink, win, _ptr(out))
+    lib().oracle_tile_map(pos0, n, bq, bk, sink, win, _ptr(out))
     return out
 
 
@@ -198,18 +200,21 @@ def attention(q, qpos, kv_k: KVValues, kv_v: KVValues, *, sink: int, win: int,
 
 
 def prefill(q, k, v, *, kv_fmt: str, sink: int, win: int, shadow_sink: int = 0,
-            shadow_win: int = 0, rows=None, with_lse: bool = False):
-    """Prefill with pos0 = 0: query t at position t over the n appended rows.
+            shadow_win: int = 0, rows=None, with_lse: bool = False, pos0: int = 0):
+    """Prefill of n queries at positions pos0 .. pos0+n-1 (query t at pos0 + t)
+    over the cache rows 0 .. pos0+n-1: q [n][Hq][hd], k, v [pos0+n][Hkv][hd].
 
-    rows selects query rows (default all); returns [len(rows)][Hq][hd], and
+    rows selects query rows t (default all); returns [len(rows)][Hq][hd], and
     with with_lse also the rows' lse [len(rows)][Hq]."""
     n = q.shape[0]
+    L = pos0 + n
+    assert k.shape[0] >= L and v.shape[0] >= L
     if rows is None:
         rows = np.arange(n, dtype=np.int32)
     rows = np.asarray(rows, dtype=np.int32)
-    kk, vv = KVValues(k, kv_fmt), KVValues(v, kv_fmt)
-    return attention(q[rows], rows, kk, vv, sink=sink, win=win, shadow_sink=shadow_sink,
-                     shadow_win=shadow_win, L=n, with_lse=with_lse)
+    kk, vv = KVValues(k[:L], kv_fmt), KVValues(v[:L], kv_fmt)
+    return attention(q[rows], rows + pos0, kk, vv, sink=sink, win=win, shadow_sink=shadow_sink,
+                     shadow_win=shadow_win, L=L, with_lse=with_lse)
 
 
 def merge_attn_states(prefix, prefix_lse, suffix, suffix_lse, with_context: int = -1):

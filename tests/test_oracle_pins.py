@@ -480,3 +480,45 @@ def test_merge_edge_cases_stated_by_the_pages(oracle_mod):
     np.testing.assert_array_equal(out2[2:], so[2:])
     np.testing.assert_array_equal(lse2[:, 2:], sl[:, 2:])
     np.testing.assert_array_equal(out2[:2], out[:2])
+
+
+# ------------------------------------------- chunked prefill (pos0 > 0)
+
+def test_tile_map_closed_form_with_offset_queries(oracle_mod):
+    """A chunk of n queries at positions pos0.. over keys 0..pos0+n-1: the
+    brute-force map equals the closed form on absolute positions
+    p0 = pos0 + qt*bq, p1 = pos0 + min(n, qt*bq+bq) - 1, with key tiles up to
+    pos0 + n; pos0 = 0 is the map of a plain prefill."""
+    for pos0 in (0, 1, 5, 16, 40):
+        for n in (1, 7, 33):
+            for bq, bk in ((4, 4), (16, 8), (8, 16)):
+                for sink, win in ((0, 0), (4, 1), (4, 16), (0, 70), (9, 3)):
+                    m = oracle_mod.tile_map(n, bq, bk, sink, win, pos0=pos0)
+                    assert m.shape == (-(-n // bq), -(-(pos0 + n) // bk))
+                    for qt in range(m.shape[0]):
+                        p0 = pos0 + qt * bq
+                        p1 = pos0 + min(n, qt * bq + bq) - 1
+                        for kt in range(m.shape[1]):
+                            j0 = kt * bk
+                            want = j0 <= p1 and (win <= 0 or j0 < min(sink, p1 + 1)
+                                                 or j0 + bk - 1 >= max(0, p0 - win + 1))
+                            assert bool(m[qt, kt]) == want, (pos0, n, bq, bk, sink, win, qt, kt)
+
+
+@pytest.mark.parametrize("fmt,shadow", [("f32", (0, 0)), ("q4_0", (4, 0)), ("q4_0", (4, 256))])
+def test_chunk_equals_rows_of_the_whole_prefill(oracle_mod, fmt, shadow):
+    """Queries pos0.. of a chunk over the cache rows 0..pos0+n-1 are the rows
+    pos0.. of the prefill of all pos0+n tokens, lse included: a row's attention
+    depends on its position and the cache only."""
+    from workloads import prefill_inputs
+    L = 300
+    q, k, v = prefill_inputs(L, 4, 2, 64, seed=61)
+    whole, whole_lse = oracle_mod.prefill(q, k, v, kv_fmt=fmt, sink=3, win=50,
+                                          shadow_sink=shadow[0], shadow_win=shadow[1],
+                                          with_lse=True)
+    for pos0 in (1, 37, 128, 299):
+        part, part_lse = oracle_mod.prefill(q[pos0:], k, v, kv_fmt=fmt, sink=3, win=50,
+                                            shadow_sink=shadow[0], shadow_win=shadow[1],
+                                            with_lse=True, pos0=pos0)
+        np.testing.assert_array_equal(part, whole[pos0:])
+        np.testing.assert_array_equal(part_lse, whole_lse[pos0:])
