@@ -38,6 +38,9 @@ SIGNATURES = {
     "fa_prefill_lse": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _SZ,
                             _P, _P]),
     "fa_merge_attn_states": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "fa_prefill_chunk_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "fa_prefill_chunk": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P,
+                              _SZ, _P, _P]),
     "fa_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "fa_decode": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _SZ,
                        _P]),
@@ -169,6 +172,25 @@ def prefill(q, k, v, out, n: int, n_q_heads: int, n_kv_heads: int, head_dim: int
     else:
         _check(lib().fa_prefill_lse(*args, _dev(lse, torch.float32, "lse"), *rest),
                "fa_prefill_lse")
+
+
+def prefill_chunk_workspace_bytes(pos0: int, n: int, n_q_heads: int, n_kv_heads: int,
+                                  head_dim: int) -> int:
+    return int(lib().fa_prefill_chunk_workspace_bytes(pos0, n, n_q_heads, n_kv_heads, head_dim))
+
+
+def prefill_chunk(q, k, v, out, pos0: int, n: int, n_q_heads: int, n_kv_heads: int,
+                  head_dim: int, sink: int, win: int, kv_fmt: int, *, max_seq: int,
+                  shadow_sink: int = 0, shadow_win: int = 0, workspace: torch.Tensor,
+                  tile_map: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                  stream=None):
+    """fa_prefill_chunk: n queries at positions pos0.. over cache rows 0..pos0+n-1."""
+    _check(lib().fa_prefill_chunk(
+        _dev(q, torch.float32, "q"), _dev(k, torch.uint8, "k"), _dev(v, torch.uint8, "v"),
+        _dev(out, torch.float32, "out"), _dev(lse, torch.float32, "lse"), pos0, n, n_q_heads,
+        n_kv_heads, head_dim, sink, win, kv_fmt, max_seq, shadow_sink, shadow_win,
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _dev(tile_map, torch.uint8, "tile_map"), _stream(stream)), "fa_prefill_chunk")
 
 
 def merge_attn_states(out, out_lse, prefix, prefix_lse, suffix, suffix_lse, *,

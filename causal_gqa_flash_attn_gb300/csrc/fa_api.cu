@@ -85,12 +85,13 @@ fa_status check_shadow(int kv_fmt, int shadow_sink, int shadow_win) {
 struct PrefillWs {
     size_t ctr_off, q_off, k_off, v_off, bytes;
 };
-PrefillWs prefill_ws(int n, int hq, int hkv, int hd) {
+// n query rows over nk key rows
+PrefillWs prefill_ws(int n, int nk, int hq, int hkv, int hd) {
     PrefillWs w;
     w.ctr_off = 0;
     w.q_off = 256;
     w.k_off = w.q_off + up256(static_cast<size_t>(n) * hq * hd * 2);
-    const size_t kv = up256(static_cast<size_t>(hkv) * n * hd * 2);
+    const size_t kv = up256(static_cast<size_t>(hkv) * nk * hd * 2);
     w.v_off = w.k_off + kv;
     w.bytes = w.v_off + kv;
     return w;
@@ -198,8 +199,13 @@ fa_status fa_kv_append(const float *k_new, const float *v_new, void *k_planes, v
 }
 
 size_t fa_prefill_workspace_bytes(int n, int n_q_heads, int n_kv_heads, int head_dim) {
-    if (n < 0 || n_q_heads < 1 || n_kv_heads < 1 || head_dim < 1) return 0;
-    return prefill_ws(n, n_q_heads, n_kv_heads, head_dim).bytes;
+    return fa_prefill_chunk_workspace_bytes(0, n, n_q_heads, n_kv_heads, head_dim);
+}
+
+size_t fa_prefill_chunk_workspace_bytes(int pos0, int n, int n_q_heads, int n_kv_heads,
+                                        int head_dim) {
+    if (pos0 < 0 || n < 0 || n_q_heads < 1 || n_kv_heads < 1 || head_dim < 1) return 0;
+    return prefill_ws(n, pos0 + n, n_q_heads, n_kv_heads, head_dim).bytes;
 }
 
 fa_status fa_prefill_tile_shape(int head_dim, int *bq, int *bk) {
@@ -223,9 +229,20 @@ fa_status fa_prefill_lse(const float *q, const void *k, const void *v, float *ou
                          int kv_fmt, int max_seq, int shadow_sink, int shadow_win,
                          void *workspace, size_t workspace_bytes, uint8_t *tile_map,
                          fa_stream_t stream) {
+    return fa_prefill_chunk(q, k, v, out, lse, 0, n, n_q_heads, n_kv_heads, head_dim, sink, win,
+                            kv_fmt, max_seq, shadow_sink, shadow_win, workspace,
+                            workspace_bytes, tile_map, stream);
+}
+
+fa_status fa_prefill_chunk(const float *q, const void *k, const void *v, float *out, float *lse,
+                           int pos0, int n, int n_q_heads, int n_kv_heads, int head_dim,
+                           int sink, int win, int kv_fmt, int max_seq, int shadow_sink,
+                           int shadow_win, void *workspace, size_t workspace_bytes,
+                           uint8_t *tile_map, fa_stream_t stream) {
     fa_status st = check_heads(n_q_heads, n_kv_heads, head_dim);
     if (st != FA_OK) return st;
-    if (n < 0 || sink < 0 || max_seq < 1 || n > max_seq) return FA_ERR_INVALID;
+    if (pos0 < 0 || n < 0 || sink < 0 || max_seq < 1 || n > max_seq || pos0 > max_seq - n)
+        return FA_ERR_INVALID;
     st = check_shadow(kv_fmt, shadow_sink, shadow_win);
     if (st != FA_OK) return st;
     if (kv_fmt == FA_KV_Q4_0 && shadow_win != 0 && shadow_win != FA_Q4_RING_ROWS)
@@ -235,7 +252,8 @@ fa_status fa_prefill_lse(const float *q, const void *k, const void *v, float *ou
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
         !aligned16(workspace) || (reinterpret_cast<uintptr_t>(lse) & 3u))
         return FA_ERR_INVALID;
-    const PrefillWs w = prefill_ws(n, n_q_heads, n_kv_heads, head_dim);
+    const int nk = pos0 + n;  // key rows 0 .. pos0+n-1
+    const PrefillWs w = prefill_ws(n, nk, n_q_heads, n_kv_heads, head_dim);
     if (workspace_bytes < w.bytes) return FA_ERR_WORKSPACE;
     fa::PlaneGeom g;
     if (!fa::plane_geom(kv_fmt, n_kv_heads, max_seq, head_dim, &g)) return FA_ERR_INVALID;
@@ -250,10 +268,10 @@ fa_status fa_prefill_lse(const float *q, const void *k, const void *v, float *ou
     cudaError_t e =
         fa::launch_stage_q(q, qh, static_cast<size_t>(n) * n_q_heads * head_dim, ctr, s);
     if (e == cudaSuccess)
-        e = fa::launch_stage_kv(static_cast<const uint8_t *>(k), kh, n, g, shadow_sink,
+        e = fa::launch_stage_kv(static_cast<const uint8_t *>(k), kh, nk, g, shadow_sink,
                                 shadow_win, s);
     if (e == cudaSuccess)
-        e = fa::launch_stage_kv(static_cast<const uint8_t *>(v), vh, n, g, shadow_sink,
+        e = fa::launch_stage_kv(static_cast<const uint8_t *>(v), vh, nk, g, shadow_sink,
                                 shadow_win, s);
     if (e != cudaSuccess) return FA_ERR_CUDA;
     fa::PrefillArgs a;
@@ -264,6 +282,7 @@ fa_status fa_prefill_lse(const float *q, const void *k, const void *v, float *ou
     a.tile_map = tile_map;
     a.work_counter = ctr;
     a.lse = lse;
+    a.pos0 = pos0;
     a.n = n;
     a.n_q_heads = n_q_heads;
     a.n_kv_heads = n_kv_heads;

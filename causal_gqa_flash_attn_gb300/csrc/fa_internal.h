@@ -50,12 +50,13 @@ cudaError_t launch_stage_kv(const uint8_t *plane, __half *dst, int n, const Plan
 // ---- prefill_tc.cu
 struct PrefillArgs {
     const __half *qh;   // [n][Hq][hd] fp16
-    const __half *kh;   // [Hkv][n][hd] fp16
-    const __half *vh;   // [Hkv][n][hd] fp16
+    const __half *kh;   // [Hkv][pos0 + n][hd] fp16
+    const __half *vh;   // [Hkv][pos0 + n][hd] fp16
     float *out;         // [n][Hq][hd] fp32
     uint8_t *tile_map;  // optional
     unsigned *work_counter;  // prefill work queue, zeroed by launch_stage_q
     float *lse;              // optional [Hq][n] fp32: log sum_j exp(s_j) per row
+    int pos0;  // position of query row 0; keys are the cache rows 0 .. pos0+n-1
     int n, n_q_heads, n_kv_heads, head_dim, sink, win;
     float scale;
 };

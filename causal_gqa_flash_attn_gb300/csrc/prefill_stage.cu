@@ -3,8 +3,9 @@
 // The prefill kernel runs its two contractions on tcgen05 tensor cores with
 // fp16 operands, fed by TMA. These single-pass kernels produce those operands:
 //   * Q: fp32 [n][Hq][hd] -> fp16 [n][Hq][hd], round to nearest even;
-//   * K and V: the cache rows 0..n-1 of every kv head -> fp16 [Hkv][n][hd],
-//     the value each key has for every query of the prefill. For an fp32 cache
+//   * K and V: the cache rows 0..n-1 of every kv head (n = the key rows: pos0
+//     plus the chunk's queries) -> fp16 [Hkv][n][hd], the value each key has
+//     for every query of the prefill. For an fp32 cache
 //     that is the fp32 value rounded to fp16. For a Q4_0 cache it is the fp16
 //     sink copy for s < shadow_sink, the fp16 ring copy for the 256 newest
 //     rows when the shadow window is 256 wide ("attention.cu",

@@ -137,8 +137,8 @@ __global__ void __launch_bounds__(256, 1)
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_o, uint8_t *__restrict__ tile_map,
-                      unsigned *__restrict__ work_counter, float *__restrict__ lse, int n,
-                      int Hq, int Hkv, int sink, int win, float sl2, unsigned *err) {
+                      unsigned *__restrict__ work_counter, float *__restrict__ lse, int pos0,
+                      int n, int Hq, int Hkv, int sink, int win, float sl2, unsigned *err) {
     using C = Cfg<HD>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(256, 1)
     const int lane = threadIdx.x & 31;
 
     const int nqt = (n + C::BQ - 1) / C::BQ;
-    const int nkt = (n + C::BK - 1) / C::BK;
+    const int nkt = (pos0 + n + C::BK - 1) / C::BK;  // keys 0 .. pos0+n-1
     const int n_units = nqt * Hq;
     const int G = gridDim.x;
     volatile int *abort_flag = nullptr;  // set below
@@ -225,7 +225,9 @@ __global__ void __launch_bounds__(256, 1)
                 bars->unit_id[slot] = w;
                 mbar_arrive(&bars->unit_full[slot]);
                 if (!to_unit(w, &u)) break;
-                const int p0 = u.qt * C::BQ, p1 = min(n, p0 + C::BQ) - 1;
+                // query rows q0.. of the chunk, at positions p0 .. p1
+                const int q0 = u.qt * C::BQ;
+                const int p0 = pos0 + q0, p1 = pos0 + min(n, q0 + C::BQ) - 1;
                 const int g = u.h / (Hq / Hkv);
                 const TilePlan plan = tile_plan(p0, p1, sink, win, C::BK);
                 // the Q buffer is free once the previous unit's last QK^T completed
@@ -243,7 +245,7 @@ __global__ void __launch_bounds__(256, 1)
                     mbar_arrive_expect_tx(&bars->q_full, C::TILE_BYTES);
                     for (int c = 0; c < C::NCHUNK; ++c)
                         tma_load_3d(smem + C::OFF_Q + c * C::CHUNK_BYTES, &tm_q, &bars->q_full,
-                                    c * 64, u.h, p0);
+                                    c * 64, u.h, q0);
                     ++q_arms;
                 }
                 auto load = [&](int i, bool is_k) -> bool {
@@ -329,7 +331,8 @@ __global__ void __launch_bounds__(256, 1)
             bool ok = true;
             Unit u;
             for (int j = 0; ok && next_unit(j, &u, true); ++j) {
-                const int p0 = u.qt * C::BQ, p1 = min(n, p0 + C::BQ) - 1;
+                const int q0 = u.qt * C::BQ;
+                const int p0 = pos0 + q0, p1 = pos0 + min(n, q0 + C::BQ) - 1;
                 const int count = tile_plan(p0, p1, sink, win, C::BK).count;
                 ok = mbar_wait(&bars->q_full, j & 1, abort, err);
                 if (!ok) break;
@@ -371,7 +374,8 @@ __global__ void __launch_bounds__(256, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->unit_empty[j % kUnitRing]);
             if (!__all_sync(0xffffffffu, have)) break;
-            const int p0 = u.qt * C::BQ, p1 = min(n, p0 + C::BQ) - 1;
+            const int q0 = u.qt * C::BQ;  // query rows q0.. at positions p0..
+            const int p0 = pos0 + q0, p1 = pos0 + min(n, q0 + C::BQ) - 1;
             const int p = p0 + r;
             const TilePlan plan = tile_plan(p0, p1, sink, win, C::BK);
             float m_used = -INFINITY;  // exp2-domain reference shared by O and l
@@ -470,8 +474,9 @@ __global__ void __launch_bounds__(256, 1)
             tc_fence_after();
             const float inv = 1.0f / l;
             // log sum_j exp(s_j) = ln 2 * m_used + ln l (l is relative to 2^m_used)
-            if (LSE && p < n)
-                lse[static_cast<size_t>(u.h) * n + p] = m_used * 0.69314718055994531f + logf(l);
+            if (LSE && q0 + r < n)
+                lse[static_cast<size_t>(u.h) * n + q0 + r] =
+                    m_used * 0.69314718055994531f + logf(l);
             const int wr = warp & 3;  // rows 32 wr .. 32 wr + 31 of the tile
 #pragma unroll 1
             for (int c = 0; c < HD / 32; ++c) {
@@ -499,8 +504,8 @@ __global__ void __launch_bounds__(256, 1)
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0 && p0 + 32 * wr < n) {  // rows past n are not stored
-                    tma_store_3d(&tm_o, box, 32 * c, u.h, p0 + 32 * wr);
+                if (lane == 0 && q0 + 32 * wr < n) {  // rows past n are not stored
+                    tma_store_3d(&tm_o, box, 32 * c, u.h, q0 + 32 * wr);
                     bulk_commit_group();
                     ++stores;
                 }
@@ -558,9 +563,10 @@ cudaError_t launch_hd(const PrefillArgs &a, unsigned *err, cudaStream_t stream) 
     using C = Cfg<HD>;
     CUtensorMap tq, tk, tv, to;
     const uint64_t n = a.n, Hq = a.n_q_heads, Hkv = a.n_kv_heads;
+    const uint64_t L = static_cast<uint64_t>(a.pos0) + a.n;  // key rows
     if (!encode_3d(&tq, a.qh, HD, Hq, n, HD * 2, Hq * HD * 2, 64, 1, C::BQ) ||
-        !encode_3d(&tk, a.kh, HD, n, Hkv, HD * 2, n * HD * 2, 64, C::BK, 1) ||
-        !encode_3d(&tv, a.vh, HD, n, Hkv, HD * 2, n * HD * 2, 64, C::BK, 1) ||
+        !encode_3d(&tk, a.kh, HD, L, Hkv, HD * 2, L * HD * 2, 64, C::BK, 1) ||
+        !encode_3d(&tv, a.vh, HD, L, Hkv, HD * 2, L * HD * 2, 64, C::BK, 1) ||
         !encode_3d(&to, a.out, HD, Hq, n, HD * 4, Hq * HD * 4, 32, 1, 32,
                    CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
         return cudaErrorInvalidValue;
@@ -573,8 +579,8 @@ cudaError_t launch_hd(const PrefillArgs &a, unsigned *err, cudaStream_t stream) 
     const int grid = units < device_sm_count() ? units : device_sm_count();
     const float sl2 = a.scale * 1.4426950408889634f;
     kernel<<<grid, 256, C::SMEM, stream>>>(
-        tq, tk, tv, to, a.tile_map, a.work_counter, a.lse, a.n, a.n_q_heads, a.n_kv_heads, a.sink,
-        a.win, sl2, err);
+        tq, tk, tv, to, a.tile_map, a.work_counter, a.lse, a.pos0, a.n, a.n_q_heads,
+        a.n_kv_heads, a.sink, a.win, sl2, err);
     return cudaGetLastError();
 }
 

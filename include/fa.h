@@ -176,6 +176,28 @@ fa_status fa_prefill_lse(const float *q, const void *k, const void *v, float *ou
                          void *workspace, size_t workspace_bytes, uint8_t *tile_map,
                          fa_stream_t stream);
 
+/* Prefill of a chunk: n queries at positions pos0 .. pos0+n-1 over the cache
+ * rows 0 .. pos0+n-1 (the rows of the chunk already appended at pos0..), the
+ * continuation of a prefill in pieces ("attention.cu", the pos0 of
+ * fc_attn_flash_prefill; no ring wrap: pos0 + n <= max_seq).
+ *   q, out     [n][n_q_heads][head_dim] fp32 (device): query row t is at
+ *              position pos0 + t.
+ *   lse        [n_q_heads][n] fp32 or NULL, as for fa_prefill_lse.
+ *   workspace  >= fa_prefill_chunk_workspace_bytes(pos0, n, ...) bytes.
+ *   tile_map   NULL, or [ceil(n/bq)][ceil((pos0+n)/bk)] bytes, as for
+ *              fa_prefill with query tiles over the chunk's rows.
+ * A Q4_0 key s is read from the fp16 ring when s >= pos0 + n - 256 (shadow
+ * window 256; prefill supports {0, 256}). pos0 = 0 is fa_prefill_lse.
+ * FA_ERR_INVALID if pos0 < 0 or pos0 + n > max_seq; otherwise fa_prefill's
+ * checks and statuses. */
+size_t fa_prefill_chunk_workspace_bytes(int pos0, int n, int n_q_heads, int n_kv_heads,
+                                        int head_dim);
+fa_status fa_prefill_chunk(const float *q, const void *k, const void *v, float *out, float *lse,
+                           int pos0, int n, int n_q_heads, int n_kv_heads, int head_dim,
+                           int sink, int win, int kv_fmt, int max_seq, int shadow_sink,
+                           int shadow_win, void *workspace, size_t workspace_bytes,
+                           uint8_t *tile_map, fa_stream_t stream);
+
 /* ------------------------------------------------------- attention-state merge
  *
  * Merge of two attention results over disjoint key sets by their log-sum-exps
