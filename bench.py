@@ -478,6 +478,41 @@ def main():
                                     "kernel_ms": statistics.mean(km)}}
         del S
         torch.cuda.empty_cache()
+    # chunked prefill: the second half of the 8192-token sequence (queries at
+    # positions 4096..8191) over the cache rows 0..8191; a step appends the
+    # chunk's rows and runs fa_prefill_chunk
+    w = BY_NAME["prefill_f32_n8192_h16x2_d256"]
+    pos0 = w.n // 2
+    nq = w.n - pos0
+    S = B.prefill_setup(w)
+    B.prefill_step(S)  # the context rows 0..pos0-1 (and the chunk's, rewritten each step)
+    qc = S["q"][pos0:].contiguous()
+    kc, vc = S["k"][:, pos0:].contiguous(), S["v"][:, pos0:].contiguous()
+    p0c = torch.full((1,), pos0, dtype=torch.int32, device=dev)
+    outc = torch.empty((nq, w.n_q_heads, w.head_dim), dtype=torch.float32, device=dev)
+    wsc = torch.empty(B.fa.prefill_chunk_workspace_bytes(pos0, nq, w.n_q_heads, w.n_kv_heads,
+                                                         w.head_dim),
+                      dtype=torch.uint8, device=dev)
+
+    def chunk_step():
+        B.fa.kv_append(kc, vc, S["kp"], S["vp"], p0c, n_kv_heads=w.n_kv_heads,
+                       head_dim=w.head_dim, max_seq=w.n, kv_fmt=S["code"])
+        B.fa.prefill_chunk(qc, S["kp"], S["vp"], outc, pos0, nq, w.n_q_heads, w.n_kv_heads,
+                           w.head_dim, w.sink, w.win, S["code"], max_seq=w.n, workspace=wsc)
+    f = 4.0 * w.head_dim * w.n_q_heads * (visible_pairs(w.n, w.sink, w.win)
+                                          - visible_pairs(pos0, w.sink, w.win))
+    sm, km = B.timed_steps(chunk_step, args.warmup, args.steps)
+    a = f / (statistics.mean(km) * 1e-3) / 1e12
+    extra["prefill_chunk_f32_pos4096_n4096_h16x2_d256"] = {
+        "value": f / (statistics.mean(sm) * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "ms_per_step": statistics.mean(sm), "flop_per_step": f,
+        "step": "kv_append of the chunk + fa_prefill_chunk",
+        "roofline": {"kernel": "prefill_tc_kernel<256>", "bound": "tensor", "achieved": a,
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": a / peaks["bf16_tflops"], "kernel_ms": statistics.mean(km)}}
+    del S, qc, kc, vc, outc, wsc
+    torch.cuda.empty_cache()
+
     if not args.no_decode:
         w = BY_NAME["decode_q4_32slots_L32768_h16x2_d256_sink4"]
         S = B.decode_setup(w)
