@@ -106,6 +106,85 @@ void oracle_f16_to_f64_array(const uint16_t *h, int64_t count, double *out) {
         out[i] = oracle_f16_to_f64(h[i]);
 }
 
+/* ---------------------------------------------------------- fp8 e4m3fn */
+
+/* fp8 e4m3fn ("vt/ops.h" fp8 KV cache: 1-byte fp8-e4m3fn pages): 1 sign bit,
+ * 4 exponent bits with bias 7, 3 mantissa bits; exponent field 0 holds the
+ * subnormals m * 2^-9; there is no infinity, S.1111.111 is NaN, so the
+ * largest finite magnitude is 1.75 * 2^8 = 448. */
+double oracle_e4m3_to_f64(uint8_t c) {
+    const int sign = (c >> 7) & 1;
+    const int e = (c >> 3) & 0xf;
+    const int m = c & 7;
+    double v;
+    if (e == 0xf && m == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)m, -9);
+    else
+        v = ldexp((double)(8 + m), e - 10);
+    return sign ? -v : v;
+}
+
+/* float -> e4m3fn, round to nearest, ties to even, magnitudes past 448
+ * (and infinities) saturate to +-448 ("vt/ops.h": fp8_e4m3(clamp(x, -448,
+ * 448)), the hardware conversion with saturation to finite); NaN gives 0x7f. */
+uint8_t oracle_e4m3_rne_sat(float f) {
+    if (isnan(f))
+        return 0x7f;
+    const uint8_t sign = signbit(f) ? 0x80 : 0x00;
+    double a = fabs((double)f);
+    if (a == 0.0)
+        return sign;
+    if (isinf(a))
+        return (uint8_t)(sign | 0x7e);
+    int e2;
+    (void)frexp(a, &e2); /* a = fr * 2^e2, fr in [0.5, 1): floor(log2 a) = e2 - 1 */
+    int e = e2 - 1;
+    if (e < -6) {
+        /* subnormal grid: multiples of 2^-9; q = 8 is the smallest normal */
+        const double t = ldexp(a, 9);
+        double q = floor(t);
+        const double r = t - q;
+        if (r > 0.5 || (r == 0.5 && fmod(q, 2.0) == 1.0))
+            q += 1.0;
+        return (uint8_t)(sign | (uint8_t)q);
+    }
+    if (e > 8)
+        return (uint8_t)(sign | 0x7e);
+    /* normal: a = q * 2^(e-3) with q in [8, 16) */
+    const double t = ldexp(a, 3 - e);
+    double q = floor(t);
+    const double r = t - q;
+    if (r > 0.5 || (r == 0.5 && fmod(q, 2.0) == 1.0))
+        q += 1.0;
+    if (q == 16.0) {
+        q = 8.0;
+        e += 1;
+    }
+    if (e > 8 || (e == 8 && q > 14.0))
+        return (uint8_t)(sign | 0x7e); /* past 448: saturate */
+    return (uint8_t)(sign | (uint8_t)(((e + 7) << 3) | ((int)q - 8)));
+}
+
+/* The fp8 KV store of "vt/ops.h" (ReshapeAndCacheFp8): each element as
+ * Quantize(x / scale), the division one float operation. */
+void oracle_e4m3_store_array(const float *x, int64_t count, float scale, uint8_t *out) {
+    for (int64_t i = 0; i < count; i++) {
+        const float t = x[i] / scale;
+        out[i] = oracle_e4m3_rne_sat(t);
+    }
+}
+
+/* The fp8 KV read: Dequant(fp8) * scale, one float multiplication. */
+void oracle_e4m3_load_array(const uint8_t *q, int64_t count, float scale, double *out) {
+    for (int64_t i = 0; i < count; i++) {
+        const float v = (float)oracle_e4m3_to_f64(q[i]);
+        const float w = v * scale;
+        out[i] = (double)w;
+    }
+}
+
 /* ------------------------------------------------------------------ Q4_0 */
 
 /* Round to nearest integer, ties to even, with the saturating conversion of

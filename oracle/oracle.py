@@ -48,6 +48,12 @@ def lib():
         L.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
         L.oracle_f16_rne_array.argtypes = [P, i64, P]
         L.oracle_f16_to_f64_array.argtypes = [P, i64, P]
+        L.oracle_e4m3_rne_sat.restype = ctypes.c_uint8
+        L.oracle_e4m3_rne_sat.argtypes = [ctypes.c_float]
+        L.oracle_e4m3_to_f64.restype = f64
+        L.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_store_array.argtypes = [P, i64, ctypes.c_float, P]
+        L.oracle_e4m3_load_array.argtypes = [P, i64, ctypes.c_float, P]
         L.oracle_q4_encode_block.argtypes = [P, P]
         L.oracle_q4_decode_block.argtypes = [P, P]
         L.oracle_q4_encode_rows.argtypes = [P, i64, i32, P]
@@ -96,6 +102,33 @@ def f16_to_f64(h) -> np.ndarray:
     h = np.ascontiguousarray(h, dtype=np.uint16)
     out = np.empty(h.shape, np.float64)
     lib().oracle_f16_to_f64_array(_ptr(h), h.size, _ptr(out))
+    return out
+
+
+# ---------------------------------------------------------- fp8 e4m3fn
+
+def e4m3(x: float) -> int:
+    """One float -> e4m3fn byte, round to nearest even, saturating at +-448."""
+    return int(lib().oracle_e4m3_rne_sat(float(np.float32(x))))
+
+
+def e4m3_value(code: int) -> float:
+    return float(lib().oracle_e4m3_to_f64(int(code) & 0xff))
+
+
+def e4m3_store(x, scale: float) -> np.ndarray:
+    """The fp8 KV store: bytes of Quantize(x / scale), elementwise."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, np.uint8)
+    lib().oracle_e4m3_store_array(_ptr(x), x.size, float(np.float32(scale)), _ptr(out))
+    return out
+
+
+def e4m3_load(q, scale: float) -> np.ndarray:
+    """The fp8 KV read: Dequant(byte) * scale in float, as float64."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    out = np.empty(q.shape, np.float64)
+    lib().oracle_e4m3_load_array(_ptr(q), q.size, float(np.float32(scale)), _ptr(out))
     return out
 
 
@@ -149,17 +182,24 @@ def reads_fp16(p: int, s: int, L: int, shadow_sink: int, shadow_win: int) -> boo
 class KVValues:
     """The values a reader of one KV cache sees, [L][Hkv][hd] float64.
 
-    ``body`` is the main store (fp32 widened, or Q4_0 decoded); ``f16`` is the
-    fp16 shadow copy of every row (None for an fp32 cache); ``q4`` the Q4_0
-    bytes the oracle quantised ([L][Hkv][row_bytes], None for fp32)."""
+    ``body`` is the main store: fp32 widened, the fp16 rounding ("f16"), the
+    fp8 e4m3fn store and read with the tensor's scale ("fp8_e4m3"), or Q4_0
+    decoded. ``f16`` is the fp16 shadow copy of every row of a Q4_0 cache (None
+    otherwise); ``q4`` / ``fp8`` the bytes the oracle stored."""
 
-    def __init__(self, x_f32: np.ndarray, kv_fmt: str):
+    def __init__(self, x_f32: np.ndarray, kv_fmt: str, scale: float = 1.0):
         x_f32 = np.ascontiguousarray(x_f32, dtype=np.float32)
         self.kv_fmt = kv_fmt
+        self.f16 = None
+        self.q4 = None
+        self.fp8 = None
         if kv_fmt == "f32":
             self.body = x_f32.astype(np.float64)
-            self.f16 = None
-            self.q4 = None
+        elif kv_fmt == "f16":
+            self.body = f16_to_f64(f16_rne(x_f32))
+        elif kv_fmt == "fp8_e4m3":
+            self.fp8 = e4m3_store(x_f32, scale)
+            self.body = e4m3_load(self.fp8, scale)
         elif kv_fmt == "q4_0":
             self.q4 = q4_encode(x_f32)
             self.body = q4_decode(self.q4, x_f32.shape[-1])
@@ -200,7 +240,8 @@ def attention(q, qpos, kv_k: KVValues, kv_v: KVValues, *, sink: int, win: int,
 
 
 def prefill(q, k, v, *, kv_fmt: str, sink: int, win: int, shadow_sink: int = 0,
-            shadow_win: int = 0, rows=None, with_lse: bool = False, pos0: int = 0):
+            shadow_win: int = 0, rows=None, with_lse: bool = False, pos0: int = 0,
+            k_scale: float = 1.0, v_scale: float = 1.0):
     """Prefill of n queries at positions pos0 .. pos0+n-1 (query t at pos0 + t)
     over the cache rows 0 .. pos0+n-1: q [n][Hq][hd], k, v [pos0+n][Hkv][hd].
 
@@ -212,7 +253,7 @@ def prefill(q, k, v, *, kv_fmt: str, sink: int, win: int, shadow_sink: int = 0,
     if rows is None:
         rows = np.arange(n, dtype=np.int32)
     rows = np.asarray(rows, dtype=np.int32)
-    kk, vv = KVValues(k[:L], kv_fmt), KVValues(v[:L], kv_fmt)
+    kk, vv = KVValues(k[:L], kv_fmt, k_scale), KVValues(v[:L], kv_fmt, v_scale)
     return attention(q[rows], rows + pos0, kk, vv, sink=sink, win=win, shadow_sink=shadow_sink,
                      shadow_win=shadow_win, L=L, with_lse=with_lse)
 
@@ -281,10 +322,10 @@ def combine(m, l, acc) -> np.ndarray:
 
 
 def decode(q, pos: int, k, v, *, kv_fmt: str, sink: int, win: int, shadow_sink: int = 0,
-           shadow_win: int = 0) -> np.ndarray:
+           shadow_win: int = 0, k_scale: float = 1.0, v_scale: float = 1.0) -> np.ndarray:
     """One decode query q [Hq][hd] at position pos over rows 0..pos of K, V [L][Hkv][hd]."""
-    kk = KVValues(np.ascontiguousarray(k[: pos + 1]), kv_fmt)
-    vv = KVValues(np.ascontiguousarray(v[: pos + 1]), kv_fmt)
+    kk = KVValues(np.ascontiguousarray(k[: pos + 1]), kv_fmt, k_scale)
+    vv = KVValues(np.ascontiguousarray(v[: pos + 1]), kv_fmt, v_scale)
     out = attention(q[None], np.array([pos], np.int32), kk, vv, sink=sink, win=win,
                     shadow_sink=shadow_sink, shadow_win=shadow_win, L=pos + 1)
     return out[0]

@@ -522,3 +522,80 @@ def test_chunk_equals_rows_of_the_whole_prefill(oracle_mod, fmt, shadow):
                                             with_lse=True, pos0=pos0)
         np.testing.assert_array_equal(part, whole[pos0:])
         np.testing.assert_array_equal(part_lse, whole_lse[pos0:])
+
+
+# ------------------------------------------------ fp16 and fp8 KV formats
+
+def test_e4m3_golden(oracle_mod):
+    for name, xb, cb in golden_lines("e4m3.txt"):
+        x = f32_from_hex(xb)
+        assert oracle_mod.e4m3(x) == int(cb, 16), name
+
+
+def test_e4m3_codes_round_trip(oracle_mod):
+    """Every finite code decodes to a value that encodes back to it, the values
+    are strictly increasing over the positive codes and span [2^-9, 448]."""
+    vals = []
+    for c in range(256):
+        v = oracle_mod.e4m3_value(c)
+        if c in (0x7f, 0xff):
+            assert math.isnan(v)
+            continue
+        assert oracle_mod.e4m3(v) == c, hex(c)
+        if c <= 0x7e:
+            vals.append(v)
+    assert vals == sorted(vals) and len(set(vals)) == len(vals)
+    assert vals[1] == 2.0 ** -9 and vals[-1] == 448.0
+
+
+def test_e4m3_is_nearest_even_with_saturation(oracle_mod):
+    """Against the table of all finite values: the encoding of x is the value
+    nearest to x, ties to the even code, and +-448 beyond."""
+    table = np.array([oracle_mod.e4m3_value(c) for c in range(0x7f)])  # 0 .. 448
+    rng = np.random.default_rng(3)
+    xs = np.concatenate([rng.standard_normal(3000) * 30, rng.standard_normal(500) * 0.01,
+                         (table[:-1] + table[1:]) / 2, table, [500.0, 463.9, 464.0]])
+    for x in xs.astype(np.float32):
+        c = oracle_mod.e4m3(float(x))
+        a = abs(float(x))
+        if a >= 448.0:
+            assert c & 0x7f == 0x7e
+            continue
+        d = np.abs(table - a)
+        best = np.flatnonzero(d == d.min())
+        want = best[0] if len(best) == 1 else [b for b in best if b % 2 == 0][0]
+        assert c & 0x7f == want, (x, hex(c))
+        assert (c >> 7) == (1 if np.signbit(x) else 0)
+
+
+def test_fp8_kv_store_and_read_use_the_scale(oracle_mod):
+    """Store x / scale, read byte * scale: with scale s the reader sees
+    s * e4m3(x / s); a power-of-two scale only moves the grid."""
+    rng = np.random.default_rng(8)
+    x = (rng.standard_normal(2000) * 3).astype(np.float32)
+    for s in (1.0, 0.25, 8.0, 0.0123):
+        q = oracle_mod.e4m3_store(x, s)
+        got = oracle_mod.e4m3_load(q, s)
+        for i in range(0, 2000, 97):
+            t = np.float32(x[i] / np.float32(s))
+            assert q[i] == oracle_mod.e4m3(t)
+            assert got[i] == float(np.float32(np.float32(oracle_mod.e4m3_value(q[i])) * np.float32(s)))
+    q1 = oracle_mod.e4m3_store(x * 4, 4.0)
+    assert np.array_equal(q1, oracle_mod.e4m3_store(x, 1.0))
+
+
+def test_f16_and_fp8_caches_are_attention_over_their_values(oracle_mod):
+    """An f16 (fp8) cache is attention over the fp16 rounding (the fp8 store
+    and read) of the same rows: equal to an fp32 cache holding those values."""
+    from workloads import prefill_inputs
+    q, k, v = prefill_inputs(64, 4, 2, 32, seed=17)
+    k16 = oracle_mod.f16_to_f64(oracle_mod.f16_rne(k)).astype(np.float32)
+    v16 = oracle_mod.f16_to_f64(oracle_mod.f16_rne(v)).astype(np.float32)
+    a = oracle_mod.prefill(q, k, v, kv_fmt="f16", sink=2, win=9)
+    b = oracle_mod.prefill(q, k16, v16, kv_fmt="f32", sink=2, win=9)
+    np.testing.assert_array_equal(a, b)
+    k8 = oracle_mod.e4m3_load(oracle_mod.e4m3_store(k, 0.5), 0.5).astype(np.float32)
+    v8 = oracle_mod.e4m3_load(oracle_mod.e4m3_store(v, 2.0), 2.0).astype(np.float32)
+    a = oracle_mod.prefill(q, k, v, kv_fmt="fp8_e4m3", sink=0, win=0, k_scale=0.5, v_scale=2.0)
+    b = oracle_mod.prefill(q, k8, v8, kv_fmt="f32", sink=0, win=0)
+    np.testing.assert_array_equal(a, b)
