@@ -203,15 +203,17 @@ class GpuBench:
     # ---- prefill workloads
     def prefill_setup(self, w):
         torch, fa = self.torch, self.fa
-        from workloads import prefill_inputs
+        from workloads import FMT_CODES, prefill_inputs
         q, k, v = prefill_inputs(w.n, w.n_q_heads, w.n_kv_heads, w.head_dim, w.seed)
-        code = fa.KV_F32 if w.kv_fmt == "f32" else fa.KV_Q4_0
+        code = FMT_CODES[w.kv_fmt]
         S = dict(w=w, code=code, q_host=q, k_host=k, v_host=v)
         S["q"] = torch.from_numpy(q).to(self.dev)
         S["k"] = torch.from_numpy(k[None]).to(self.dev)
         S["v"] = torch.from_numpy(v[None]).to(self.dev)
-        S["kp"] = fa.alloc_planes(1, code, w.n_kv_heads, w.n, w.head_dim, device=self.dev)
-        S["vp"] = fa.alloc_planes(1, code, w.n_kv_heads, w.n, w.head_dim, device=self.dev)
+        S["kp"] = fa.alloc_planes(1, code, w.n_kv_heads, w.n, w.head_dim, device=self.dev,
+                                  scale=w.k_scale)
+        S["vp"] = fa.alloc_planes(1, code, w.n_kv_heads, w.n, w.head_dim, device=self.dev,
+                                  scale=w.v_scale)
         S["pos0"] = torch.zeros(1, dtype=torch.int32, device=self.dev)
         S["out"] = torch.empty((w.n, w.n_q_heads, w.head_dim), dtype=torch.float32,
                                device=self.dev)
@@ -254,13 +256,16 @@ class GpuBench:
     # ---- decode workload
     def decode_setup(self, w):
         torch, fa = self.torch, self.fa
-        code = fa.KV_Q4_0 if w.kv_fmt == "q4_0" else fa.KV_F32
+        from workloads import FMT_CODES
+        code = FMT_CODES[w.kv_fmt]
         L = w.n
         g = torch.Generator(device=self.dev)
         g.manual_seed(w.seed)
         S = dict(w=w, code=code, L=L)
-        S["kp"] = fa.alloc_planes(w.nslots, code, w.n_kv_heads, L, w.head_dim, device=self.dev)
-        S["vp"] = fa.alloc_planes(w.nslots, code, w.n_kv_heads, L, w.head_dim, device=self.dev)
+        S["kp"] = fa.alloc_planes(w.nslots, code, w.n_kv_heads, L, w.head_dim, device=self.dev,
+                                  scale=w.k_scale)
+        S["vp"] = fa.alloc_planes(w.nslots, code, w.n_kv_heads, L, w.head_dim, device=self.dev,
+                                  scale=w.v_scale)
         # cache rows 0..L-2 appended once (untimed), slot by slot chunks
         chunk = 4
         pos0 = torch.zeros(chunk, dtype=torch.int32, device=self.dev)
@@ -307,9 +312,11 @@ class GpuBench:
 
 def decode_kv_bytes(w):
     """KV bytes a decode step must read: per (slot, kv head) the fp16 sink
-    rows (K and V, 2*hd bytes each) and the Q4_0 (or fp32) rows of the rest."""
+    rows (K and V, 2*hd bytes each) and the Q4_0 (fp32, fp16, fp8) rows of
+    the rest."""
     L = w.n
-    row = w.head_dim // 32 * 18 if w.kv_fmt == "q4_0" else w.head_dim * 4
+    row = {"q4_0": w.head_dim // 32 * 18, "f32": w.head_dim * 4, "f16": w.head_dim * 2,
+           "fp8_e4m3": w.head_dim}[w.kv_fmt]
     fp16_rows = min(w.shadow_sink, L) if w.kv_fmt == "q4_0" else 0
     if w.kv_fmt == "q4_0" and w.shadow_win > 0:
         fp16_rows = min(L, fp16_rows + w.shadow_win)
@@ -464,7 +471,8 @@ def main():
     # ---------------- other workloads
     extra = {}
     for name in ("prefill_f32_n8192_h16x2_d256_sink4_win1024",
-                 "prefill_q4_n8192_h16x2_d256_shadow4_256"):
+                 "prefill_q4_n8192_h16x2_d256_shadow4_256", "prefill_f16_n8192_h16x2_d256",
+                 "prefill_fp8_n8192_h16x2_d256"):
         w = BY_NAME[name]
         S = B.prefill_setup(w)
         f = 4.0 * w.head_dim * w.n_q_heads * visible_pairs(w.n, w.sink, w.win)
@@ -513,8 +521,12 @@ def main():
     del S, qc, kc, vc, outc, wsc
     torch.cuda.empty_cache()
 
-    if not args.no_decode:
-        w = BY_NAME["decode_q4_32slots_L32768_h16x2_d256_sink4"]
+    decode_names = () if args.no_decode else (
+        "decode_q4_32slots_L32768_h16x2_d256_sink4", "decode_f16_32slots_L32768_h16x2_d256_sink4",
+        "decode_fp8_32slots_L32768_h16x2_d256_sink4")
+    for name in decode_names:
+        w = BY_NAME[name]
+        kname = "decode_q4_kernel<256>" if w.kv_fmt == "q4_0" else "decode_kernel<256,1>"
         S = B.decode_setup(w)
         kvb = decode_kv_bytes(w)
         sm, km = B.timed_steps(lambda: B.decode_step(S), args.warmup, args.steps)
@@ -522,11 +534,10 @@ def main():
         extra[w.name] = {"value": kvb / (statistics.mean(sm) * 1e-3) / 1e9, "unit": "GB/s",
                          "ms_per_step": statistics.mean(sm), "kv_bytes_per_step": kvb,
                          "step": "append 1 row/slot + split decode + combine",
-                         "roofline": {"kernel": "decode_q4_kernel<256>", "bound": "hbm",
+                         "roofline": {"kernel": kname, "bound": "hbm",
                                       "achieved": a, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                       "frac": a / peaks["hbm_gbs"], "frac_of_8tbs": a / 8000.0,
-                                      "traffic": profiled_traffic("decode_q4_kernel<256>",
-                                                                  src_hash("decode.cu")),
+                                      "traffic": profiled_traffic(kname, src_hash("decode.cu")),
                                       "kernel_ms": statistics.mean(km)}}
         del S
         torch.cuda.empty_cache()

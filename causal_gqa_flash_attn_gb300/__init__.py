@@ -20,6 +20,8 @@ LIB_PATH = os.path.join(_HERE, "_build", "libfa.so")
 
 KV_F32 = 0
 KV_Q4_0 = 1
+KV_F16 = 2
+KV_FP8_E4M3 = 3
 Q4_SINK_MAX = 8
 Q4_RING_ROWS = 256
 
@@ -30,6 +32,8 @@ _P, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 SIGNATURES = {
     "fa_kv_plane_bytes": (_SZ, [_I, _I, _I, _I]),
     "fa_kv_plane_layout": (_I, [_I, _I, _I, _I, _P, _P, _P, _P]),
+    "fa_kv_scale_offset": (_SZ, [_I, _I, _I, _I]),
+    "fa_kv_set_scale": (_I, [_P, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
     "fa_kv_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "fa_prefill_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "fa_prefill_tile_shape": (_I, [_I, _P, _P]),
@@ -122,13 +126,33 @@ def kv_plane_layout(kv_fmt: int, n_kv_heads: int, max_seq: int, head_dim: int):
     return tuple(int(v.value) for v in vals)
 
 
+def kv_scale_offset(kv_fmt: int, n_kv_heads: int, max_seq: int, head_dim: int) -> int:
+    """Byte offset of an fp8 plane's fp32 scale (0 for the other formats)."""
+    return int(lib().fa_kv_scale_offset(kv_fmt, n_kv_heads, max_seq, head_dim))
+
+
+def kv_set_scale(planes, kv_fmt: int, n_kv_heads: int, max_seq: int, head_dim: int,
+                 scale: float, stream=None):
+    """Set the scale of every fp8 plane in ``planes`` (consecutive planes)."""
+    pb = kv_plane_bytes(kv_fmt, n_kv_heads, max_seq, head_dim)
+    if pb == 0 or planes.numel() % pb:
+        raise ValueError("planes is not a whole number of planes of this geometry")
+    _check(lib().fa_kv_set_scale(_dev(planes, torch.uint8, "planes"), planes.numel() // pb,
+                                 kv_fmt, n_kv_heads, max_seq, head_dim, float(scale),
+                                 _stream(stream)), "fa_kv_set_scale")
+
+
 def alloc_planes(nslots: int, kv_fmt: int, n_kv_heads: int, max_seq: int, head_dim: int,
-                 device="cuda") -> torch.Tensor:
-    """nslots consecutive zeroed planes as one uint8 tensor."""
+                 device="cuda", scale: float = 1.0) -> torch.Tensor:
+    """nslots consecutive zeroed planes as one uint8 tensor; fp8 planes get
+    ``scale`` (the per-tensor k_scale or v_scale, 1.0 uncalibrated)."""
     pb = kv_plane_bytes(kv_fmt, n_kv_heads, max_seq, head_dim)
     if pb == 0:
         raise ValueError("invalid plane geometry")
-    return torch.zeros(nslots * pb, dtype=torch.uint8, device=device)
+    planes = torch.zeros(nslots * pb, dtype=torch.uint8, device=device)
+    if kv_fmt == KV_FP8_E4M3:
+        kv_set_scale(planes, kv_fmt, n_kv_heads, max_seq, head_dim, scale)
+    return planes
 
 
 def kv_append(k_new, v_new, k_planes, v_planes, pos0, *, n_kv_heads: int, head_dim: int,

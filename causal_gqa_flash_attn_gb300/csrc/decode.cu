@@ -55,7 +55,7 @@ struct DecodeParams {
     int entries;       // entries written per (slot, head)
     int stride;        // entry stride of the workspace
     int shadow_entry;  // entry index of the fp16-shadow keys, or -1
-    size_t plane_bytes, body_off, row_bytes, sink_off, ring_off;
+    size_t plane_bytes, body_off, row_bytes, sink_off, ring_off, scale_off;
     float sl2;  // scale * log2(e)
     unsigned *err;
 };
@@ -71,7 +71,7 @@ __device__ __forceinline__ int dec_plan(int seq_len, int kps, int cap, int *spli
 
 // Is key s read from an fp16 shadow copy by the decode query at p?
 __device__ __forceinline__ bool is_shadow_key(const DecodeParams &P, int p, int s) {
-    return P.fmt != 0 && (s < P.shadow_sink || (P.shadow_win > 0 && s > p - P.shadow_win));
+    return P.fmt == kFmtQ4 && (s < P.shadow_sink || (P.shadow_win > 0 && s > p - P.shadow_win));
 }
 
 __device__ __forceinline__ void write_empty(const DecodeParams &P, size_t head0, int G, int e) {
@@ -210,10 +210,12 @@ __device__ __forceinline__ void fold_scores(float (&sv)[2][N], float sl2, float 
 
 // Stage the fp16 values of keys [c0, c0+16) (clamped to kmax) of one K or V
 // plane into a [16][HD+8] fp16 tile; the read rule picks the fp16 sink, the
-// fp16 ring, the Q4_0 body or the fp32 body.
+// fp16 ring, the Q4_0 body, the fp32 body (rounded), the fp16 body, or the
+// fp8 body times the plane's scale c (rounded).
 template <int HD>
 __device__ __forceinline__ void stage_rows(const DecodeParams &P, const uint8_t *plane, int g,
-                                           int p, int c0, int kmax, __half *tile, int lane) {
+                                           int p, int c0, int kmax, __half *tile, int lane,
+                                           float c) {
     constexpr int UPR = HD / 8;  // 16-byte units per row
     constexpr int STRIDE = HD + 8;
 #pragma unroll 4
@@ -222,12 +224,17 @@ __device__ __forceinline__ void stage_rows(const DecodeParams &P, const uint8_t 
         const int e0 = (uu % UPR) * 8;
         const int key = min(c0 + k, kmax);
         uint4 v;
-        if (P.fmt == 0) {
-            const float4 *src = reinterpret_cast<const float4 *>(
-                plane + P.body_off + ((static_cast<size_t>(g) * P.max_seq + key) * HD + e0) * 4);
+        const size_t elem = (static_cast<size_t>(g) * P.max_seq + key) * HD + e0;
+        if (P.fmt == kFmtF32) {
+            const float4 *src = reinterpret_cast<const float4 *>(plane + P.body_off + elem * 4);
             const float4 a = __ldg(src), b = __ldg(src + 1);
             v = make_uint4(pack_half2(a.x, a.y), pack_half2(a.z, a.w), pack_half2(b.x, b.y),
                            pack_half2(b.z, b.w));
+        } else if (P.fmt == kFmtF16) {
+            v = __ldg(reinterpret_cast<const uint4 *>(plane + P.body_off + elem * 2));
+        } else if (P.fmt == kFmtFp8) {
+            v = fp8x8_to_half8_scaled(__ldg(reinterpret_cast<const uint2 *>(plane + P.body_off + elem)),
+                                      c);
         } else if (key < P.shadow_sink) {
             v = __ldg(reinterpret_cast<const uint4 *>(
                 plane + P.sink_off + ((static_cast<size_t>(g) * kSinkMax + key) * HD + e0) * 2));
@@ -275,6 +282,11 @@ __device__ __forceinline__ void generic_body(const DecodeParams &P, uint8_t *dsm
     __half *tv = tk + kChunk * STRIDE;
     const uint8_t *kplane = P.k_planes + static_cast<size_t>(u) * P.plane_bytes;
     const uint8_t *vplane = P.v_planes + static_cast<size_t>(u) * P.plane_bytes;
+    float kscale = 1.0f, vscale = 1.0f;
+    if (P.fmt == kFmtFp8) {
+        kscale = __ldg(reinterpret_cast<const float *>(kplane + P.scale_off));
+        vscale = __ldg(reinterpret_cast<const float *>(vplane + P.scale_off));
+    }
 
     // Q^T fragments (B operand): head nt*8 + r, dims 16kk + 2t + {0,1} and + {8,9}.
     uint32_t qb[NT][MT][2];
@@ -323,8 +335,8 @@ __device__ __forceinline__ void generic_body(const DecodeParams &P, uint8_t *dsm
         const int c0 = first ? lo0 + kChunk * ci : lo1 + kChunk * (ci - n0);
         const int k_hi = first ? hi0 : hi1;
         if (P.win > 0 && !(c0 < P.sink || c0 + kChunk - 1 >= p - P.win + 1)) continue;
-        stage_rows<HD>(P, kplane, g, p, c0, k_hi - 1, tk, lane);
-        stage_rows<HD>(P, vplane, g, p, c0, k_hi - 1, tv, lane);
+        stage_rows<HD>(P, kplane, g, p, c0, k_hi - 1, tk, lane, kscale);
+        stage_rows<HD>(P, vplane, g, p, c0, k_hi - 1, tv, lane, vscale);
         __syncwarp();
 
         float sacc[NT][4];
@@ -1067,7 +1079,7 @@ DecodeShape decode_shape(int nslots, int n_q_heads, int n_kv_heads, int kv_fmt, 
     const int G = n_q_heads / n_kv_heads;
     // The Q4_0 path bulk-copies rows of a kv head; a copy must start 16-byte
     // aligned, so every head's body must start 16-byte aligned.
-    d.fast = kv_fmt == 1 && G <= 8 && (static_cast<size_t>(max_seq) * row_bytes) % 16 == 0;
+    d.fast = kv_fmt == kFmtQ4 && G <= 8 && (static_cast<size_t>(max_seq) * row_bytes) % 16 == 0;
     // Blocks to aim at: the Q4_0 path keeps 2 blocks per SM, so 8 per SM is
     // about four waves and the last one is short; the generic path, 4 per SM.
     const long long pairs = static_cast<long long>(nslots) * n_kv_heads;
@@ -1132,6 +1144,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodeWs &ws, const DecodeS
     P.row_bytes = a.g.row_bytes;
     P.sink_off = a.g.sink_off;
     P.ring_off = a.g.ring_off;
+    P.scale_off = a.g.scale_off;
     P.sl2 = a.scale * 1.4426950408889634f;
     P.err = err;
     if (d.entries > ws.stride) return cudaErrorInvalidValue;

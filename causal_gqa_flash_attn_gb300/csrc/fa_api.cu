@@ -4,6 +4,7 @@
 // runs in the kernels of the other translation units.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <mutex>
 
 #include "../../include/fa.h"
@@ -72,8 +73,14 @@ fa_status check_heads(int n_q_heads, int n_kv_heads, int head_dim) {
     return FA_OK;
 }
 
+bool known_fmt(int kv_fmt) {
+    return kv_fmt == FA_KV_F32 || kv_fmt == FA_KV_Q4_0 || kv_fmt == FA_KV_F16 ||
+           kv_fmt == FA_KV_FP8_E4M3;
+}
+
 fa_status check_shadow(int kv_fmt, int shadow_sink, int shadow_win) {
-    if (kv_fmt == FA_KV_F32) return (shadow_sink == 0 && shadow_win == 0) ? FA_OK : FA_ERR_INVALID;
+    if (kv_fmt == FA_KV_F32 || kv_fmt == FA_KV_F16 || kv_fmt == FA_KV_FP8_E4M3)
+        return (shadow_sink == 0 && shadow_win == 0) ? FA_OK : FA_ERR_INVALID;
     if (kv_fmt != FA_KV_Q4_0) return FA_ERR_INVALID;
     if (shadow_sink < 0 || shadow_sink > FA_Q4_SINK_MAX) return FA_ERR_INVALID;
     if (shadow_win < 0 || shadow_win > FA_Q4_RING_ROWS) return FA_ERR_INVALID;
@@ -103,23 +110,30 @@ namespace fa {
 
 bool plane_geom(int fmt, int n_kv, int max_seq, int hd, PlaneGeom *g) {
     if (n_kv < 1 || max_seq < 1 || hd < 32 || hd % 32) return false;
-    if (fmt != FA_KV_F32 && fmt != FA_KV_Q4_0) return false;
+    if (!known_fmt(fmt)) return false;
     g->fmt = fmt;
     g->n_kv = n_kv;
     g->max_seq = max_seq;
     g->hd = hd;
-    g->row_bytes = fmt == FA_KV_F32 ? static_cast<size_t>(hd) * 4
-                                    : static_cast<size_t>(hd / kQ4Block) * kQ4BlockBytes;
+    switch (fmt) {
+        case FA_KV_F32: g->row_bytes = static_cast<size_t>(hd) * 4; break;
+        case FA_KV_F16: g->row_bytes = static_cast<size_t>(hd) * 2; break;
+        case FA_KV_FP8_E4M3: g->row_bytes = static_cast<size_t>(hd); break;
+        default: g->row_bytes = static_cast<size_t>(hd / kQ4Block) * kQ4BlockBytes; break;
+    }
     g->body_off = 0;
     const size_t body = up256(static_cast<size_t>(n_kv) * max_seq * g->row_bytes);
-    if (fmt == FA_KV_F32) {
-        g->sink_off = 0;
-        g->ring_off = 0;
-        g->bytes = body;
-    } else {
+    g->sink_off = 0;
+    g->ring_off = 0;
+    g->scale_off = 0;
+    g->bytes = body;
+    if (fmt == FA_KV_Q4_0) {
         g->sink_off = body;
         g->ring_off = body + up256(static_cast<size_t>(n_kv) * kSinkMax * hd * 2);
         g->bytes = g->ring_off + up256(static_cast<size_t>(n_kv) * kRingRows * hd * 2);
+    } else if (fmt == FA_KV_FP8_E4M3) {
+        g->scale_off = body;
+        g->bytes = body + 256;
     }
     return true;
 }
@@ -171,6 +185,27 @@ fa_status fa_kv_plane_layout(int kv_fmt, int n_kv_heads, int max_seq, int head_d
     if (sink_offset) *sink_offset = g.sink_off;
     if (ring_offset) *ring_offset = g.ring_off;
     return FA_OK;
+}
+
+size_t fa_kv_scale_offset(int kv_fmt, int n_kv_heads, int max_seq, int head_dim) {
+    fa::PlaneGeom g;
+    if (!supported_hd(head_dim) || !fa::plane_geom(kv_fmt, n_kv_heads, max_seq, head_dim, &g))
+        return 0;
+    return g.scale_off;
+}
+
+fa_status fa_kv_set_scale(void *planes, int nslots, int kv_fmt, int n_kv_heads, int max_seq,
+                          int head_dim, float scale, fa_stream_t stream) {
+    if (kv_fmt != FA_KV_FP8_E4M3 || nslots < 0) return FA_ERR_INVALID;
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return FA_ERR_INVALID;
+    fa::PlaneGeom g;
+    if (!fa::plane_geom(kv_fmt, n_kv_heads, max_seq, head_dim, &g)) return FA_ERR_INVALID;
+    if (!supported_hd(head_dim)) return FA_ERR_UNSUPPORTED;
+    if (nslots == 0) return FA_OK;
+    if (!planes || !aligned16(planes)) return FA_ERR_INVALID;
+    return from_cuda(fa::launch_kv_set_scale(static_cast<uint8_t *>(planes), nslots, g.bytes,
+                                             g.scale_off, scale,
+                                             reinterpret_cast<cudaStream_t>(stream)));
 }
 
 fa_status fa_kv_append(const float *k_new, const float *v_new, void *k_planes, void *v_planes,
@@ -267,17 +302,26 @@ fa_status fa_prefill_chunk(const float *q, const void *k, const void *v, float *
     unsigned *ctr = reinterpret_cast<unsigned *>(ws + w.ctr_off);
     cudaError_t e =
         fa::launch_stage_q(q, qh, static_cast<size_t>(n) * n_q_heads * head_dim, ctr, s);
-    if (e == cudaSuccess)
-        e = fa::launch_stage_kv(static_cast<const uint8_t *>(k), kh, nk, g, shadow_sink,
-                                shadow_win, s);
-    if (e == cudaSuccess)
-        e = fa::launch_stage_kv(static_cast<const uint8_t *>(v), vh, nk, g, shadow_sink,
-                                shadow_win, s);
+    // An fp16 cache body is already the kernel's operand layout ([Hkv][rows]
+    // [hd] binary16): the kernel's tensor maps read the planes in place.
+    const bool direct = kv_fmt == FA_KV_F16;
+    if (direct) {
+        kh = reinterpret_cast<__half *>(static_cast<uint8_t *>(const_cast<void *>(k)) + g.body_off);
+        vh = reinterpret_cast<__half *>(static_cast<uint8_t *>(const_cast<void *>(v)) + g.body_off);
+    } else {
+        if (e == cudaSuccess)
+            e = fa::launch_stage_kv(static_cast<const uint8_t *>(k), kh, nk, g, shadow_sink,
+                                    shadow_win, s);
+        if (e == cudaSuccess)
+            e = fa::launch_stage_kv(static_cast<const uint8_t *>(v), vh, nk, g, shadow_sink,
+                                    shadow_win, s);
+    }
     if (e != cudaSuccess) return FA_ERR_CUDA;
     fa::PrefillArgs a;
     a.qh = qh;
     a.kh = kh;
     a.vh = vh;
+    a.kv_rows = direct ? max_seq : nk;
     a.out = out;
     a.tile_map = tile_map;
     a.work_counter = ctr;

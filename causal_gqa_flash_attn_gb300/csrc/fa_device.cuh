@@ -9,6 +9,7 @@
 
 #include <cuda.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include "fa_internal.h"
@@ -306,6 +307,32 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// fp8 e4m3fn store of 4 values (byte i = value i): x / c with IEEE division,
+// then the conversion with nearest-even rounding and saturation to +-448.
+__device__ __forceinline__ uint32_t fp8x4(float4 x, float c) {
+    const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+        make_float2(__fdiv_rn(x.x, c), __fdiv_rn(x.y, c)), __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+        make_float2(__fdiv_rn(x.z, c), __fdiv_rn(x.w, c)), __NV_SATFINITE, __NV_E4M3);
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// fp8 e4m3fn read of 2 values (byte 0 first): float(byte) * c in fp32, the
+// product rounded to binary16 (the MMA operand) and packed low-first. Every
+// e4m3 value is exact in binary16, so the first conversion loses nothing.
+__device__ __forceinline__ uint32_t fp8x2_to_half2_scaled(uint32_t two_bytes, float c) {
+    const __half2_raw r =
+        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_bytes), __NV_E4M3);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&r));
+    return pack_half2(__fmul_rn(f.x, c), __fmul_rn(f.y, c));
+}
+
+// 8 fp8 values (bytes 0..7 of w) -> 8 binary16 values, scaled.
+__device__ __forceinline__ uint4 fp8x8_to_half8_scaled(uint2 w, float c) {
+    return make_uint4(fp8x2_to_half2_scaled(w.x & 0xffffu, c), fp8x2_to_half2_scaled(w.x >> 16, c),
+                      fp8x2_to_half2_scaled(w.y & 0xffffu, c), fp8x2_to_half2_scaled(w.y >> 16, c));
 }
 
 // ---------------------------------------------------- warp-level MMA path

@@ -27,14 +27,23 @@ struct PlaneGeom {
     int hd;
     size_t row_bytes;
     size_t body_off;
-    size_t sink_off;  // Q4_0 only
-    size_t ring_off;  // Q4_0 only
-    size_t bytes;     // whole plane, multiple of 256
+    size_t sink_off;   // Q4_0 only
+    size_t ring_off;   // Q4_0 only
+    size_t scale_off;  // FP8_E4M3 only: the plane's fp32 scale
+    size_t bytes;      // whole plane, multiple of 256
 };
+
+// Format codes (include/fa.h).
+constexpr int kFmtF32 = 0;
+constexpr int kFmtQ4 = 1;
+constexpr int kFmtF16 = 2;
+constexpr int kFmtFp8 = 3;
 
 bool plane_geom(int fmt, int n_kv, int max_seq, int hd, PlaneGeom *g);
 
 // ---- kv_append.cu
+cudaError_t launch_kv_set_scale(uint8_t *planes, int nslots, size_t plane_bytes, size_t scale_off,
+                                float scale, cudaStream_t stream);
 cudaError_t launch_kv_append(const float *k_new, const float *v_new, uint8_t *k_planes,
                              uint8_t *v_planes, const int32_t *pos0, int nslots, int n,
                              const PlaneGeom &g, int shadow_sink, int shadow_win,
@@ -50,8 +59,9 @@ cudaError_t launch_stage_kv(const uint8_t *plane, __half *dst, int n, const Plan
 // ---- prefill_tc.cu
 struct PrefillArgs {
     const __half *qh;   // [n][Hq][hd] fp16
-    const __half *kh;   // [Hkv][pos0 + n][hd] fp16
-    const __half *vh;   // [Hkv][pos0 + n][hd] fp16
+    const __half *kh;   // [Hkv][kv_rows][hd] fp16, rows 0 .. pos0+n-1 read
+    const __half *vh;   // [Hkv][kv_rows][hd] fp16
+    int kv_rows;        // rows per kv head of kh, vh (>= pos0 + n)
     float *out;         // [n][Hq][hd] fp32
     uint8_t *tile_map;  // optional
     unsigned *work_counter;  // prefill work queue, zeroed by launch_stage_q

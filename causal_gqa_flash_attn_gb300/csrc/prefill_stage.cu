@@ -11,7 +11,9 @@
 //     rows when the shadow window is 256 wide ("attention.cu",
 //     fc_kvq4_is_fp16 with the ring liveness floor of fc_attn_flash_prefill_q4,
 //     which for that width depends on s alone), and otherwise the decoded
-//     (c - 8) * d, exact in fp32, rounded once to fp16.
+//     (c - 8) * d, exact in fp32, rounded once to fp16. For an fp8 e4m3fn cache
+//     it is float(byte) * scale in fp32 (the plane's scale), rounded to fp16.
+//     An fp16 cache needs no staging: the prefill reads its planes in place.
 // Dequantising once here, instead of inside every prefill block that reads a
 // key tile, keeps the Q4_0 ALU work O(n) instead of O(n^2 / 128).
 #include "fa_device.cuh"
@@ -48,6 +50,25 @@ __global__ void __launch_bounds__(kThreads)
         const float4 x = __ldg(reinterpret_cast<const float4 *>(
             plane + body_off + ((static_cast<size_t>(g) * max_seq + s) * hd + 4 * e4) * 4));
         dst[i] = make_uint2(pack_half2(x.x, x.y), pack_half2(x.z, x.w));
+    }
+}
+
+// fp8 e4m3fn cache rows -> fp16, one thread per 8 values (8 bytes in, 16 out).
+__global__ void __launch_bounds__(kThreads)
+    stage_kv_fp8_kernel(const uint8_t *__restrict__ plane, uint4 *__restrict__ dst, int n,
+                        int n_kv, int hd, int max_seq, size_t body_off, size_t scale_off) {
+    const int q8 = hd / 8;
+    const long long total = static_cast<long long>(n_kv) * n * q8;
+    const float c = __ldg(reinterpret_cast<const float *>(plane + scale_off));
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int e8 = static_cast<int>(i % q8);
+        const long long r = i / q8;
+        const int s = static_cast<int>(r % n);
+        const int g = static_cast<int>(r / n);
+        const uint2 w = __ldg(reinterpret_cast<const uint2 *>(
+            plane + body_off + (static_cast<size_t>(g) * max_seq + s) * hd + 8 * e8));
+        dst[i] = fp8x8_to_half8_scaled(w, c);
     }
 }
 
@@ -125,10 +146,17 @@ cudaError_t launch_stage_q(const float *q, __half *qh, size_t count, unsigned *c
 
 cudaError_t launch_stage_kv(const uint8_t *plane, __half *dst, int n, const PlaneGeom &g,
                             int shadow_sink, int shadow_win, cudaStream_t stream) {
-    if (g.fmt == 0) {
+    if (g.fmt == kFmtF32) {
         const long long items = static_cast<long long>(g.n_kv) * n * (g.hd / 4);
         stage_kv_f32_kernel<<<grid_for(items), kThreads, 0, stream>>>(
             plane, reinterpret_cast<uint2 *>(dst), n, g.n_kv, g.hd, g.max_seq, g.body_off);
+    } else if (g.fmt == kFmtFp8) {
+        const long long items = static_cast<long long>(g.n_kv) * n * (g.hd / 8);
+        stage_kv_fp8_kernel<<<grid_for(items), kThreads, 0, stream>>>(
+            plane, reinterpret_cast<uint4 *>(dst), n, g.n_kv, g.hd, g.max_seq, g.body_off,
+            g.scale_off);
+    } else if (g.fmt != kFmtQ4) {
+        return cudaErrorInvalidValue;  // fp16 planes are read in place
     } else {
         const long long items = static_cast<long long>(g.n_kv) * n * (g.hd / kQ4Block);
         stage_kv_q4_kernel<<<grid_for(items), kThreads, 0, stream>>>(

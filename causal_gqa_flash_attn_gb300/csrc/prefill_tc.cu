@@ -564,9 +564,12 @@ cudaError_t launch_hd(const PrefillArgs &a, unsigned *err, cudaStream_t stream) 
     CUtensorMap tq, tk, tv, to;
     const uint64_t n = a.n, Hq = a.n_q_heads, Hkv = a.n_kv_heads;
     const uint64_t L = static_cast<uint64_t>(a.pos0) + a.n;  // key rows
+    const uint64_t head_stride = static_cast<uint64_t>(a.kv_rows) * HD * 2;
+    // rows L .. kv_rows-1 of a head are outside the map: a box reaching them
+    // reads zeros, never the unwritten rows of a cache plane
     if (!encode_3d(&tq, a.qh, HD, Hq, n, HD * 2, Hq * HD * 2, 64, 1, C::BQ) ||
-        !encode_3d(&tk, a.kh, HD, L, Hkv, HD * 2, L * HD * 2, 64, C::BK, 1) ||
-        !encode_3d(&tv, a.vh, HD, L, Hkv, HD * 2, L * HD * 2, 64, C::BK, 1) ||
+        !encode_3d(&tk, a.kh, HD, L, Hkv, HD * 2, head_stride, 64, C::BK, 1) ||
+        !encode_3d(&tv, a.vh, HD, L, Hkv, HD * 2, head_stride, 64, C::BK, 1) ||
         !encode_3d(&to, a.out, HD, Hq, n, HD * 4, Hq * HD * 4, 32, 1, 32,
                    CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
         return cudaErrorInvalidValue;

@@ -53,8 +53,10 @@ typedef enum {
 
 /* KV cache formats. */
 enum {
-    FA_KV_F32 = 0, /* rows of head_dim fp32 values */
-    FA_KV_Q4_0 = 1 /* rows of head_dim/32 Q4_0 blocks of 18 bytes, plus fp16 shadows */
+    FA_KV_F32 = 0,     /* rows of head_dim fp32 values */
+    FA_KV_Q4_0 = 1,    /* rows of head_dim/32 Q4_0 blocks of 18 bytes, plus fp16 shadows */
+    FA_KV_F16 = 2,     /* rows of head_dim binary16 values */
+    FA_KV_FP8_E4M3 = 3 /* rows of head_dim fp8 e4m3fn bytes, plus the plane's fp32 scale */
 };
 
 /* Q4_0 fp16 shadow capacity ("attention.cu", 4-bit KV cache section): up to 8
@@ -81,6 +83,17 @@ enum {
  *   ring  [n_kv_heads][FA_Q4_RING_ROWS][head_dim] binary16 (Q4_0 only)
  *         position s in slot s % 256 while s is among the 256 newest rows.
  *
+ *   F16:  row_bytes = head_dim * 2, each value stored as binary16, rounded to
+ *         nearest even (the half-width KV cache of "qwen38_batched.rs", the
+ *         BQ_KV16 storage: store __float2half, read __half2float).
+ *   FP8_E4M3: row_bytes = head_dim, one fp8 e4m3fn byte per value (1 sign,
+ *         4 exponent bits with bias 7, 3 mantissa bits, no infinities, 0x7f
+ *         and 0xff are NaN, largest finite 448). The plane holds one fp32
+ *         scale at fa_kv_scale_offset() (the per-tensor k_scale / v_scale of
+ *         "vt/ops.h", PagedAttentionArgs and ReshapeAndCacheFp8): the append
+ *         stores byte = e4m3(x / scale), rounded to nearest even and
+ *         saturated to +-448; readers see float(byte) * scale.
+ *
  * The bytes are an interface: a host can read or write a plane directly
  * (a checkpoint of the cache is a copy of its planes).
  */
@@ -88,11 +101,24 @@ enum {
 /* Bytes of one plane, or 0 for an invalid/unsupported geometry. */
 size_t fa_kv_plane_bytes(int kv_fmt, int n_kv_heads, int max_seq, int head_dim);
 
-/* Offsets of the parts of a plane; sink/ring offsets are 0 for FA_KV_F32.
+/* Offsets of the parts of a plane; sink/ring offsets are 0 for every format
+ * but FA_KV_Q4_0.
  * Any output pointer may be NULL. */
 fa_status fa_kv_plane_layout(int kv_fmt, int n_kv_heads, int max_seq, int head_dim,
                              size_t *row_bytes, size_t *body_offset, size_t *sink_offset,
                              size_t *ring_offset);
+
+/* Offset of the fp32 scale inside an FA_KV_FP8_E4M3 plane (the body rounded
+ * up to 256 bytes), or 0 for the other formats and invalid geometries. */
+size_t fa_kv_scale_offset(int kv_fmt, int n_kv_heads, int max_seq, int head_dim);
+
+/* Set the scale of nslots consecutive FA_KV_FP8_E4M3 planes (the K planes
+ * take k_scale, the V planes v_scale: one call for each). Set it before the
+ * first append: rows stored under one scale and read under another are
+ * misread. scale must be finite and > 0, else FA_ERR_INVALID. Asynchronous
+ * on stream (a kernel writes the value, so the call can be captured). */
+fa_status fa_kv_set_scale(void *planes, int nslots, int kv_fmt, int n_kv_heads, int max_seq,
+                          int head_dim, float scale, fa_stream_t stream);
 
 /* Append n new K/V rows to each of nslots caches ("attention.cu",
  * fc_attn_kv_append, fc_attn_kv_append_q4, fc_attn_kv_append_slots_q4).
@@ -104,6 +130,12 @@ fa_status fa_kv_plane_layout(int kv_fmt, int n_kv_heads, int max_seq, int head_d
  *                 position pos0[u] + t. Rows with pos0[u] < 0 or
  *                 pos0[u] + t >= max_seq are skipped and flag FA_ERR_DEVICE.
  *   kv_fmt        FA_KV_F32: rows are copied.
+ *                 FA_KV_F16: each value rounded to binary16, nearest even.
+ *                 FA_KV_FP8_E4M3: each value x of a plane with scale c
+ *                 becomes e4m3(x / c) (IEEE fp32 division, nearest even,
+ *                 saturating to +-448; NaN stays NaN). A plane whose scale
+ *                 is not finite and > 0 is not written and flags
+ *                 FA_ERR_DEVICE.
  *                 FA_KV_Q4_0: each 32-element block is quantised: amax =
  *                 max |x| (NaN ignored), d = amax / -8, id = d != 0 ? 1/d : 0,
  *                 code = clamp(round_half_even(x * id) + 8, 0, 15) with the
@@ -113,8 +145,8 @@ fa_status fa_kv_plane_layout(int kv_fmt, int n_kv_heads, int max_seq, int head_d
  *                 also written to the fp16 sink; when shadow_win > 0 the rows
  *                 of this call that remain among the 256 newest are written to
  *                 the fp16 ring.
- *   shadow_sink   0..8 (Q4_0; must be 0 for F32).
- *   shadow_win    0..256 (Q4_0; must be 0 for F32). Readers must pass the same
+ *   shadow_sink   0..8 (Q4_0; must be 0 for the other formats).
+ *   shadow_win    0..256 (Q4_0; must be 0 for the other formats). Readers must pass the same
  *                 shadow geometry as the appends that built the cache.
  */
 fa_status fa_kv_append(const float *k_new, const float *v_new, void *k_planes, void *v_planes,
@@ -145,7 +177,8 @@ fa_status fa_prefill_tile_shape(int head_dim, int *bq, int *bk);
  *              [0, sink) U [p - win + 1, p] for the query at p. Key tiles
  *              outside it are skipped before any load; boundary tiles are
  *              masked key by key.
- *   kv_fmt     FA_KV_F32 or FA_KV_Q4_0. A Q4_0 key s is read from its fp16
+ *   kv_fmt     FA_KV_F32, FA_KV_F16, FA_KV_FP8_E4M3 (the plane's scale
+ *              applied on read) or FA_KV_Q4_0. A Q4_0 key s is read from its fp16
  *              copy when s < shadow_sink, or when shadow_win > 0 and s is in
  *              the shadow window of the query and still in the ring
  *              ("attention.cu", fc_kvq4_is_fp16 and the ring liveness floor

@@ -32,12 +32,15 @@ def assert_close(got, want, what=""):
 
 
 def fmt_code(kv_fmt: str) -> int:
-    return {"f32": 0, "q4_0": 1}[kv_fmt]
+    from workloads import FMT_CODES
+    return FMT_CODES[kv_fmt]
 
 
-def build_cache(k, v, *, kv_fmt, shadow_sink=0, shadow_win=0, max_seq=None, pos0=None):
+def build_cache(k, v, *, kv_fmt, shadow_sink=0, shadow_win=0, max_seq=None, pos0=None,
+                k_scale=1.0, v_scale=1.0):
     """Append K, V ([nslots][n][Hkv][hd] or [n][Hkv][hd] float32 numpy) into
-    fresh planes; returns (k_planes, v_planes, max_seq)."""
+    fresh planes (fp8 planes with the given scales); returns (k_planes,
+    v_planes, max_seq)."""
     m = fa()
     k = np.asarray(k, np.float32)
     v = np.asarray(v, np.float32)
@@ -47,8 +50,8 @@ def build_cache(k, v, *, kv_fmt, shadow_sink=0, shadow_win=0, max_seq=None, pos0
     if max_seq is None:
         max_seq = n
     code = fmt_code(kv_fmt)
-    kp = m.alloc_planes(nslots, code, hkv, max_seq, hd)
-    vp = m.alloc_planes(nslots, code, hkv, max_seq, hd)
+    kp = m.alloc_planes(nslots, code, hkv, max_seq, hd, scale=k_scale)
+    vp = m.alloc_planes(nslots, code, hkv, max_seq, hd, scale=v_scale)
     p0 = torch.zeros(nslots, dtype=torch.int32, device="cuda") if pos0 is None else \
         torch.as_tensor(np.asarray(pos0, np.int32), device="cuda")
     m.kv_append(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(), kp, vp, p0,
@@ -57,13 +60,15 @@ def build_cache(k, v, *, kv_fmt, shadow_sink=0, shadow_win=0, max_seq=None, pos0
     return kp, vp, max_seq
 
 
-def run_prefill(q, k, v, *, kv_fmt, sink, win, shadow_sink=0, shadow_win=0, tile_map=False):
+def run_prefill(q, k, v, *, kv_fmt, sink, win, shadow_sink=0, shadow_win=0, tile_map=False,
+                max_seq=None, k_scale=1.0, v_scale=1.0):
     """Append then prefill on the GPU; returns out (numpy) and the tile map."""
     m = fa()
     n, hq, hd = q.shape
     hkv = k.shape[1]
     kp, vp, max_seq = build_cache(k, v, kv_fmt=kv_fmt, shadow_sink=shadow_sink,
-                                  shadow_win=shadow_win)
+                                  shadow_win=shadow_win, max_seq=max_seq, k_scale=k_scale,
+                                  v_scale=v_scale)
     qd = torch.from_numpy(np.ascontiguousarray(q)).cuda()
     out = torch.full((n, hq, hd), float("nan"), dtype=torch.float32, device="cuda")
     ws = torch.empty(m.prefill_workspace_bytes(n, hq, hkv, hd), dtype=torch.uint8, device="cuda")

@@ -89,8 +89,10 @@ def test_prefill_validation(fa):
     assert _prefill_status(fa, out=24) == fa.ERR_INVALID           # misaligned
     assert _prefill_status(fa, n=17, max_seq=16) == fa.ERR_INVALID
     assert _prefill_status(fa, sink=-1) == fa.ERR_INVALID
-    assert _prefill_status(fa, fmt=3) == fa.ERR_INVALID
-    assert _prefill_status(fa, fmt=0, ss=4) == fa.ERR_INVALID       # shadows only for Q4_0
+    assert _prefill_status(fa, fmt=7) == fa.ERR_INVALID            # no such format
+    for fmt in (0, 2, 3):                                          # shadows only for Q4_0
+        assert _prefill_status(fa, fmt=fmt, ss=4) == fa.ERR_INVALID
+        assert _prefill_status(fa, fmt=fmt, sw=256) == fa.ERR_INVALID
     assert _prefill_status(fa, fmt=1, ss=9) == fa.ERR_INVALID
     assert _prefill_status(fa, fmt=1, sw=257) == fa.ERR_INVALID
     assert _prefill_status(fa, fmt=1, sw=100) == fa.ERR_UNSUPPORTED
@@ -148,3 +150,33 @@ def test_prefill_lse_and_merge_reject_bad_arguments(fa):
     assert merge(out=8) == fa.ERR_INVALID
     assert merge(pl=18) == fa.ERR_INVALID
     assert merge(out_lse=2) == fa.ERR_INVALID
+
+
+def test_f16_and_fp8_planes(fa):
+    """fp16 rows of 2*hd bytes; fp8 rows of hd bytes plus a 256-byte block for
+    the plane's fp32 scale right after the (256-rounded) body."""
+    for hd in (64, 128, 256):
+        row, body, sink, ring = fa.kv_plane_layout(fa.KV_F16, 2, 1000, hd)
+        assert (row, body, sink, ring) == (2 * hd, 0, 0, 0)
+        assert fa.kv_plane_bytes(fa.KV_F16, 2, 1000, hd) == ((2 * 1000 * 2 * hd + 255) // 256) * 256
+        assert fa.kv_scale_offset(fa.KV_F16, 2, 1000, hd) == 0
+        row, body, sink, ring = fa.kv_plane_layout(fa.KV_FP8_E4M3, 2, 1000, hd)
+        assert (row, body, sink, ring) == (hd, 0, 0, 0)
+        so = fa.kv_scale_offset(fa.KV_FP8_E4M3, 2, 1000, hd)
+        assert so == ((2 * 1000 * hd + 255) // 256) * 256
+        assert fa.kv_plane_bytes(fa.KV_FP8_E4M3, 2, 1000, hd) == so + 256
+    assert fa.kv_scale_offset(fa.KV_Q4_0, 2, 1000, 64) == 0
+
+
+def test_fp8_scale_and_narrow_format_validation(fa):
+    L = fa.lib()
+    # fa_kv_set_scale(planes, nslots, fmt, hkv, max_seq, hd, scale, stream)
+    for bad in (0.0, -1.0, float("nan"), float("inf")):
+        assert L.fa_kv_set_scale(16, 1, fa.KV_FP8_E4M3, 2, 64, 64, bad, None) == fa.ERR_INVALID
+    assert L.fa_kv_set_scale(16, 1, fa.KV_F16, 2, 64, 64, 1.0, None) == fa.ERR_INVALID
+    assert L.fa_kv_set_scale(None, 1, fa.KV_FP8_E4M3, 2, 64, 64, 1.0, None) == fa.ERR_INVALID
+    assert L.fa_kv_set_scale(16, 0, fa.KV_FP8_E4M3, 2, 64, 64, 1.0, None) == fa.OK
+    # the narrow formats have no fp16 shadows
+    for fmt in (fa.KV_F16, fa.KV_FP8_E4M3):
+        assert L.fa_kv_append(16, 16, 16, 16, 16, 1, 8, 2, 64, 16, fmt, 1, 0, None) == fa.ERR_INVALID
+        assert L.fa_kv_append(16, 16, 16, 16, 16, 0, 8, 2, 64, 16, fmt, 0, 0, None) == fa.OK

@@ -32,11 +32,13 @@ class Workload:
     head_dim: int
     sink: int          # attended set: sinks [0, sink)
     win: int           # attended set: recent window of win keys (<= 0: full causal)
-    kv_fmt: str        # "f32" or "q4_0"
+    kv_fmt: str        # "f32", "q4_0", "f16" or "fp8_e4m3"
     shadow_sink: int = 0   # fp16 shadow geometry of a Q4_0 cache
     shadow_win: int = 0
     nslots: int = 1
     split_keys: int = 256
+    k_scale: float = 1.0   # per-tensor scales of an fp8 cache (1.0: uncalibrated)
+    v_scale: float = 1.0
 
     @property
     def seed(self) -> int:
@@ -52,7 +54,16 @@ WORKLOADS = [
              "q4_0", shadow_sink=4, shadow_win=256),
     Workload("decode_q4_32slots_L32768_h16x2_d256_sink4", 4, "decode", 32768, 16, 2, 256, 4, 0,
              "q4_0", shadow_sink=4, shadow_win=0, nslots=32, split_keys=256),
+    # the same shapes over the fp16 and fp8 e4m3fn cache formats
+    Workload("prefill_f16_n8192_h16x2_d256", 5, "prefill", 8192, 16, 2, 256, 0, 0, "f16"),
+    Workload("prefill_fp8_n8192_h16x2_d256", 6, "prefill", 8192, 16, 2, 256, 0, 0, "fp8_e4m3"),
+    Workload("decode_f16_32slots_L32768_h16x2_d256_sink4", 7, "decode", 32768, 16, 2, 256, 4, 0,
+             "f16", nslots=32, split_keys=256),
+    Workload("decode_fp8_32slots_L32768_h16x2_d256_sink4", 8, "decode", 32768, 16, 2, 256, 4, 0,
+             "fp8_e4m3", nslots=32, split_keys=256),
 ]
+
+FMT_CODES = {"f32": 0, "q4_0": 1, "f16": 2, "fp8_e4m3": 3}  # include/fa.h FA_KV_*
 
 BY_NAME = {w.name: w for w in WORKLOADS}
 
