@@ -526,7 +526,8 @@ def main():
         "decode_fp8_32slots_L32768_h16x2_d256_sink4")
     for name in decode_names:
         w = BY_NAME[name]
-        kname = "decode_q4_kernel<256>" if w.kv_fmt == "q4_0" else "decode_kernel<256,1>"
+        kname = {"q4_0": "decode_q4_kernel<256>", "f16": "decode_dense_kernel<256,f16>",
+                 "fp8_e4m3": "decode_dense_kernel<256,fp8>"}[w.kv_fmt]
         S = B.decode_setup(w)
         kvb = decode_kv_bytes(w)
         sm, km = B.timed_steps(lambda: B.decode_step(S), args.warmup, args.steps)
@@ -537,7 +538,9 @@ def main():
                          "roofline": {"kernel": kname, "bound": "hbm",
                                       "achieved": a, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                       "frac": a / peaks["hbm_gbs"], "frac_of_8tbs": a / 8000.0,
-                                      "traffic": profiled_traffic(kname, src_hash("decode.cu")),
+                                      "traffic": profiled_traffic(
+                                          kname, src_hash("decode.cu" if w.kv_fmt == "q4_0"
+                                                          else "decode_dense.cu")),
                                       "kernel_ms": statistics.mean(km)}}
         del S
         torch.cuda.empty_cache()

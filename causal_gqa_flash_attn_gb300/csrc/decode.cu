@@ -28,6 +28,7 @@
 //  * decode_kernel (fp32 caches, group 16, and that shadow entry): stages
 //    16-key fp16 tiles in shared memory, reads fragments with ldmatrix.
 // Each block merges its warps; fa_decode_combine merges the entries.
+#include "decode_softmax.cuh"
 #include "fa_device.cuh"
 #include "fa_internal.h"
 
@@ -161,48 +162,6 @@ __device__ __forceinline__ void merge_finish(const DecodeParams &P, uint8_t *dsm
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) a += sm_f[w * 16 + head] * sm_o[(w * 16 + head) * HD + dim];
         P.ws_acc[((head0 + head) * P.stride + e) * HD + dim] = a;
-    }
-}
-
-// Online-softmax fold of one group of scores of two heads (exp2 domain).
-// sv: this thread's scores (-inf when masked), n of them per head.
-template <int MT, int NT, int N>
-__device__ __forceinline__ void fold_scores(float (&sv)[2][N], float sl2, float thr,
-                                            float &mu0, float &mu1, float &mt0, float &mt1,
-                                            float &ls0, float &ls1, float (&o)[MT][NT][4],
-                                            int nt, float (&pv)[2][N]) {
-    float *mu[2] = {&mu0, &mu1};
-    float *mtr[2] = {&mt0, &mt1};
-    float *ls[2] = {&ls0, &ls1};
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-        float mx = sv[hh][0];
-#pragma unroll
-        for (int k = 1; k < N; ++k) mx = fmaxf(mx, sv[hh][k]);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float mx2 = mx * sl2;
-        *mtr[hh] = fmaxf(*mtr[hh], mx2);
-        const float m_new = fmaxf(*mu[hh], mx2);
-        if (m_new > *mu[hh] + thr) {
-            const float corr = ex2(*mu[hh] - m_new);  // 0 while nothing was seen
-            *ls[hh] *= corr;
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                o[mt][nt][hh] *= corr;
-                o[mt][nt][2 + hh] *= corr;
-            }
-            *mu[hh] = m_new;
-        }
-        const float mref = (*mu[hh] == -INFINITY) ? 0.0f : *mu[hh];
-        float s = 0.0f;
-#pragma unroll
-        for (int k = 0; k < N; ++k) {
-            pv[hh][k] = ex2(fmaf(sv[hh][k], sl2, -mref));
-            s += pv[hh][k];
-        }
-        *ls[hh] += s;
     }
 }
 
@@ -1080,6 +1039,16 @@ DecodeShape decode_shape(int nslots, int n_q_heads, int n_kv_heads, int kv_fmt, 
     // The Q4_0 path bulk-copies rows of a kv head; a copy must start 16-byte
     // aligned, so every head's body must start 16-byte aligned.
     d.fast = kv_fmt == kFmtQ4 && G <= 8 && (static_cast<size_t>(max_seq) * row_bytes) % 16 == 0;
+    const int hd = kv_fmt == kFmtF16 ? static_cast<int>(row_bytes / 2) : static_cast<int>(row_bytes);
+    d.dense = (kv_fmt == kFmtF16 || kv_fmt == kFmtFp8) && dense_decode_supported(kv_fmt, G, hd);
+    if (d.dense) {
+        // persistent stream-K kernel: any entry of the workspace may be used
+        d.splits_per_cta = 1;
+        d.body_entries = max_splits + 1;
+        d.shadow_entry = -1;
+        d.entries = max_splits + 1;
+        return d;
+    }
     // Blocks to aim at: the Q4_0 path keeps 2 blocks per SM, so 8 per SM is
     // about four waves and the last one is short; the generic path, 4 per SM.
     const long long pairs = static_cast<long long>(nslots) * n_kv_heads;
@@ -1147,6 +1116,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodeWs &ws, const DecodeS
     P.scale_off = a.g.scale_off;
     P.sl2 = a.scale * 1.4426950408889634f;
     P.err = err;
+    if (d.dense) return launch_decode_dense(a, ws, err, stream);
     if (d.entries > ws.stride) return cudaErrorInvalidValue;
     const int G = a.n_q_heads / a.n_kv_heads;
     if (d.fast) {

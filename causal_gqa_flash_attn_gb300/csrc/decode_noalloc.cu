@@ -68,7 +68,7 @@ extern "C" fa_status fa_decode_noalloc(const float *q, const void *k_planes,
         return FA_ERR_UNSUPPORTED;
     if (nslots < 0 || sink < 0 || max_seq < 1 || split_keys < 1 || max_splits < 1)
         return FA_ERR_INVALID;
-    if (kv_fmt == FA_KV_F32) {
+    if (kv_fmt == FA_KV_F32 || kv_fmt == FA_KV_F16 || kv_fmt == FA_KV_FP8_E4M3) {
         if (shadow_sink != 0 || shadow_win != 0) return FA_ERR_INVALID;
     } else if (kv_fmt == FA_KV_Q4_0) {
         if (shadow_sink < 0 || shadow_sink > FA_Q4_SINK_MAX || shadow_win < 0 ||
@@ -90,7 +90,13 @@ extern "C" fa_status fa_decode_noalloc(const float *q, const void *k_planes,
     const fa::DecodeShape shape = fa::decode_shape(nslots, n_q_heads, n_kv_heads, kv_fmt,
                                                    shadow_sink, shadow_win, max_splits, max_seq,
                                                    g.row_bytes);
-    const int entries = shape.entries;
+    int entries = shape.entries;
+    if (shape.dense) {
+        // the streaming kernel adapts its work split to the entries it has
+        while (entries > 2 &&
+               fa::decode_ws_bytes(nslots, n_q_heads, head_dim, entries) > kFaDecodeScratchBytes)
+            --entries;
+    }
     if (fa::decode_ws_bytes(nslots, n_q_heads, head_dim, entries) > kFaDecodeScratchBytes)
         return FA_ERR_WORKSPACE;
 

@@ -74,6 +74,11 @@ constexpr int kPrefillBQ = 128;
 constexpr int kPrefillBK = 128;
 cudaError_t launch_prefill_tc(const PrefillArgs &a, unsigned *err, cudaStream_t stream);
 
+// 128-byte-swizzled tiled tensor map (rank 1..5, zero fill outside the
+// tensor); strides_bytes holds rank-1 entries. False if the driver refuses.
+bool encode_tiled(CUtensorMap *m, CUtensorMapDataType dtype, int rank, const void *base,
+                  const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box);
+
 // ---- merge.cu
 cudaError_t launch_merge_attn_states(float *out, float *out_lse, const float *prefix,
                                      const float *prefix_lse, const float *suffix,
@@ -102,6 +107,7 @@ struct DecodeWs {
 // shadow keys when the Q4_0 fast path is used.
 struct DecodeShape {
     bool fast;           // Q4_0 kernel (group <= 8, 16-byte aligned K/V rows per head)
+    bool dense;          // fp16 / fp8 streaming kernel (decode_dense.cu)
     int splits_per_cta;
     int body_entries;
     int shadow_entry;    // -1 if none
@@ -110,6 +116,11 @@ struct DecodeShape {
 DecodeShape decode_shape(int nslots, int n_q_heads, int n_kv_heads, int kv_fmt, int shadow_sink,
                          int shadow_win, int max_splits, int max_seq, size_t row_bytes);
 size_t decode_ws_bytes(int nslots, int n_q_heads, int head_dim, int stride);
+// ---- decode_dense.cu: fp16 (head_dim 64..256) and fp8 (128, 256) caches, G <= 8.
+// Uses up to ws.stride entries per head (>= 2) and writes the header's count.
+bool dense_decode_supported(int kv_fmt, int G, int head_dim);
+cudaError_t launch_decode_dense(const DecodeArgs &a, const DecodeWs &ws, unsigned *err,
+                                cudaStream_t stream);
 void decode_ws_carve(void *ws, int nslots, int n_q_heads, int head_dim, int stride,
                      DecodeWs *out);
 cudaError_t launch_decode(const DecodeArgs &a, const DecodeWs &ws, const DecodeShape &d,

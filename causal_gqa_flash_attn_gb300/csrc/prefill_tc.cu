@@ -558,6 +558,27 @@ bool encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint6
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+}  // namespace
+
+bool encode_tiled(CUtensorMap *m, CUtensorMapDataType dtype, int rank, const void *base,
+                  const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || rank < 1 || rank > 5) return false;
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], e[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        e[i] = 1;
+        if (i + 1 < rank) st[i] = strides_bytes[i];
+    }
+    return fn(m, dtype, static_cast<cuuint32_t>(rank), const_cast<void *>(base), d, st, b, e,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
 template <int HD>
 cudaError_t launch_hd(const PrefillArgs &a, unsigned *err, cudaStream_t stream) {
     using C = Cfg<HD>;

@@ -176,12 +176,21 @@ def test_prefill_chunk_formats(oracle_mod, fmt, ks, vs):
 
 DECODE_CASES = [
     # lens per slot, hq, hkv, hd, sink, win, fmt, k_scale, v_scale, split_keys, max_seq
+    # (group <= 8 and fp8 head_dim >= 128 run the streaming kernel, the rest the
+    # generic one)
     ((1, 17, 300, 1000), 16, 2, 256, 4, 0, "f16", 1.0, 1.0, 256, 1024),
     ((700, 64, 1500), 8, 2, 128, 4, 100, "f16", 1.0, 1.0, 64, 1600),
     ((999, 5), 16, 1, 64, 0, 0, "f16", 1.0, 1.0, 100, 1000),
     ((1, 17, 300, 1000), 16, 2, 256, 4, 0, "fp8_e4m3", 1.0, 1.0, 256, 1024),
     ((513, 2000), 8, 2, 128, 0, 0, "fp8_e4m3", 0.25, 3.0, 256, 2048),
     ((640, 640, 33), 4, 4, 64, 2, 37, "fp8_e4m3", 0.9, 0.45, 128, 700),
+    # streaming kernel: groups 1, 2, 4, 8; positions 0 and tile edges; windows
+    # that leave one tile, sinks past the position; a workspace of 2 entries
+    ((1, 16, 17, 32, 33, 250), 2, 2, 64, 0, 0, "f16", 1.0, 1.0, 16, 256),
+    ((4000, 1, 2500), 4, 1, 128, 3, 1, "f16", 1.0, 1.0, 4000, 4096),
+    ((3000, 3001, 15, 2999), 8, 8, 128, 40, 16, "fp8_e4m3", 1.7, 0.3, 128, 3072),
+    ((777,) * 9, 32, 4, 256, 0, 0, "fp8_e4m3", 0.5, 0.5, 256, 800),
+    ((2048, 100), 16, 16, 256, 2000, 64, "f16", 1.0, 1.0, 256, 2048),
 ]
 
 
@@ -260,3 +269,45 @@ def test_prefill_format_workload_sampled(oracle_mod, name):
                               k_scale=w.k_scale, v_scale=w.v_scale)
     assert_close(got[rows], want, name)
     assert np.all(np.isfinite(got))
+
+
+def test_decode_dense_noalloc_and_bad_position(oracle_mod):
+    """The streaming kernel through fa_decode_noalloc (fewer entries: the
+    library's fixed array) matches the oracle; a slot whose position is past
+    max_seq flags FA_ERR_DEVICE and leaves the other slots right."""
+    m = fa()
+    lens, hq, hkv, hd, max_seq = (3000, 700, 1), 16, 2, 256, 3072
+    qs, kk, vv = [], [], []
+    for u in range(len(lens)):
+        qu, ku, vu = decode_slot_inputs(max(lens), hq, hkv, hd, seed=6060, slot=u)
+        qs.append(qu)
+        kk.append(ku)
+        vv.append(vu)
+    q = torch.from_numpy(np.stack(qs)).cuda()
+    for fmt, ks, vs in (("f16", 1.0, 1.0), ("fp8_e4m3", 0.8, 1.25)):
+        code = fmt_code(fmt)
+        kp = m.alloc_planes(len(lens), code, hkv, max_seq, hd, scale=ks)
+        vp = m.alloc_planes(len(lens), code, hkv, max_seq, hd, scale=vs)
+        pb = m.kv_plane_bytes(code, hkv, max_seq, hd)
+        for u, L in enumerate(lens):
+            m.kv_append(torch.from_numpy(kk[u][None, :L]).cuda(),
+                        torch.from_numpy(vv[u][None, :L]).cuda(), kp[u * pb:(u + 1) * pb],
+                        vp[u * pb:(u + 1) * pb], torch.zeros(1, dtype=torch.int32, device="cuda"),
+                        n_kv_heads=hkv, head_dim=hd, max_seq=max_seq, kv_fmt=code)
+        out = torch.full((len(lens), hq, hd), float("nan"), device="cuda")
+        pos = torch.tensor([L - 1 for L in lens], dtype=torch.int32, device="cuda")
+        m.decode_noalloc(q, kp, vp, pos, out, n_q_heads=hq, n_kv_heads=hkv, head_dim=hd,
+                         max_seq=max_seq, sink=4, win=0, kv_fmt=code, split_keys=256,
+                         max_splits=12)
+        assert m.get_device_error() == m.OK
+        got = out.cpu().numpy()
+        for u, L in enumerate(lens):
+            want = oracle_mod.decode(qs[u], L - 1, kk[u], vv[u], kv_fmt=fmt, sink=4, win=0,
+                                     k_scale=ks, v_scale=vs)
+            assert_close(got[u], want, f"noalloc {fmt} slot {u}")
+        bad = torch.tensor([lens[0] - 1, max_seq, lens[2] - 1], dtype=torch.int32, device="cuda")
+        ws = torch.empty(m.decode_workspace_bytes(len(lens), hq, hd, 12), dtype=torch.uint8,
+                         device="cuda")
+        m.decode(q, kp, vp, bad, n_q_heads=hq, n_kv_heads=hkv, head_dim=hd, max_seq=max_seq,
+                 sink=4, win=0, kv_fmt=code, split_keys=256, max_splits=12, workspace=ws)
+        assert m.get_device_error() == m.ERR_DEVICE

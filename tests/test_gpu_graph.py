@@ -15,7 +15,8 @@ from workloads import decode_slot_inputs
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("kv_fmt,shadow", [("q4_0", (4, 256)), ("f32", (0, 0))])
+@pytest.mark.parametrize("kv_fmt,shadow", [("q4_0", (4, 256)), ("f32", (0, 0)), ("f16", (0, 0)),
+                                           ("fp8_e4m3", (0, 0))])
 def test_decode_step_graph_replay(oracle_mod, kv_fmt, shadow):
     nslots, hq, hkv, hd, max_seq = 3, 16, 2, 128, 1024
     sink, win, kps = 4, 0, 64
