@@ -371,6 +371,11 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--profile", default=None,
                     help="run only this workload (name from workloads.py) for an ncu capture")
+    ap.add_argument("--profile-slots", type=int, default=0,
+                    help="with --profile: decode slots instead of the workload's")
+    ap.add_argument("--profile-n", type=int, default=0,
+                    help="with --profile: prefill tokens (or decode context) instead of the "
+                         "workload's")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -421,7 +426,10 @@ def main():
     peaks = load_peaks()
 
     if args.profile:
+        import dataclasses
         w = BY_NAME[args.profile]
+        w = dataclasses.replace(w, nslots=args.profile_slots or w.nslots,
+                                n=args.profile_n or w.n)
         S = B.decode_setup(w) if w.kind == "decode" else B.prefill_setup(w)
         fn = (lambda: B.decode_step(S)) if w.kind == "decode" else (lambda: B.prefill_step(S))
         sm, km = B.timed_steps(fn, args.warmup, args.steps)
