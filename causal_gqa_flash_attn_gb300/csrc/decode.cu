@@ -459,6 +459,11 @@ constexpr int kPRing = 2;      // P records in flight per pair
 #ifndef FA_Q4_MIN_BLOCKS
 #define FA_Q4_MIN_BLOCKS 2
 #endif
+// Blocks per SM the Q4_0 work split aims at (runs of splits per block are
+// sized so that the grid has about this many blocks per SM).
+#ifndef FA_Q4_TARGET_PER_SM
+#define FA_Q4_TARGET_PER_SM 4
+#endif
 // Unroll factors (1 or 2) of the loops over a tile's two 16-key halves in the
 // QK and PV warps: 2 interleaves the halves' dependency chains, 1 keeps the
 // registers and the code small.
@@ -1049,10 +1054,13 @@ DecodeShape decode_shape(int nslots, int n_q_heads, int n_kv_heads, int kv_fmt, 
         d.entries = max_splits + 1;
         return d;
     }
-    // Blocks to aim at: the Q4_0 path keeps 2 blocks per SM, so 8 per SM is
-    // about four waves and the last one is short; the generic path, 4 per SM.
+    // Blocks to aim at: the Q4_0 path keeps 2 blocks per SM, so 4 per SM is
+    // about two waves (measured at 32 slots x 32768 keys: 160 us against 163 us
+    // at 8 per SM, 195 us at 2, with fewer partials for the combine); the
+    // generic path, 4 per SM.
     const long long pairs = static_cast<long long>(nslots) * n_kv_heads;
-    const long long target = (d.fast ? 8LL : 4LL) * device_sm_count();
+    const long long target =
+        (d.fast ? static_cast<long long>(FA_Q4_TARGET_PER_SM) : 4LL) * device_sm_count();
     long long cpc = (pairs * max_splits + target - 1) / target;
     if (cpc < 1) cpc = 1;
     if (cpc > max_splits) cpc = max_splits;

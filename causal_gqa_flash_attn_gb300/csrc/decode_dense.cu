@@ -41,13 +41,23 @@ constexpr int kBoxRows = 16;                // keys per tile
 constexpr int kBoxBytes = kBoxRows * 128;   // one box: 16 rows x 128 bytes
 constexpr float kRescaleDense = 8.0f;       // lazy-rescale threshold (log2 units)
 
+// Warps per block for 16-KB stages (fp16 at head_dim 256) and for smaller ones.
+#ifndef FA_DENSE_NW_BIG
+#define FA_DENSE_NW_BIG 3
+#endif
+#ifndef FA_DENSE_NW_SMALL
+#define FA_DENSE_NW_SMALL 8
+#endif
+
 template <int HD, int FMT>
 struct DenseCfg {
     static constexpr int EB = FMT == kFmtF16 ? 2 : 1;  // bytes per element
     static constexpr int NBX = HD * EB / 128;          // boxes per K (or V) tile
     static constexpr int TILE = NBX * kBoxBytes;       // K (or V) bytes of a tile
     static constexpr int STAGE = 2 * TILE;
-    static constexpr int NW = (49152 / STAGE >= 6) ? 8 : 4;  // warps per block
+    // warps per block: more stages per warp keep more bytes in flight, more
+    // warps cover the fp8 conversions
+    static constexpr int NW = STAGE >= 16384 ? FA_DENSE_NW_BIG : FA_DENSE_NW_SMALL;
     static constexpr int NS0 = 196608 / (NW * STAGE);
     static constexpr int NS = NS0 > 8 ? 8 : NS0;       // ring stages per warp
     static constexpr int MT = HD / 16;
@@ -121,10 +131,15 @@ __device__ __forceinline__ void it_next(const DenseParams &P, TileIt &it) {
     }
 }
 
-__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two) {
-    const __half2_raw h =
-        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xffffu), __NV_E4M3);
-    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+// Four e4m3 bytes -> two fp16 pairs: bytes 0, 1 -> lo (byte 0 in the low
+// half), bytes 2, 3 -> hi. Exact: every e4m3 value is an fp16 value.
+__device__ __forceinline__ void e4m3x4_to_h2x2(uint32_t x, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(x));
 }
 
 // A bounded wait that ignores the abort flag: used to let this warp's own
@@ -358,10 +373,11 @@ __global__ void __launch_bounds__(DenseCfg<HD, FMT>::NW * 32, 1)
             for (int kp = 0; kp < HD / 32; ++kp) {
                 uint32_t x[4];
                 ldmatrix_x4(x, kb + (kp >> 2) * kBoxBytes + koff + (((2 * (kp & 3)) ^ kz) << 4));
-                uint32_t a0[4] = {e4m3x2_to_h2(x[0]), e4m3x2_to_h2(x[1]), e4m3x2_to_h2(x[0] >> 16),
-                                  e4m3x2_to_h2(x[1] >> 16)};
-                uint32_t a1[4] = {e4m3x2_to_h2(x[2]), e4m3x2_to_h2(x[3]), e4m3x2_to_h2(x[2] >> 16),
-                                  e4m3x2_to_h2(x[3] >> 16)};
+                uint32_t a0[4], a1[4];  // {row r, row r + 8} x {dims 4t..4t+1, 4t+2..4t+3}
+                e4m3x4_to_h2x2(x[0], a0[0], a0[2]);
+                e4m3x4_to_h2x2(x[1], a0[1], a0[3]);
+                e4m3x4_to_h2x2(x[2], a1[0], a1[2]);
+                e4m3x4_to_h2x2(x[3], a1[1], a1[3]);
                 mma_16816(s0, a0, qb[2 * kp]);
                 mma_16816(s1, a1, qb[2 * kp + 1]);
             }
@@ -395,10 +411,11 @@ __global__ void __launch_bounds__(DenseCfg<HD, FMT>::NW * 32, 1)
                 ldmatrix_x4_trans(x, vb + (mp >> 2) * kBoxBytes + voff + (((2 * (mp & 3)) ^ vz) << 4));
                 const uint32_t y0 = __byte_perm(x[0], 0u, 0x3120), y1 = __byte_perm(x[1], 0u, 0x3120);
                 const uint32_t y2 = __byte_perm(x[2], 0u, 0x3120), y3 = __byte_perm(x[3], 0u, 0x3120);
-                uint32_t a0[4] = {e4m3x2_to_h2(y0), e4m3x2_to_h2(y0 >> 16), e4m3x2_to_h2(y1),
-                                  e4m3x2_to_h2(y1 >> 16)};
-                uint32_t a1[4] = {e4m3x2_to_h2(y2), e4m3x2_to_h2(y2 >> 16), e4m3x2_to_h2(y3),
-                                  e4m3x2_to_h2(y3 >> 16)};
+                uint32_t a0[4], a1[4];  // {dim 2r, dim 2r + 1} x {keys 2t.., keys 2t+8..}
+                e4m3x4_to_h2x2(y0, a0[0], a0[1]);
+                e4m3x4_to_h2x2(y1, a0[2], a0[3]);
+                e4m3x4_to_h2x2(y2, a1[0], a1[1]);
+                e4m3x4_to_h2x2(y3, a1[2], a1[3]);
                 mma_16816(o[2 * mp][0], a0, pb);
                 mma_16816(o[2 * mp + 1][0], a1, pb);
             }
