@@ -32,6 +32,7 @@ _P, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 SIGNATURES = {
     "fa_kv_plane_bytes": (_SZ, [_I, _I, _I, _I]),
     "fa_kv_plane_layout": (_I, [_I, _I, _I, _I, _P, _P, _P, _P]),
+    "fa_kv_init": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, _P]),
     "fa_kv_scale_offset": (_SZ, [_I, _I, _I, _I]),
     "fa_kv_set_scale": (_I, [_P, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
     "fa_kv_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
@@ -142,15 +143,28 @@ def kv_set_scale(planes, kv_fmt: int, n_kv_heads: int, max_seq: int, head_dim: i
                                  _stream(stream)), "fa_kv_set_scale")
 
 
+def kv_init(planes, kv_fmt: int, n_kv_heads: int, max_seq: int, head_dim: int,
+            shadow_sink: int = 0, shadow_win: int = 0, stream=None):
+    """fa_kv_init over every plane in ``planes`` (consecutive planes)."""
+    pb = kv_plane_bytes(kv_fmt, n_kv_heads, max_seq, head_dim)
+    if pb == 0 or planes.numel() % pb:
+        raise ValueError("planes is not a whole number of planes of this geometry")
+    _check(lib().fa_kv_init(_dev(planes, torch.uint8, "planes"), planes.numel() // pb, kv_fmt,
+                            n_kv_heads, max_seq, head_dim, shadow_sink, shadow_win,
+                            _stream(stream)), "fa_kv_init")
+
+
 def alloc_planes(nslots: int, kv_fmt: int, n_kv_heads: int, max_seq: int, head_dim: int,
                  device="cuda", scale: float = 1.0) -> torch.Tensor:
-    """nslots consecutive zeroed planes as one uint8 tensor; fp8 planes get
-    ``scale`` (the per-tensor k_scale or v_scale, 1.0 uncalibrated)."""
+    """nslots consecutive planes as one uint8 tensor, prepared by fa_kv_init;
+    fp8 planes get ``scale`` (the per-tensor k_scale or v_scale, 1.0
+    uncalibrated)."""
     pb = kv_plane_bytes(kv_fmt, n_kv_heads, max_seq, head_dim)
     if pb == 0:
         raise ValueError("invalid plane geometry")
-    planes = torch.zeros(nslots * pb, dtype=torch.uint8, device=device)
-    if kv_fmt == KV_FP8_E4M3:
+    planes = torch.empty(nslots * pb, dtype=torch.uint8, device=device)
+    kv_init(planes, kv_fmt, n_kv_heads, max_seq, head_dim)
+    if kv_fmt == KV_FP8_E4M3 and scale != 1.0:
         kv_set_scale(planes, kv_fmt, n_kv_heads, max_seq, head_dim, scale)
     return planes
 

@@ -187,6 +187,25 @@ fa_status fa_kv_plane_layout(int kv_fmt, int n_kv_heads, int max_seq, int head_d
     return FA_OK;
 }
 
+fa_status fa_kv_init(void *planes, int nslots, int kv_fmt, int n_kv_heads, int max_seq,
+                     int head_dim, int shadow_sink, int shadow_win, fa_stream_t stream) {
+    if (nslots < 0 || n_kv_heads < 1 || max_seq < 1 || head_dim < 32 || head_dim % 32)
+        return FA_ERR_INVALID;
+    if (!supported_hd(head_dim)) return FA_ERR_UNSUPPORTED;
+    fa_status st = check_shadow(kv_fmt, shadow_sink, shadow_win);
+    if (st != FA_OK) return st;
+    fa::PlaneGeom g;
+    if (!fa::plane_geom(kv_fmt, n_kv_heads, max_seq, head_dim, &g)) return FA_ERR_INVALID;
+    if (nslots == 0) return FA_OK;
+    if (!planes || !aligned16(planes)) return FA_ERR_INVALID;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(planes, 0, g.bytes * static_cast<size_t>(nslots), s);
+    if (e == cudaSuccess && kv_fmt == FA_KV_FP8_E4M3)
+        e = fa::launch_kv_set_scale(static_cast<uint8_t *>(planes), nslots, g.bytes, g.scale_off,
+                                    1.0f, s);
+    return from_cuda(e);
+}
+
 size_t fa_kv_scale_offset(int kv_fmt, int n_kv_heads, int max_seq, int head_dim) {
     fa::PlaneGeom g;
     if (!supported_hd(head_dim) || !fa::plane_geom(kv_fmt, n_kv_heads, max_seq, head_dim, &g))

@@ -108,6 +108,16 @@ fa_status fa_kv_plane_layout(int kv_fmt, int n_kv_heads, int max_seq, int head_d
                              size_t *row_bytes, size_t *body_offset, size_t *sink_offset,
                              size_t *ring_offset);
 
+/* Prepare nslots consecutive planes for a new sequence: every byte zero
+ * (rows never appended read as 0; Q4_0 shadows empty) and, for
+ * FA_KV_FP8_E4M3, the scale 1.0 (the uncalibrated default; fa_kv_set_scale
+ * changes it). The planes keep no record of the geometry: every later call
+ * on them passes the same (kv_fmt, n_kv_heads, max_seq, head_dim) and the
+ * same shadow geometry, which this call validates (FA_ERR_INVALID /
+ * FA_ERR_UNSUPPORTED as fa_kv_append). Asynchronous on stream; capturable. */
+fa_status fa_kv_init(void *planes, int nslots, int kv_fmt, int n_kv_heads, int max_seq,
+                     int head_dim, int shadow_sink, int shadow_win, fa_stream_t stream);
+
 /* Offset of the fp32 scale inside an FA_KV_FP8_E4M3 plane (the body rounded
  * up to 256 bytes), or 0 for the other formats and invalid geometries. */
 size_t fa_kv_scale_offset(int kv_fmt, int n_kv_heads, int max_seq, int head_dim);

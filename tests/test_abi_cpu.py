@@ -180,3 +180,15 @@ def test_fp8_scale_and_narrow_format_validation(fa):
     for fmt in (fa.KV_F16, fa.KV_FP8_E4M3):
         assert L.fa_kv_append(16, 16, 16, 16, 16, 1, 8, 2, 64, 16, fmt, 1, 0, None) == fa.ERR_INVALID
         assert L.fa_kv_append(16, 16, 16, 16, 16, 0, 8, 2, 64, 16, fmt, 0, 0, None) == fa.OK
+
+
+def test_kv_init_validation(fa):
+    L = fa.lib()
+    # fa_kv_init(planes, nslots, fmt, hkv, max_seq, hd, shadow_sink, shadow_win, stream)
+    assert L.fa_kv_init(16, 1, 7, 2, 64, 64, 0, 0, None) == fa.ERR_INVALID        # format
+    assert L.fa_kv_init(16, 1, fa.KV_F32, 2, 64, 64, 4, 0, None) == fa.ERR_INVALID  # shadows
+    assert L.fa_kv_init(16, 1, fa.KV_Q4_0, 2, 64, 64, 9, 0, None) == fa.ERR_INVALID
+    assert L.fa_kv_init(16, 1, fa.KV_F16, 2, 64, 96, 0, 0, None) == fa.ERR_UNSUPPORTED
+    assert L.fa_kv_init(None, 1, fa.KV_F16, 2, 64, 64, 0, 0, None) == fa.ERR_INVALID
+    assert L.fa_kv_init(24, 1, fa.KV_F16, 2, 64, 64, 0, 0, None) == fa.ERR_INVALID   # misaligned
+    assert L.fa_kv_init(16, 0, fa.KV_Q4_0, 2, 64, 64, 4, 256, None) == fa.OK         # no planes

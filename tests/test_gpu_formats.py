@@ -311,3 +311,21 @@ def test_decode_dense_noalloc_and_bad_position(oracle_mod):
         m.decode(q, kp, vp, bad, n_q_heads=hq, n_kv_heads=hkv, head_dim=hd, max_seq=max_seq,
                  sink=4, win=0, kv_fmt=code, split_keys=256, max_splits=12, workspace=ws)
         assert m.get_device_error() == m.ERR_DEVICE
+
+
+@pytest.mark.parametrize("fmt", ["f32", "q4_0", "f16", "fp8_e4m3"])
+def test_kv_init_zeroes_planes_and_sets_the_fp8_scale(fmt):
+    m = fa()
+    code = fmt_code(fmt)
+    hkv, max_seq, hd, nslots = 2, 40, 64, 3
+    pb = m.kv_plane_bytes(code, hkv, max_seq, hd)
+    planes = torch.full((nslots * pb,), 0xAB, dtype=torch.uint8, device="cuda")
+    m.kv_init(planes, code, hkv, max_seq, hd)
+    torch.cuda.synchronize()
+    host = planes.cpu().numpy().reshape(nslots, pb)
+    so = m.kv_scale_offset(code, hkv, max_seq, hd)
+    for u in range(nslots):
+        if fmt == "fp8_e4m3":
+            assert host[u, so:so + 4].view(np.float32)[0] == 1.0
+            host[u, so:so + 4] = 0
+        assert not host[u].any(), (fmt, u)
