@@ -376,6 +376,8 @@ def main():
     ap.add_argument("--profile-n", type=int, default=0,
                     help="with --profile: prefill tokens (or decode context) instead of the "
                          "workload's")
+    ap.add_argument("--profile-window", default=None,
+                    help="with --profile: 'sink,win' attended set instead of the workload's")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -430,6 +432,9 @@ def main():
         w = BY_NAME[args.profile]
         w = dataclasses.replace(w, nslots=args.profile_slots or w.nslots,
                                 n=args.profile_n or w.n)
+        if args.profile_window:
+            sk, wn = (int(x) for x in args.profile_window.split(","))
+            w = dataclasses.replace(w, sink=sk, win=wn)
         S = B.decode_setup(w) if w.kind == "decode" else B.prefill_setup(w)
         fn = (lambda: B.decode_step(S)) if w.kind == "decode" else (lambda: B.prefill_step(S))
         sm, km = B.timed_steps(fn, args.warmup, args.steps)
