@@ -484,8 +484,9 @@ def main():
     # ---------------- other workloads
     extra = {}
     for name in ("prefill_f32_n8192_h16x2_d256_sink4_win1024",
-                 "prefill_q4_n8192_h16x2_d256_shadow4_256", "prefill_f16_n8192_h16x2_d256",
-                 "prefill_fp8_n8192_h16x2_d256"):
+                 "prefill_q4_n8192_h16x2_d256_shadow4_256",
+                 "prefill_q4_n8192_h16x2_d256_shadow4_256_sink4_win1024",
+                 "prefill_f16_n8192_h16x2_d256", "prefill_fp8_n8192_h16x2_d256"):
         w = BY_NAME[name]
         S = B.prefill_setup(w)
         f = 4.0 * w.head_dim * w.n_q_heads * visible_pairs(w.n, w.sink, w.win)

@@ -157,7 +157,8 @@ def sample_rows(n):
 
 @pytest.mark.parametrize("name", ["prefill_f32_n128_h8x2_d64", "prefill_f32_n8192_h16x2_d256",
                                   "prefill_f32_n8192_h16x2_d256_sink4_win1024",
-                                  "prefill_q4_n8192_h16x2_d256_shadow4_256"])
+                                  "prefill_q4_n8192_h16x2_d256_shadow4_256",
+                                  "prefill_q4_n8192_h16x2_d256_shadow4_256_sink4_win1024"])
 def test_prefill_workload(oracle_mod, name):
     w = BY_NAME[name]
     q, k, v = prefill_inputs(w.n, w.n_q_heads, w.n_kv_heads, w.head_dim, w.seed)

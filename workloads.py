@@ -61,6 +61,9 @@ WORKLOADS = [
              "f16", nslots=32, split_keys=256),
     Workload("decode_fp8_32slots_L32768_h16x2_d256_sink4", 8, "decode", 32768, 16, 2, 256, 4, 0,
              "fp8_e4m3", nslots=32, split_keys=256),
+    # the windowed prefill over a Q4_0 cache with fp16 shadows (4 sinks, 256-row ring)
+    Workload("prefill_q4_n8192_h16x2_d256_shadow4_256_sink4_win1024", 9, "prefill", 8192, 16, 2,
+             256, 4, 1024, "q4_0", shadow_sink=4, shadow_win=256),
 ]
 
 FMT_CODES = {"f32": 0, "q4_0": 1, "f16": 2, "fp8_e4m3": 3}  # include/fa.h FA_KV_*
