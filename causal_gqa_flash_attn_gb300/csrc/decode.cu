@@ -953,15 +953,23 @@ __global__ void __launch_bounds__(2 * kPairs * 32, FA_Q4_MIN_BLOCKS)
     q4_body<HD>(P, dsmem, e, g, u, p, k_lo, k_hi);
 }
 
-// One warp per (slot, q head): ascending merge of the entries.
+// One warp per (slot, q head). The lanes take the entries 32 at a time to
+// find the common reference M = max m_e and every entry's weight
+// w_e = exp(m_e - M); then the warp accumulates sum w_e acc_e over the
+// entries in ascending order (lanes split head_dim), with the loads of
+// several entries in flight, and out = sum w_e acc_e / sum w_e l_e. An empty
+// entry (m = -inf) has weight 0 and its acc, which was never written, is
+// read but not used.
+constexpr int kCombineWarps = 2;
+
 template <int HD>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(32 * kCombineWarps)
     combine_kernel(const uint32_t *__restrict__ header, const float *__restrict__ ws_m,
                    const float *__restrict__ ws_l, const float *__restrict__ ws_acc,
                    float *__restrict__ out, int nslots, int Hq, int stride, unsigned *err) {
     constexpr int PER = HD / 32;  // dims per lane
     const int lane = threadIdx.x & 31;
-    const long long head = blockIdx.x * 4LL + (threadIdx.x >> 5);
+    const long long head = blockIdx.x * static_cast<long long>(kCombineWarps) + (threadIdx.x >> 5);
     if (head >= static_cast<long long>(nslots) * Hq) return;
     if (header[0] != kDecodeMagic || header[1] != static_cast<uint32_t>(nslots) ||
         header[2] != static_cast<uint32_t>(Hq) || header[3] != static_cast<uint32_t>(HD)) {
@@ -986,23 +994,31 @@ __global__ void __launch_bounds__(128)
     float acc[PER];
 #pragma unroll
     for (int k = 0; k < PER; ++k) acc[k] = 0.0f;
-    float L = 0.0f;
-    for (int i = 0; i < E; ++i) {
-        const float mi = m[i];
-        if (mi == -INFINITY) continue;
-        const float w = ex2((mi - M) * 1.4426950408889634f);
-        L += w * l[i];
-        const float *a = ws_acc + (head * stride + i) * HD + lane * PER;
+    float Lp = 0.0f;  // this lane's entries' w * l
+    const float *a0 = ws_acc + head * stride * HD + lane * PER;
+    for (int i0 = 0; i0 < E; i0 += 32) {
+        const int i = i0 + lane;
+        const float mi = i < E ? m[i] : -INFINITY;
+        const float w = (mi == -INFINITY) ? 0.0f : ex2((mi - M) * 1.4426950408889634f);
+        if (w != 0.0f) Lp += w * l[i];
+        const int cnt = min(32, E - i0);
+#pragma unroll 4
+        for (int k = 0; k < cnt; ++k) {
+            const float wk = __shfl_sync(0xffffffffu, w, k);
+            const float *a = a0 + static_cast<long long>(i0 + k) * HD;
 #pragma unroll
-        for (int k = 0; k < PER; k += 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(a + k);
-            acc[k] += w * v.x;
-            acc[k + 1] += w * v.y;
-            acc[k + 2] += w * v.z;
-            acc[k + 3] += w * v.w;
+            for (int d = 0; d < PER; d += 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(a + d);
+                acc[d] += wk != 0.0f ? wk * v.x : 0.0f;
+                acc[d + 1] += wk != 0.0f ? wk * v.y : 0.0f;
+                acc[d + 2] += wk != 0.0f ? wk * v.z : 0.0f;
+                acc[d + 3] += wk != 0.0f ? wk * v.w : 0.0f;
+            }
         }
     }
-    const float inv = 1.0f / L;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Lp += __shfl_xor_sync(0xffffffffu, Lp, o);
+    const float inv = 1.0f / Lp;
     float *dst = out + head * HD + lane * PER;
 #pragma unroll
     for (int k = 0; k < PER; k += 4)
@@ -1149,19 +1165,19 @@ cudaError_t launch_combine(const void *workspace, float *out, int nslots, int n_
     DecodeWs ws;
     decode_ws_carve(const_cast<void *>(workspace), nslots, n_q_heads, head_dim, stride, &ws);
     const long long heads = static_cast<long long>(nslots) * n_q_heads;
-    const int blocks = static_cast<int>((heads + 3) / 4);
+    const int blocks = static_cast<int>((heads + kCombineWarps - 1) / kCombineWarps);
     switch (head_dim) {
         case 64:
-            combine_kernel<64><<<blocks, 128, 0, stream>>>(ws.header, ws.m, ws.l, ws.acc, out,
-                                                           nslots, n_q_heads, ws.stride, err);
+            combine_kernel<64><<<blocks, 32 * kCombineWarps, 0, stream>>>(
+                ws.header, ws.m, ws.l, ws.acc, out, nslots, n_q_heads, ws.stride, err);
             break;
         case 128:
-            combine_kernel<128><<<blocks, 128, 0, stream>>>(ws.header, ws.m, ws.l, ws.acc, out,
-                                                            nslots, n_q_heads, ws.stride, err);
+            combine_kernel<128><<<blocks, 32 * kCombineWarps, 0, stream>>>(
+                ws.header, ws.m, ws.l, ws.acc, out, nslots, n_q_heads, ws.stride, err);
             break;
         case 256:
-            combine_kernel<256><<<blocks, 128, 0, stream>>>(ws.header, ws.m, ws.l, ws.acc, out,
-                                                            nslots, n_q_heads, ws.stride, err);
+            combine_kernel<256><<<blocks, 32 * kCombineWarps, 0, stream>>>(
+                ws.header, ws.m, ws.l, ws.acc, out, nslots, n_q_heads, ws.stride, err);
             break;
         default: return cudaErrorInvalidValue;
     }

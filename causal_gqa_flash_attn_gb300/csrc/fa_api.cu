@@ -20,11 +20,17 @@ constexpr int kMaxDevices = 64;
 
 cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;  // fa_set_kernel_events
 
+// External records, so that a call captured in a CUDA graph records the
+// events on every replay (a plain record under capture only orders work).
 cudaError_t record_start(cudaStream_t s) {
-    return (g_ev_start && g_ev_stop) ? cudaEventRecord(g_ev_start, s) : cudaSuccess;
+    return (g_ev_start && g_ev_stop)
+               ? cudaEventRecordWithFlags(g_ev_start, s, cudaEventRecordExternal)
+               : cudaSuccess;
 }
 cudaError_t record_stop(cudaStream_t s) {
-    return (g_ev_start && g_ev_stop) ? cudaEventRecord(g_ev_stop, s) : cudaSuccess;
+    return (g_ev_start && g_ev_stop)
+               ? cudaEventRecordWithFlags(g_ev_stop, s, cudaEventRecordExternal)
+               : cudaSuccess;
 }
 
 struct DeviceInfo {

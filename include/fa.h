@@ -349,9 +349,10 @@ fa_status fa_decode_noalloc(const float *q, const void *k_planes, const void *v_
  * created by the caller), every later fa_prefill records `start` on its
  * stream immediately before its tensor-core kernel and `stop` immediately
  * after it, and every fa_decode does the same around its split kernel, so
- * cudaEventElapsedTime(start, stop) is that one kernel's duration. Pass
- * NULL, NULL to stop. Process-wide setting, not thread-safe; never needed for
- * correctness. */
+ * cudaEventElapsedTime(start, stop) is that one kernel's duration. A call
+ * captured in a CUDA graph records them as external event nodes, so every
+ * replay records them. Pass NULL, NULL to stop. Process-wide setting, not
+ * thread-safe; never needed for correctness. */
 fa_status fa_set_kernel_events(void *start, void *stop);
 
 /* ------------------------------------------------------------------- status */
