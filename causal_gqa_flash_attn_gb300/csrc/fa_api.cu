@@ -20,17 +20,22 @@ constexpr int kMaxDevices = 64;
 
 cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;  // fa_set_kernel_events
 
-// External records, so that a call captured in a CUDA graph records the
-// events on every replay (a plain record under capture only orders work).
+// Under stream capture the records are external event nodes, so that every
+// replay of the graph records them (a plain record under capture only orders
+// work); outside capture they are plain records.
+cudaError_t record_event(cudaEvent_t ev, cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return e;
+    return cs == cudaStreamCaptureStatusActive
+               ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal)
+               : cudaEventRecord(ev, s);
+}
 cudaError_t record_start(cudaStream_t s) {
-    return (g_ev_start && g_ev_stop)
-               ? cudaEventRecordWithFlags(g_ev_start, s, cudaEventRecordExternal)
-               : cudaSuccess;
+    return (g_ev_start && g_ev_stop) ? record_event(g_ev_start, s) : cudaSuccess;
 }
 cudaError_t record_stop(cudaStream_t s) {
-    return (g_ev_start && g_ev_stop)
-               ? cudaEventRecordWithFlags(g_ev_stop, s, cudaEventRecordExternal)
-               : cudaSuccess;
+    return (g_ev_start && g_ev_stop) ? record_event(g_ev_stop, s) : cudaSuccess;
 }
 
 struct DeviceInfo {
