@@ -10,9 +10,10 @@
 // bound by HBM if it keeps enough bytes in flight and reads shared memory
 // without bank conflicts. Design:
 //  * persistent: one block per SM, every warp an independent worker with a
-//    private ring of NS stages; a stage holds a 16-key K tile and V tile,
-//    each as 128-byte-wide boxes loaded by TMA with the 128-byte swizzle, so
-//    ldmatrix reads them conflict-free;
+//    private ring of NS stages; a stage holds a K tile and a V tile of TK
+//    keys (16 for fp16, 32 for fp8, processed as 16-key MMA slices), each as
+//    128-byte-wide boxes loaded by TMA with the 128-byte swizzle, so ldmatrix
+//    reads them conflict-free;
 //  * stream-K work split: the visible 16-key tiles of all (slot, kv head)
 //    pairs, in order, are cut into equal runs, one per warp; a warp writes one
 //    partial per (slot, kv head) piece it covers, as entry (warp - first warp
@@ -37,27 +38,40 @@
 namespace fa {
 namespace {
 
-constexpr int kBoxRows = 16;                // keys per tile
-constexpr int kBoxBytes = kBoxRows * 128;   // one box: 16 rows x 128 bytes
-constexpr float kRescaleDense = 8.0f;       // lazy-rescale threshold (log2 units)
+constexpr float kRescaleDense = 8.0f;  // lazy-rescale threshold (log2 units)
 
-// Warps per block for 16-KB stages (fp16 at head_dim 256) and for smaller ones.
+// Warps per block: fp16 with 16-KB stages (head_dim 256), fp16 with smaller
+// stages, and fp8.
 #ifndef FA_DENSE_NW_BIG
 #define FA_DENSE_NW_BIG 3
 #endif
 #ifndef FA_DENSE_NW_SMALL
 #define FA_DENSE_NW_SMALL 8
 #endif
+#ifndef FA_DENSE_NW_FP8
+#define FA_DENSE_NW_FP8 6
+#endif
+// Keys per tile of the fp8 kernel (16 or 32; fp16 uses 16): a longer tile
+// spreads each tile's fixed work (waits, copies, masks, the softmax step)
+// over more bytes.
+#ifndef FA_DENSE_TK_FP8
+#define FA_DENSE_TK_FP8 32
+#endif
 
 template <int HD, int FMT>
 struct DenseCfg {
     static constexpr int EB = FMT == kFmtF16 ? 2 : 1;  // bytes per element
+    static constexpr int TK = FMT == kFmtF16 ? 16 : FA_DENSE_TK_FP8;  // keys per tile
+    static constexpr int NSUB = TK / 16;               // 16-key MMA slices of a tile
+    static constexpr int BOXB = TK * 128;              // one box: TK rows x 128 bytes
     static constexpr int NBX = HD * EB / 128;          // boxes per K (or V) tile
-    static constexpr int TILE = NBX * kBoxBytes;       // K (or V) bytes of a tile
+    static constexpr int TILE = NBX * BOXB;            // K (or V) bytes of a tile
     static constexpr int STAGE = 2 * TILE;
     // warps per block: more stages per warp keep more bytes in flight, more
     // warps cover the fp8 conversions
-    static constexpr int NW = STAGE >= 16384 ? FA_DENSE_NW_BIG : FA_DENSE_NW_SMALL;
+    static constexpr int NW = FMT == kFmtFp8      ? FA_DENSE_NW_FP8
+                              : STAGE >= 16384 ? FA_DENSE_NW_BIG
+                                               : FA_DENSE_NW_SMALL;
     static constexpr int NS0 = 196608 / (NW * STAGE);
     static constexpr int NS = NS0 > 8 ? 8 : NS0;       // ring stages per warp
     static constexpr int MT = HD / 16;
@@ -65,7 +79,7 @@ struct DenseCfg {
     static constexpr int BAR_OFF = NW * WARP_BYTES;
     static constexpr int ABORT_OFF = BAR_OFF + NW * NS * 8;
     static constexpr int SMEM = ABORT_OFF + 16 + 1024;  // + slack to align the base to 1 KB
-    static_assert(NBX >= 1 && NS >= 2, "tile geometry");
+    static_assert(NBX >= 1 && NS >= 2 && (TK == 16 || TK == 32), "tile geometry");
 };
 
 struct DenseParams {
@@ -80,21 +94,23 @@ struct DenseParams {
     unsigned *err;
 };
 
-// The visible 16-key tiles of the query at p (ascending): tiles 0 .. st-1
-// hold the sinks; tiles wt .. p/16 the window. With win <= 0 all tiles up to
-// p/16 (st covers them). nt = 0 marks a position out of range.
+// The visible TK-key tiles of the query at p (ascending): tiles 0 .. st-1
+// hold the sinks; tiles wt .. p/TK the window. With win <= 0 all tiles up to
+// p/TK (st covers them). nt = 0 marks a position out of range.
 struct SlotTiles {
     int nt, st, wt, p;
 };
 
+template <int TK>
 __device__ __forceinline__ SlotTiles slot_tiles(const DenseParams &P, int u) {
+    constexpr int SH = TK == 32 ? 5 : 4;
     SlotTiles s;
     s.p = __ldg(P.pos + u);
     s.nt = 0;
     s.st = 0;
     s.wt = 0;
     if (s.p < 0 || s.p >= P.max_seq) return s;
-    const int last = s.p >> 4;
+    const int last = s.p >> SH;
     if (P.win <= 0) {
         s.st = last + 1;
         s.wt = last + 1;
@@ -102,14 +118,15 @@ __device__ __forceinline__ SlotTiles slot_tiles(const DenseParams &P, int u) {
         return s;
     }
     const int s_end = min(P.sink, s.p + 1);
-    s.st = (s_end + 15) >> 4;
-    s.wt = max(max(0, s.p - P.win + 1) >> 4, s.st);
+    s.st = (s_end + TK - 1) >> SH;
+    s.wt = max(max(0, s.p - P.win + 1) >> SH, s.st);
     s.nt = s.st + max(0, last - s.wt + 1);
     return s;
 }
 
+template <int TK>
 __device__ __forceinline__ int tile_key(const SlotTiles &s, int j) {
-    return j < s.st ? 16 * j : 16 * (s.wt + j - s.st);
+    return j < s.st ? TK * j : TK * (s.wt + j - s.st);
 }
 
 // Position in the flattened tile order (slot, kv head, visible tile).
@@ -119,6 +136,7 @@ struct TileIt {
     SlotTiles s;
 };
 
+template <int TK>
 __device__ __forceinline__ void it_next(const DenseParams &P, TileIt &it) {
     if (++it.j < it.s.nt) return;
     it.j = 0;
@@ -126,7 +144,7 @@ __device__ __forceinline__ void it_next(const DenseParams &P, TileIt &it) {
     if (++it.g < P.Hkv) return;
     it.g = 0;
     while (++it.u < P.nslots) {
-        it.s = slot_tiles(P, it.u);
+        it.s = slot_tiles<TK>(P, it.u);
         if (it.s.nt > 0) return;
     }
 }
@@ -180,7 +198,7 @@ __global__ void __launch_bounds__(DenseCfg<HD, FMT>::NW * 32, 1)
     int maxt = 0;
     for (int u0 = 0; u0 < P.nslots; u0 += 32) {
         const int u = u0 + lane;
-        const int nt = u < P.nslots ? slot_tiles(P, u).nt : 0;
+        const int nt = u < P.nslots ? slot_tiles<C::TK>(P, u).nt : 0;
         long long sum = nt;
         int mx = nt;
 #pragma unroll
@@ -211,7 +229,7 @@ __global__ void __launch_bounds__(DenseCfg<HD, FMT>::NW * 32, 1)
     if (gw == 0) {
         // slots whose position is out of range: all entries empty, and flagged
         for (int u = 0; u < P.nslots; ++u) {
-            if (slot_tiles(P, u).nt > 0) continue;
+            if (slot_tiles<C::TK>(P, u).nt > 0) continue;
             if (lane == 0) flag_error(P.err, FA_ERRBIT_DEVICE);
             for (int i = lane; i < P.Hq * E; i += 32) {
                 const size_t idx = (static_cast<size_t>(u) * P.Hq + i / E) * P.stride + i % E;
@@ -233,7 +251,7 @@ __global__ void __launch_bounds__(DenseCfg<HD, FMT>::NW * 32, 1)
         for (int u0 = 0; u0 < P.nslots && u_hit < 0; u0 += 32) {
             const int u = u0 + lane;
             const long long cnt =
-                u < P.nslots ? static_cast<long long>(slot_tiles(P, u).nt) * P.Hkv : 0;
+                u < P.nslots ? static_cast<long long>(slot_tiles<C::TK>(P, u).nt) * P.Hkv : 0;
             long long inc = cnt;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -251,7 +269,7 @@ __global__ void __launch_bounds__(DenseCfg<HD, FMT>::NW * 32, 1)
         }
         if (u_hit < 0) return;  // unreachable: T_begin < T
         cons.u = u_hit;
-        cons.s = slot_tiles(P, u_hit);
+        cons.s = slot_tiles<C::TK>(P, u_hit);
         const long long local = T_begin - slot_base;
         cons.g = static_cast<int>(local / cons.s.nt);
         cons.j = static_cast<int>(local % cons.s.nt);
@@ -264,18 +282,18 @@ __global__ void __launch_bounds__(DenseCfg<HD, FMT>::NW * 32, 1)
         mbar_arrive_expect_tx(b, C::STAGE);
         uint8_t *dk = ring + stage * C::STAGE;
         uint8_t *dv = dk + C::TILE;
-        const int c0 = tile_key(it.s, it.j);
+        const int c0 = tile_key<C::TK>(it.s, it.j);
 #pragma unroll
         for (int bx = 0; bx < C::NBX; ++bx) {
-            tma_load_4d(dk + bx * kBoxBytes, &kmap, b, bx * (128 / C::EB), c0, it.g, it.u);
-            tma_load_4d(dv + bx * kBoxBytes, &vmap, b, bx * (128 / C::EB), c0, it.g, it.u);
+            tma_load_4d(dk + bx * C::BOXB, &kmap, b, bx * (128 / C::EB), c0, it.g, it.u);
+            tma_load_4d(dv + bx * C::BOXB, &vmap, b, bx * (128 / C::EB), c0, it.g, it.u);
         }
     };
 
     long long Tp = T_begin;
     for (int s = 0; s < C::NS && Tp < T_end; ++s, ++Tp) {
         if (lane == 0) issue(prod, s);
-        it_next(P, prod);
+        it_next<C::TK>(P, prod);
     }
 
     // fragment addressing (row and swizzle phase of this lane)
@@ -338,20 +356,20 @@ __global__ void __launch_bounds__(DenseCfg<HD, FMT>::NW * 32, 1)
             }
             return;
         }
-        const int c0 = tile_key(cons.s, cons.j);
+        const int c0 = tile_key<C::TK>(cons.s, cons.j);
         const int p = cons.s.p;
         uint8_t *kt = ring + stage * C::STAGE;
         uint8_t *vt = kt + C::TILE;
         bool wrote = false;
-        if (c0 + kBoxRows - 1 > p) {
+        if (c0 + C::TK - 1 > p) {
             // rows past the slot's last key hold whatever the plane held:
             // zero them in V so that P = 0 meets finite values
             const int z0 = p - c0 + 1;
-            const int nchunk = (kBoxRows - z0) * 8 * C::NBX;
+            const int nchunk = (C::TK - z0) * 8 * C::NBX;
             for (int i = lane; i < nchunk; i += 32) {
-                const int bx = i / ((kBoxRows - z0) * 8);
-                const int rem = i % ((kBoxRows - z0) * 8);
-                *reinterpret_cast<uint4 *>(vt + bx * kBoxBytes + (z0 + rem / 8) * 128 +
+                const int bx = i / ((C::TK - z0) * 8);
+                const int rem = i % ((C::TK - z0) * 8);
+                *reinterpret_cast<uint4 *>(vt + bx * C::BOXB + (z0 + rem / 8) * 128 +
                                            (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
             }
             wrote = true;
@@ -359,65 +377,77 @@ __global__ void __launch_bounds__(DenseCfg<HD, FMT>::NW * 32, 1)
         }
         const uint32_t kb = smem_u32(kt), vb = smem_u32(vt);
 
-        // S^T = K Q^T: two accumulator chains
-        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-        if (FMT == kFmtF16) {
+        // S^T = K Q^T per 16-key slice of the tile: two accumulator chains each
+        constexpr int NSUB = C::NSUB;
+        float sv[2][2 * NSUB], pv[2][2 * NSUB];
 #pragma unroll
-            for (int kk = 0; kk < MT; ++kk) {
-                uint32_t a[4];
-                ldmatrix_x4(a, kb + (kk >> 2) * kBoxBytes + koff + (((2 * (kk & 3)) ^ kz) << 4));
-                mma_16816((kk & 1) ? s1 : s0, a, qb[kk]);
+        for (int sub = 0; sub < NSUB; ++sub) {
+            const uint32_t kbs = kb + sub * 16 * 128 + koff;  // rows 16 sub .. of every box
+            float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+            if (FMT == kFmtF16) {
+#pragma unroll
+                for (int kk = 0; kk < MT; ++kk) {
+                    uint32_t a[4];
+                    ldmatrix_x4(a, kbs + (kk >> 2) * C::BOXB + (((2 * (kk & 3)) ^ kz) << 4));
+                    mma_16816((kk & 1) ? s1 : s0, a, qb[kk]);
+                }
+            } else {
+#pragma unroll
+                for (int kp = 0; kp < HD / 32; ++kp) {
+                    uint32_t x[4];
+                    ldmatrix_x4(x, kbs + (kp >> 2) * C::BOXB + (((2 * (kp & 3)) ^ kz) << 4));
+                    uint32_t a0[4], a1[4];  // {row r, row r + 8} x {dims 4t..4t+1, 4t+2..4t+3}
+                    e4m3x4_to_h2x2(x[0], a0[0], a0[2]);
+                    e4m3x4_to_h2x2(x[1], a0[1], a0[3]);
+                    e4m3x4_to_h2x2(x[2], a1[0], a1[2]);
+                    e4m3x4_to_h2x2(x[3], a1[1], a1[3]);
+                    mma_16816(s0, a0, qb[2 * kp]);
+                    mma_16816(s1, a1, qb[2 * kp + 1]);
+                }
             }
-        } else {
+            const int keyA = c0 + 16 * sub + r, keyB = keyA + 8;
+            const bool visA = key_visible(p, keyA, P.sink, P.win);
+            const bool visB = key_visible(p, keyB, P.sink, P.win);
 #pragma unroll
-            for (int kp = 0; kp < HD / 32; ++kp) {
-                uint32_t x[4];
-                ldmatrix_x4(x, kb + (kp >> 2) * kBoxBytes + koff + (((2 * (kp & 3)) ^ kz) << 4));
-                uint32_t a0[4], a1[4];  // {row r, row r + 8} x {dims 4t..4t+1, 4t+2..4t+3}
-                e4m3x4_to_h2x2(x[0], a0[0], a0[2]);
-                e4m3x4_to_h2x2(x[1], a0[1], a0[3]);
-                e4m3x4_to_h2x2(x[2], a1[0], a1[2]);
-                e4m3x4_to_h2x2(x[3], a1[1], a1[3]);
-                mma_16816(s0, a0, qb[2 * kp]);
-                mma_16816(s1, a1, qb[2 * kp + 1]);
+            for (int hh = 0; hh < 2; ++hh) {
+                sv[hh][2 * sub] = visA ? s0[hh] + s1[hh] : -INFINITY;
+                sv[hh][2 * sub + 1] = visB ? s0[2 + hh] + s1[2 + hh] : -INFINITY;
             }
         }
-        const int keyA = c0 + r, keyB = c0 + r + 8;
-        const bool visA = key_visible(p, keyA, P.sink, P.win);
-        const bool visB = key_visible(p, keyB, P.sink, P.win);
-        float sv[2][2], pv[2][2];
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            sv[hh][0] = visA ? s0[hh] + s1[hh] : -INFINITY;
-            sv[hh][1] = visB ? s0[2 + hh] + s1[2 + hh] : -INFINITY;
-        }
-        fold_scores<MT, 1, 2>(sv, sl2, kRescaleDense, mu0, mu1, mt0, mt1, ls0, ls1, o, 0, pv);
-        uint32_t pb[2];
-        pb[0] = movmatrix_trans(pack_half2(pv[0][0], pv[1][0]));
-        pb[1] = movmatrix_trans(pack_half2(pv[0][1], pv[1][1]));
+        fold_scores<MT, 1, 2 * NSUB>(sv, sl2, kRescaleDense, mu0, mu1, mt0, mt1, ls0, ls1, o, 0,
+                                     pv);
 
-        // O^T += V^T P^T
-        if (FMT == kFmtF16) {
+        // O^T += V^T P^T per slice
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                uint32_t a[4];
-                ldmatrix_x4_trans(a, vb + (mt >> 2) * kBoxBytes + voff + (((2 * (mt & 3)) ^ vz) << 4));
-                mma_16816(o[mt][0], a, pb);
-            }
-        } else {
+        for (int sub = 0; sub < NSUB; ++sub) {
+            uint32_t pb[2];
+            pb[0] = movmatrix_trans(pack_half2(pv[0][2 * sub], pv[1][2 * sub]));
+            pb[1] = movmatrix_trans(pack_half2(pv[0][2 * sub + 1], pv[1][2 * sub + 1]));
+            const uint32_t vbs = vb + sub * 16 * 128 + voff;
+            if (FMT == kFmtF16) {
 #pragma unroll
-            for (int mp = 0; mp < HD / 32; ++mp) {
-                uint32_t x[4];
-                ldmatrix_x4_trans(x, vb + (mp >> 2) * kBoxBytes + voff + (((2 * (mp & 3)) ^ vz) << 4));
-                const uint32_t y0 = __byte_perm(x[0], 0u, 0x3120), y1 = __byte_perm(x[1], 0u, 0x3120);
-                const uint32_t y2 = __byte_perm(x[2], 0u, 0x3120), y3 = __byte_perm(x[3], 0u, 0x3120);
-                uint32_t a0[4], a1[4];  // {dim 2r, dim 2r + 1} x {keys 2t.., keys 2t+8..}
-                e4m3x4_to_h2x2(y0, a0[0], a0[1]);
-                e4m3x4_to_h2x2(y1, a0[2], a0[3]);
-                e4m3x4_to_h2x2(y2, a1[0], a1[1]);
-                e4m3x4_to_h2x2(y3, a1[2], a1[3]);
-                mma_16816(o[2 * mp][0], a0, pb);
-                mma_16816(o[2 * mp + 1][0], a1, pb);
+                for (int mt = 0; mt < MT; ++mt) {
+                    uint32_t a[4];
+                    ldmatrix_x4_trans(a, vbs + (mt >> 2) * C::BOXB + (((2 * (mt & 3)) ^ vz) << 4));
+                    mma_16816(o[mt][0], a, pb);
+                }
+            } else {
+#pragma unroll
+                for (int mp = 0; mp < HD / 32; ++mp) {
+                    uint32_t x[4];
+                    ldmatrix_x4_trans(x, vbs + (mp >> 2) * C::BOXB + (((2 * (mp & 3)) ^ vz) << 4));
+                    const uint32_t y0 = __byte_perm(x[0], 0u, 0x3120);
+                    const uint32_t y1 = __byte_perm(x[1], 0u, 0x3120);
+                    const uint32_t y2 = __byte_perm(x[2], 0u, 0x3120);
+                    const uint32_t y3 = __byte_perm(x[3], 0u, 0x3120);
+                    uint32_t a0[4], a1[4];  // {dim 2r, dim 2r + 1} x {keys 2t.., keys 2t+8..}
+                    e4m3x4_to_h2x2(y0, a0[0], a0[1]);
+                    e4m3x4_to_h2x2(y1, a0[2], a0[3]);
+                    e4m3x4_to_h2x2(y2, a1[0], a1[1]);
+                    e4m3x4_to_h2x2(y3, a1[2], a1[3]);
+                    mma_16816(o[2 * mp][0], a0, pb);
+                    mma_16816(o[2 * mp + 1][0], a1, pb);
+                }
             }
         }
 
@@ -472,10 +502,10 @@ __global__ void __launch_bounds__(DenseCfg<HD, FMT>::NW * 32, 1)
         __syncwarp();
         if (Tp < T_end) {
             if (lane == 0) issue(prod, stage);
-            it_next(P, prod);
+            it_next<C::TK>(P, prod);
             ++Tp;
         }
-        it_next(P, cons);
+        it_next<C::TK>(P, cons);
     }
 }
 
@@ -488,7 +518,7 @@ cudaError_t launch_dense_hd(const DecodeArgs &a, const DecodeWs &ws, unsigned *e
     const uint64_t dims[4] = {static_cast<uint64_t>(HD), static_cast<uint64_t>(a.g.max_seq),
                               static_cast<uint64_t>(a.n_kv_heads), static_cast<uint64_t>(a.nslots)};
     const uint64_t strides[3] = {a.g.row_bytes, a.g.row_bytes * a.g.max_seq, a.g.bytes};
-    const uint32_t box[4] = {static_cast<uint32_t>(128 / C::EB), static_cast<uint32_t>(kBoxRows), 1,
+    const uint32_t box[4] = {static_cast<uint32_t>(128 / C::EB), static_cast<uint32_t>(C::TK), 1,
                              1};
     CUtensorMap km, vm;
     if (!encode_tiled(&km, dt, 4, a.k_planes + a.g.body_off, dims, strides, box) ||

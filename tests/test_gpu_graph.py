@@ -96,3 +96,46 @@ def test_decode_step_graph_replay(oracle_mod, kv_fmt, shadow):
                                      sink=sink, win=win, shadow_sink=ss, shadow_win=sw)
             assert_close(got[u], want, f"{kv_fmt} step {t} slot {u}")
     assert pos.cpu().tolist() == [L + steps for L in lens0]
+
+
+def test_kernel_events_eager_and_in_a_captured_graph():
+    """fa_set_kernel_events brackets the split-decode kernel: a plain call
+    records the events, and a call captured in a CUDA graph records them on
+    every replay."""
+    m = fa()
+    nslots, hq, hkv, hd, max_seq = 2, 16, 2, 128, 512
+    code = fmt_code("f16")
+    kp = m.alloc_planes(nslots, code, hkv, max_seq, hd)
+    vp = m.alloc_planes(nslots, code, hkv, max_seq, hd)
+    k = torch.randn(nslots, 300, hkv, hd, device="cuda")
+    m.kv_append(k, k, kp, vp, torch.zeros(nslots, dtype=torch.int32, device="cuda"),
+                n_kv_heads=hkv, head_dim=hd, max_seq=max_seq, kv_fmt=code)
+    q = torch.randn(nslots, hq, hd, device="cuda")
+    pos = torch.full((nslots,), 299, dtype=torch.int32, device="cuda")
+    max_splits = 2
+    ws = torch.empty(m.decode_workspace_bytes(nslots, hq, hd, max_splits), dtype=torch.uint8,
+                     device="cuda")
+    kw = dict(n_q_heads=hq, n_kv_heads=hkv, head_dim=hd, max_seq=max_seq, sink=0, win=0,
+              kv_fmt=code, split_keys=256, max_splits=max_splits, workspace=ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for e in (e0, e1, g0, g1):  # create the CUDA events
+        e.record()
+    torch.cuda.synchronize()
+    try:
+        m.set_kernel_events(e0, e1)
+        m.decode(q, kp, vp, pos, **kw)
+        torch.cuda.synchronize()
+        assert e0.elapsed_time(e1) > 0.0
+        m.set_kernel_events(g0, g1)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            m.decode(q, kp, vp, pos, **kw)
+        m.set_kernel_events(None, None)
+        for _ in range(2):
+            graph.replay()
+            torch.cuda.synchronize()
+            assert g0.elapsed_time(g1) > 0.0
+    finally:
+        m.set_kernel_events(None, None)
+    assert m.get_device_error() == m.OK
