@@ -329,3 +329,32 @@ def test_kv_init_zeroes_planes_and_sets_the_fp8_scale(fmt):
             assert host[u, so:so + 4].view(np.float32)[0] == 1.0
             host[u, so:so + 4] = 0
         assert not host[u].any(), (fmt, u)
+
+
+@pytest.mark.parametrize("fmt", ["f16", "fp8_e4m3"])
+def test_decode_dense_with_two_entries(oracle_mod, fmt):
+    """max_splits = 1 leaves the streaming kernel two entries per head: every
+    (slot, kv head) must then be covered by at most two pieces of the
+    warps' runs, whatever the slot lengths."""
+    lens, hq, hkv, hd, max_seq = (2000, 17, 1, 1999), 8, 2, 128, 2048
+    qs, kk, vv = [], [], []
+    for u in range(len(lens)):
+        qu, ku, vu = decode_slot_inputs(max(lens), hq, hkv, hd, seed=7070, slot=u)
+        qs.append(qu)
+        kk.append(ku)
+        vv.append(vu)
+    m = fa()
+    code = fmt_code(fmt)
+    kp = m.alloc_planes(len(lens), code, hkv, max_seq, hd)
+    vp = m.alloc_planes(len(lens), code, hkv, max_seq, hd)
+    pb = m.kv_plane_bytes(code, hkv, max_seq, hd)
+    for u, L in enumerate(lens):
+        m.kv_append(torch.from_numpy(kk[u][None, :L]).cuda(), torch.from_numpy(vv[u][None, :L]).cuda(),
+                    kp[u * pb:(u + 1) * pb], vp[u * pb:(u + 1) * pb],
+                    torch.zeros(1, dtype=torch.int32, device="cuda"), n_kv_heads=hkv,
+                    head_dim=hd, max_seq=max_seq, kv_fmt=code)
+    got = run_decode(np.stack(qs), kp, vp, np.array(lens, np.int32) - 1, hkv=hkv, hd=hd,
+                     max_seq=max_seq, sink=0, win=0, kv_fmt=fmt, split_keys=4096, max_splits=1)
+    for u, L in enumerate(lens):
+        want = oracle_mod.decode(qs[u], L - 1, kk[u], vv[u], kv_fmt=fmt, sink=0, win=0)
+        assert_close(got[u], want, f"{fmt} slot {u}")
