@@ -44,6 +44,7 @@ SIGNATURES = {
                             _P, _P]),
     "fa_merge_attn_states": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "fa_prefill_chunk_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "fa_prefill_chunk_workspace_bytes_for": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "fa_prefill_chunk": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P,
                               _SZ, _P, _P]),
     "fa_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
@@ -183,7 +184,13 @@ def kv_append(k_new, v_new, k_planes, v_planes, pos0, *, n_kv_heads: int, head_d
 
 # ----------------------------------------------------------------- prefill
 
-def prefill_workspace_bytes(n: int, n_q_heads: int, n_kv_heads: int, head_dim: int) -> int:
+def prefill_workspace_bytes(n: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
+                            kv_fmt: int | None = None, shadow_win: int = 0) -> int:
+    """Workspace of fa_prefill; pass kv_fmt and shadow_win to size a Q4_0 cache
+    whose shadow window is neither 0 nor the whole ring."""
+    if kv_fmt is not None:
+        return prefill_chunk_workspace_bytes(0, n, n_q_heads, n_kv_heads, head_dim, kv_fmt,
+                                             shadow_win)
     return int(lib().fa_prefill_workspace_bytes(n, n_q_heads, n_kv_heads, head_dim))
 
 
@@ -213,7 +220,11 @@ def prefill(q, k, v, out, n: int, n_q_heads: int, n_kv_heads: int, head_dim: int
 
 
 def prefill_chunk_workspace_bytes(pos0: int, n: int, n_q_heads: int, n_kv_heads: int,
-                                  head_dim: int) -> int:
+                                  head_dim: int, kv_fmt: int | None = None,
+                                  shadow_win: int = 0) -> int:
+    if kv_fmt is not None:
+        return int(lib().fa_prefill_chunk_workspace_bytes_for(pos0, n, n_q_heads, n_kv_heads,
+                                                              head_dim, kv_fmt, shadow_win))
     return int(lib().fa_prefill_chunk_workspace_bytes(pos0, n, n_q_heads, n_kv_heads, head_dim))
 
 

@@ -98,21 +98,116 @@ fa_status check_shadow(int kv_fmt, int shadow_sink, int shadow_win) {
     return FA_OK;
 }
 
-// Prefill workspace: a 256-byte header holding the kernel's work counter,
-// then the fp16 staging of Q [n][Hq][hd], K and V [Hkv][n][hd].
+// Prefill workspace: a 256-byte header holding the kernel's work counters,
+// then the fp16 staging of Q [n][Hq][hd], K and V [Hkv][n][hd]. A split
+// prefill (Q4_0 with a shadow window narrower than the ring) adds a second
+// K and V staging (the fp16 ring values) and the two parts' outputs
+// [n][Hq][hd] and lses [Hq][n], fp32.
 struct PrefillWs {
-    size_t ctr_off, q_off, k_off, v_off, bytes;
+    size_t ctr_off, ctr2_off, q_off, k_off, v_off, bytes;
+    size_t k2_off, v2_off, o1_off, o2_off, l1_off, l2_off;  // split only
 };
 // n query rows over nk key rows
-PrefillWs prefill_ws(int n, int nk, int hq, int hkv, int hd) {
+PrefillWs prefill_ws(int n, int nk, int hq, int hkv, int hd, bool split = false) {
     PrefillWs w;
     w.ctr_off = 0;
+    w.ctr2_off = 128;
     w.q_off = 256;
     w.k_off = w.q_off + up256(static_cast<size_t>(n) * hq * hd * 2);
     const size_t kv = up256(static_cast<size_t>(hkv) * nk * hd * 2);
     w.v_off = w.k_off + kv;
     w.bytes = w.v_off + kv;
+    w.k2_off = w.v2_off = w.o1_off = w.o2_off = w.l1_off = w.l2_off = 0;
+    if (split) {
+        const size_t ob = up256(static_cast<size_t>(n) * hq * hd * 4);
+        const size_t lb = up256(static_cast<size_t>(hq) * n * 4);
+        w.k2_off = w.bytes;
+        w.v2_off = w.k2_off + kv;
+        w.o1_off = w.v2_off + kv;
+        w.o2_off = w.o1_off + ob;
+        w.l1_off = w.o2_off + ob;
+        w.l2_off = w.l1_off + lb;
+        w.bytes = w.l2_off + lb;
+    }
     return w;
+}
+
+// A Q4_0 cache whose fp16 window is neither empty nor the whole ring: which
+// copy of a key a query reads depends on the query, so the prefill runs as
+// two parts merged by their log-sum-exps.
+bool split_prefill(int kv_fmt, int shadow_win) {
+    return kv_fmt == FA_KV_Q4_0 && shadow_win != 0 && shadow_win != FA_Q4_RING_ROWS;
+}
+
+}  // namespace
+
+namespace fa {
+bool plane_geom(int fmt, int n_kv, int max_seq, int hd, PlaneGeom *g);
+}
+
+namespace {
+
+// The split prefill after the Q staging and the far K/V staging: stage the
+// fp16 ring values, run the far part and the near part (each with its lse)
+// and merge them into out (and lse when requested).
+fa_status prefill_split(const float *q, const void *k, const void *v, float *out, float *lse,
+                        int pos0, int n, int hq, int hkv, int hd, int sink, int win,
+                        const fa::PlaneGeom &g, int shadow_sink, int shadow_win, uint8_t *ws,
+                        const PrefillWs &w, __half *qh, __half *kh, __half *vh,
+                        uint8_t *tile_map, unsigned *err, cudaStream_t s) {
+    (void)q;
+    const int nk = pos0 + n;
+    __half *kh2 = reinterpret_cast<__half *>(ws + w.k2_off);
+    __half *vh2 = reinterpret_cast<__half *>(ws + w.v2_off);
+    float *o1 = reinterpret_cast<float *>(ws + w.o1_off);
+    float *o2 = reinterpret_cast<float *>(ws + w.o2_off);
+    float *l1 = reinterpret_cast<float *>(ws + w.l1_off);
+    float *l2 = reinterpret_cast<float *>(ws + w.l2_off);
+    unsigned *ctr2 = reinterpret_cast<unsigned *>(ws + w.ctr2_off);
+    // the ring holds the 256 newest rows (ring liveness): near keys start at F
+    const int F = nk - FA_Q4_RING_ROWS > shadow_sink ? nk - FA_Q4_RING_ROWS : shadow_sink;
+    cudaError_t e = fa::launch_stage_kv(static_cast<const uint8_t *>(k), kh2, nk, g, shadow_sink,
+                                        FA_Q4_RING_ROWS, s);
+    if (e == cudaSuccess)
+        e = fa::launch_stage_kv(static_cast<const uint8_t *>(v), vh2, nk, g, shadow_sink,
+                                FA_Q4_RING_ROWS, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ctr2, 0, sizeof(unsigned), s);
+    fa::PrefillArgs a;
+    a.qh = qh;
+    a.kv_rows = nk;
+    a.pos0 = pos0;
+    a.n = n;
+    a.n_q_heads = hq;
+    a.n_kv_heads = hkv;
+    a.head_dim = hd;
+    a.sink = sink;
+    a.win = win;
+    a.scale = 1.0f / sqrtf(static_cast<float>(hd));
+    a.split_f = F;
+    a.split_w = shadow_win;
+    // far part (the work counter was zeroed by the Q staging)
+    a.kh = kh;
+    a.vh = vh;
+    a.out = o1;
+    a.lse = l1;
+    a.tile_map = tile_map;
+    a.work_counter = reinterpret_cast<unsigned *>(ws + w.ctr_off);
+    a.split = 1;
+    if (e == cudaSuccess) e = record_start(s);
+    if (e == cudaSuccess) e = fa::launch_prefill_tc(a, err, s);
+    // near part
+    a.kh = kh2;
+    a.vh = vh2;
+    a.out = o2;
+    a.lse = l2;
+    a.tile_map = nullptr;
+    a.work_counter = ctr2;
+    a.split = 2;
+    if (e == cudaSuccess) e = fa::launch_prefill_tc(a, err, s);
+    if (e == cudaSuccess) e = record_stop(s);
+    if (e == cudaSuccess)
+        e = fa::launch_merge_attn_states(out, lse, o1, l1, o2, l2, n, hq, hd, -1, s);
+    return from_cuda(e);
 }
 
 }  // namespace
@@ -273,6 +368,14 @@ size_t fa_prefill_chunk_workspace_bytes(int pos0, int n, int n_q_heads, int n_kv
     return prefill_ws(n, pos0 + n, n_q_heads, n_kv_heads, head_dim).bytes;
 }
 
+size_t fa_prefill_chunk_workspace_bytes_for(int pos0, int n, int n_q_heads, int n_kv_heads,
+                                            int head_dim, int kv_fmt, int shadow_win) {
+    if (pos0 < 0 || n < 0 || n_q_heads < 1 || n_kv_heads < 1 || head_dim < 1) return 0;
+    return prefill_ws(n, pos0 + n, n_q_heads, n_kv_heads, head_dim,
+                      split_prefill(kv_fmt, shadow_win))
+        .bytes;
+}
+
 fa_status fa_prefill_tile_shape(int head_dim, int *bq, int *bk) {
     if (!supported_hd(head_dim)) return FA_ERR_UNSUPPORTED;
     if (bq) *bq = fa::kPrefillBQ;
@@ -310,15 +413,14 @@ fa_status fa_prefill_chunk(const float *q, const void *k, const void *v, float *
         return FA_ERR_INVALID;
     st = check_shadow(kv_fmt, shadow_sink, shadow_win);
     if (st != FA_OK) return st;
-    if (kv_fmt == FA_KV_Q4_0 && shadow_win != 0 && shadow_win != FA_Q4_RING_ROWS)
-        return FA_ERR_UNSUPPORTED;
+    const bool split = split_prefill(kv_fmt, shadow_win);
     if (n == 0) return FA_OK;
     if (!q || !k || !v || !out || !workspace) return FA_ERR_INVALID;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
         !aligned16(workspace) || (reinterpret_cast<uintptr_t>(lse) & 3u))
         return FA_ERR_INVALID;
     const int nk = pos0 + n;  // key rows 0 .. pos0+n-1
-    const PrefillWs w = prefill_ws(n, nk, n_q_heads, n_kv_heads, head_dim);
+    const PrefillWs w = prefill_ws(n, nk, n_q_heads, n_kv_heads, head_dim, split);
     if (workspace_bytes < w.bytes) return FA_ERR_WORKSPACE;
     fa::PlaneGeom g;
     if (!fa::plane_geom(kv_fmt, n_kv_heads, max_seq, head_dim, &g)) return FA_ERR_INVALID;
@@ -339,14 +441,20 @@ fa_status fa_prefill_chunk(const float *q, const void *k, const void *v, float *
         kh = reinterpret_cast<__half *>(static_cast<uint8_t *>(const_cast<void *>(k)) + g.body_off);
         vh = reinterpret_cast<__half *>(static_cast<uint8_t *>(const_cast<void *>(v)) + g.body_off);
     } else {
+        // the split's far part reads sinks and Q4_0 rows (no ring); the other
+        // paths read what the shadow geometry gives every query
+        const int sw_stage = split ? 0 : shadow_win;
         if (e == cudaSuccess)
             e = fa::launch_stage_kv(static_cast<const uint8_t *>(k), kh, nk, g, shadow_sink,
-                                    shadow_win, s);
+                                    sw_stage, s);
         if (e == cudaSuccess)
             e = fa::launch_stage_kv(static_cast<const uint8_t *>(v), vh, nk, g, shadow_sink,
-                                    shadow_win, s);
+                                    sw_stage, s);
     }
     if (e != cudaSuccess) return FA_ERR_CUDA;
+    if (split) return prefill_split(q, k, v, out, lse, pos0, n, n_q_heads, n_kv_heads, head_dim,
+                                    sink, win, g, shadow_sink, shadow_win, ws, w, qh, kh, vh,
+                                    tile_map, d->err, s);
     fa::PrefillArgs a;
     a.qh = qh;
     a.kh = kh;

@@ -69,6 +69,10 @@ struct PrefillArgs {
     int pos0;  // position of query row 0; keys are the cache rows 0 .. pos0+n-1
     int n, n_q_heads, n_kv_heads, head_dim, sink, win;
     float scale;
+    // 0: every visible key; 1 / 2: the far / near keys of a Q4_0 cache whose
+    // fp16 window split_w is narrower than the ring (near: key >= split_f and
+    // key > p - split_w); 1 and 2 need lse
+    int split = 0, split_f = 0, split_w = 0;
 };
 constexpr int kPrefillBQ = 128;
 constexpr int kPrefillBK = 128;

@@ -111,6 +111,14 @@ __device__ __forceinline__ bool tile_full(int kt, int p0, int p1, int sink, int 
     return j0 >= p1 - win + 1;
 }
 
+// The tiles a unit visits: the attended set's plan, or for the near part of a
+// split the tiles of the window [p - split_w + 1, p].
+template <int SPLIT>
+__device__ __forceinline__ TilePlan unit_plan(int p0, int p1, int sink, int win, int split_w,
+                                              int bk) {
+    return SPLIT == 2 ? tile_plan(p0, p1, 0, split_w, bk) : tile_plan(p0, p1, sink, win, bk);
+}
+
 // Wait ignoring the abort flag (still bounded): used to drain copies and MMAs
 // already in flight before the block releases its TMEM and exits.
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
@@ -131,14 +139,22 @@ struct Unit {
 
 // LSE: also write each row's log-sum-exp (a separate instantiation, so that
 // the plain prefill keeps its own register allocation).
-template <int HD, bool LSE>
+// SPLIT (Q4_0 caches whose fp16 window is narrower than the ring): the keys a
+// query p sees split into the "near" keys s >= F with s > p - shadow_win,
+// read from the fp16 ring, and the rest ("far"), read from the sinks or the
+// Q4_0 rows. SPLIT = 1 attends the far keys only (over the usual tile plan),
+// SPLIT = 2 the near keys only (over the tiles of the window [p - sw + 1, p]);
+// the two results are merged by their log-sum-exps. A row with no key in its
+// part gets O = 0 and lse = -inf.
+template <int HD, bool LSE, int SPLIT>
 __global__ void __launch_bounds__(256, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_o, uint8_t *__restrict__ tile_map,
                       unsigned *__restrict__ work_counter, float *__restrict__ lse, int pos0,
-                      int n, int Hq, int Hkv, int sink, int win, float sl2, unsigned *err) {
+                      int n, int Hq, int Hkv, int sink, int win, float sl2, unsigned *err,
+                      int split_f, int split_w) {
     using C = Cfg<HD>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -229,7 +245,7 @@ __global__ void __launch_bounds__(256, 1)
                 const int q0 = u.qt * C::BQ;
                 const int p0 = pos0 + q0, p1 = pos0 + min(n, q0 + C::BQ) - 1;
                 const int g = u.h / (Hq / Hkv);
-                const TilePlan plan = tile_plan(p0, p1, sink, win, C::BK);
+                const TilePlan plan = unit_plan<SPLIT>(p0, p1, sink, win, split_w, C::BK);
                 // the Q buffer is free once the previous unit's last QK^T completed
                 if (j > 0 && !mbar_wait(&bars->q_empty, (j - 1) & 1, abort, err)) {
                     ok = false;
@@ -333,7 +349,7 @@ __global__ void __launch_bounds__(256, 1)
             for (int j = 0; ok && next_unit(j, &u, true); ++j) {
                 const int q0 = u.qt * C::BQ;
                 const int p0 = pos0 + q0, p1 = pos0 + min(n, q0 + C::BQ) - 1;
-                const int count = tile_plan(p0, p1, sink, win, C::BK).count;
+                const int count = unit_plan<SPLIT>(p0, p1, sink, win, split_w, C::BK).count;
                 ok = mbar_wait(&bars->q_full, j & 1, abort, err);
                 if (!ok) break;
                 tc_fence_after();
@@ -377,7 +393,7 @@ __global__ void __launch_bounds__(256, 1)
             const int q0 = u.qt * C::BQ;  // query rows q0.. at positions p0..
             const int p0 = pos0 + q0, p1 = pos0 + min(n, q0 + C::BQ) - 1;
             const int p = p0 + r;
-            const TilePlan plan = tile_plan(p0, p1, sink, win, C::BK);
+            const TilePlan plan = unit_plan<SPLIT>(p0, p1, sink, win, split_w, C::BK);
             float m_used = -INFINITY;  // exp2-domain reference shared by O and l
             float l = 0.0f;
             for (int i = 0; i < plan.count; ++i) {
@@ -398,7 +414,9 @@ __global__ void __launch_bounds__(256, 1)
                 const int kt = plan.kt(i);
                 const int j0 = kt * C::BK;
                 float mx = -INFINITY;
-                if (tile_full(kt, p0, p1, sink, win, C::BK)) {
+                if (tile_full(kt, p0, p1, sink, win, C::BK) &&
+                    (SPLIT == 0 || (SPLIT == 1 && (j0 + C::BK - 1 < split_f ||
+                                                   j0 + C::BK - 1 <= p0 - split_w)))) {
 #pragma unroll
                     for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
                 } else {
@@ -406,9 +424,12 @@ __global__ void __launch_bounds__(256, 1)
                     const int hi = p - j0;
                     const int lo = win > 0 ? p - win + 1 - j0 : -1;
                     const int sk = win > 0 ? sink - j0 : -1;
+                    const int fk = split_f - j0, hs = p - split_w - j0;  // near: c >= fk, c > hs
 #pragma unroll
                     for (int c = 0; c < 128; ++c) {
-                        const bool vis = (c <= hi) & ((c >= lo) | (c < sk));
+                        bool vis = (c <= hi) & ((c >= lo) | (c < sk));
+                        if (SPLIT == 1) vis &= (c < fk) | (c <= hs);
+                        if (SPLIT == 2) vis &= (c >= fk) & (c > hs);
                         const float v = vis ? __uint_as_float(s[c]) : -INFINITY;
                         s[c] = __float_as_uint(v);
                         mx = fmaxf(mx, v);
@@ -472,11 +493,12 @@ __global__ void __launch_bounds__(256, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            const float inv = 1.0f / l;
+            // a row with no visible key (possible only in a SPLIT part) has l = 0
+            const float inv = l > 0.0f ? 1.0f / l : 0.0f;
             // log sum_j exp(s_j) = ln 2 * m_used + ln l (l is relative to 2^m_used)
             if (LSE && q0 + r < n)
                 lse[static_cast<size_t>(u.h) * n + q0 + r] =
-                    m_used * 0.69314718055994531f + logf(l);
+                    l > 0.0f ? m_used * 0.69314718055994531f + logf(l) : -INFINITY;
             const int wr = warp & 3;  // rows 32 wr .. 32 wr + 31 of the tile
 #pragma unroll 1
             for (int c = 0; c < HD / 32; ++c) {
@@ -594,7 +616,11 @@ cudaError_t launch_hd(const PrefillArgs &a, unsigned *err, cudaStream_t stream) 
         !encode_3d(&to, a.out, HD, Hq, n, HD * 4, Hq * HD * 4, 32, 1, 32,
                    CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
         return cudaErrorInvalidValue;
-    auto kernel = a.lse ? prefill_tc_kernel<HD, true> : prefill_tc_kernel<HD, false>;
+    if (a.split && !a.lse) return cudaErrorInvalidValue;
+    auto kernel = a.split == 1   ? prefill_tc_kernel<HD, true, 1>
+                  : a.split == 2 ? prefill_tc_kernel<HD, true, 2>
+                  : a.lse        ? prefill_tc_kernel<HD, true, 0>
+                                 : prefill_tc_kernel<HD, false, 0>;
     cudaError_t e =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
@@ -604,7 +630,7 @@ cudaError_t launch_hd(const PrefillArgs &a, unsigned *err, cudaStream_t stream) 
     const float sl2 = a.scale * 1.4426950408889634f;
     kernel<<<grid, 256, C::SMEM, stream>>>(
         tq, tk, tv, to, a.tile_map, a.work_counter, a.lse, a.pos0, a.n, a.n_q_heads,
-        a.n_kv_heads, a.sink, a.win, sl2, err);
+        a.n_kv_heads, a.sink, a.win, sl2, err, a.split_f, a.split_w);
     return cudaGetLastError();
 }
 

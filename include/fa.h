@@ -166,7 +166,9 @@ fa_status fa_kv_append(const float *k_new, const float *v_new, void *k_planes, v
 
 /* ------------------------------------------------------------------ prefill */
 
-/* Workspace bytes fa_prefill needs (fp16 staging of K and V). */
+/* Workspace bytes fa_prefill needs (fp16 staging of K and V) for every cache
+ * but a Q4_0 one whose shadow window is neither 0 nor FA_Q4_RING_ROWS; that
+ * case needs fa_prefill_chunk_workspace_bytes_for(). */
 size_t fa_prefill_workspace_bytes(int n, int n_q_heads, int n_kv_heads, int head_dim);
 
 /* Tile geometry of the prefill kernel for a head_dim: query rows per tile
@@ -192,8 +194,10 @@ fa_status fa_prefill_tile_shape(int head_dim, int *bq, int *bk);
  *              copy when s < shadow_sink, or when shadow_win > 0 and s is in
  *              the shadow window of the query and still in the ring
  *              ("attention.cu", fc_kvq4_is_fp16 and the ring liveness floor
- *              of fc_attn_flash_prefill_q4); prefill supports shadow_win in
- *              {0, 256}, where that rule depends on s alone.
+ *              of fc_attn_flash_prefill_q4). For shadow_win in {0, 256} that
+ *              rule depends on s alone; for other windows it depends on the
+ *              query too, and the prefill runs in two merged parts (see
+ *              fa_prefill_chunk_workspace_bytes_for for the workspace).
  *   max_seq    row capacity of the planes (n <= max_seq).
  *   workspace  >= fa_prefill_workspace_bytes() bytes of device memory; its
  *              contents are scratch and need no initialisation.
@@ -226,13 +230,25 @@ fa_status fa_prefill_lse(const float *q, const void *k, const void *v, float *ou
  *   q, out     [n][n_q_heads][head_dim] fp32 (device): query row t is at
  *              position pos0 + t.
  *   lse        [n_q_heads][n] fp32 or NULL, as for fa_prefill_lse.
- *   workspace  >= fa_prefill_chunk_workspace_bytes(pos0, n, ...) bytes.
+ *   workspace  >= fa_prefill_chunk_workspace_bytes_for(pos0, n, ..., kv_fmt,
+ *              shadow_win) bytes (FA_ERR_WORKSPACE otherwise).
  *   tile_map   NULL, or [ceil(n/bq)][ceil((pos0+n)/bk)] bytes, as for
  *              fa_prefill with query tiles over the chunk's rows.
- * A Q4_0 key s is read from the fp16 ring when s >= pos0 + n - 256 (shadow
- * window 256; prefill supports {0, 256}). pos0 = 0 is fa_prefill_lse.
- * FA_ERR_INVALID if pos0 < 0 or pos0 + n > max_seq; otherwise fa_prefill's
- * checks and statuses. */
+ * A Q4_0 key s >= shadow_sink is read from the fp16 ring by the query at p
+ * when s >= pos0 + n - 256 (it is still in the ring) and s > p - shadow_win;
+ * with shadow_win = 256 that holds for every query. pos0 = 0 is
+ * fa_prefill_lse. FA_ERR_INVALID if pos0 < 0 or pos0 + n > max_seq;
+ * otherwise fa_prefill's checks and statuses. */
+/* Workspace bytes of fa_prefill_chunk (and fa_prefill, pos0 = 0) for the given
+ * cache format and shadow window. A Q4_0 cache whose shadow window is neither
+ * 0 nor FA_Q4_RING_ROWS runs the prefill in two parts (keys read from the fp16
+ * ring, the other keys), each with its log-sum-exp, merged as
+ * fa_merge_attn_states does; this needs a second K/V staging and the parts'
+ * outputs. For every other case the value equals
+ * fa_prefill_chunk_workspace_bytes(). 0 for invalid sizes. */
+size_t fa_prefill_chunk_workspace_bytes_for(int pos0, int n, int n_q_heads, int n_kv_heads,
+                                            int head_dim, int kv_fmt, int shadow_win);
+
 size_t fa_prefill_chunk_workspace_bytes(int pos0, int n, int n_q_heads, int n_kv_heads,
                                         int head_dim);
 fa_status fa_prefill_chunk(const float *q, const void *k, const void *v, float *out, float *lse,

@@ -71,7 +71,9 @@ def run_prefill(q, k, v, *, kv_fmt, sink, win, shadow_sink=0, shadow_win=0, tile
                                   v_scale=v_scale)
     qd = torch.from_numpy(np.ascontiguousarray(q)).cuda()
     out = torch.full((n, hq, hd), float("nan"), dtype=torch.float32, device="cuda")
-    ws = torch.empty(m.prefill_workspace_bytes(n, hq, hkv, hd), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(m.prefill_workspace_bytes(n, hq, hkv, hd, kv_fmt=fmt_code(kv_fmt),
+                                               shadow_win=shadow_win),
+                     dtype=torch.uint8, device="cuda")
     tm = None
     if tile_map:
         bq, bk = m.prefill_tile_shape(hd)

@@ -95,7 +95,14 @@ def test_prefill_validation(fa):
         assert _prefill_status(fa, fmt=fmt, sw=256) == fa.ERR_INVALID
     assert _prefill_status(fa, fmt=1, ss=9) == fa.ERR_INVALID
     assert _prefill_status(fa, fmt=1, sw=257) == fa.ERR_INVALID
-    assert _prefill_status(fa, fmt=1, sw=100) == fa.ERR_UNSUPPORTED
+    # a Q4_0 shadow window narrower than the ring runs the prefill in two parts
+    # and needs the larger workspace
+    plain = fa.prefill_workspace_bytes(16, 8, 2, 64)
+    split = fa.prefill_workspace_bytes(16, 8, 2, 64, kv_fmt=1, shadow_win=100)
+    assert split > plain
+    assert _prefill_status(fa, fmt=1, sw=100, wsb=plain) == fa.ERR_WORKSPACE
+    for fmt, sw in ((1, 0), (1, 256), (0, 0), (2, 0), (3, 0)):
+        assert fa.prefill_workspace_bytes(16, 8, 2, 64, kv_fmt=fmt, shadow_win=sw) == plain
     assert _prefill_status(fa, wsb=10) == fa.ERR_WORKSPACE
     assert _prefill_status(fa, n=0) == fa.OK                       # empty input: nothing to do
 

@@ -26,6 +26,15 @@ CHUNK_CASES = [
     (1000, 130, 16, 2, 256, 0, 0, "q4_0", (4, 256)),
     (250, 260, 8, 2, 64, 4, 1, "q4_0", (8, 256)),
     (333, 77, 4, 1, 128, 2, 40, "q4_0", (4, 0)),
+    # fp16 windows narrower than the ring: which copy a query reads depends on
+    # the query (the prefill runs as two merged parts)
+    (0, 300, 8, 2, 128, 0, 0, "q4_0", (4, 64)),
+    (0, 200, 16, 2, 256, 0, 0, "q4_0", (2, 100)),
+    (517, 300, 16, 2, 256, 4, 200, "q4_0", (4, 64)),
+    (1000, 130, 16, 2, 256, 0, 0, "q4_0", (8, 255)),
+    (250, 260, 8, 2, 64, 4, 1, "q4_0", (0, 1)),
+    (64, 700, 4, 1, 128, 9, 3, "q4_0", (4, 17)),
+    (300, 1, 8, 2, 64, 0, 0, "q4_0", (4, 128)),
 ]
 
 
@@ -43,8 +52,9 @@ def run_chunk(q, k, v, pos0, *, hq, hkv, hd, sink, win, kv_fmt, shadow, want_map
                         torch.from_numpy(np.ascontiguousarray(v[None, lo:hi])).cuda(), kp, vp,
                         torch.tensor([lo], dtype=torch.int32, device="cuda"), n_kv_heads=hkv,
                         head_dim=hd, max_seq=L, kv_fmt=code, shadow_sink=ss, shadow_win=sw)
-    ws = torch.empty(m.prefill_chunk_workspace_bytes(pos0, n, hq, hkv, hd), dtype=torch.uint8,
-                     device="cuda")
+    ws = torch.empty(m.prefill_chunk_workspace_bytes(pos0, n, hq, hkv, hd, kv_fmt=code,
+                                                     shadow_win=sw),
+                     dtype=torch.uint8, device="cuda")
     out = torch.full((n, hq, hd), float("nan"), dtype=torch.float32, device="cuda")
     lse = torch.full((hq, n), float("nan"), dtype=torch.float32, device="cuda")
     tm = None
@@ -77,8 +87,8 @@ def test_prefill_chunk(oracle_mod, case):
     assert np.array_equal(tm, oracle_mod.tile_map(n, bq, bk, sink, win, pos0=pos0))
 
 
-@pytest.mark.parametrize("fmt", ["f32", "q4_0"])
-def test_prefill_in_chunks(oracle_mod, fmt):
+@pytest.mark.parametrize("fmt,shadow", [("f32", (0, 0)), ("q4_0", (4, 256)), ("q4_0", (4, 64))])
+def test_prefill_in_chunks(oracle_mod, fmt, shadow):
     """A 1000-token sequence prefilled in three chunks (300, 1, 699 tokens),
     each over the cache grown so far. With an fp32 cache the chunks are the
     rows of one prefill of all 1000 tokens; with Q4_0 and the 256-row fp16
@@ -89,7 +99,7 @@ def test_prefill_in_chunks(oracle_mod, fmt):
     q, k, v = prefill_inputs(L, hq, hkv, hd, seed=977)
     whole = oracle_mod.prefill(q, k, v, kv_fmt="f32", sink=sink, win=win) if fmt == "f32" \
         else None
-    ss, sw = (4, 256) if fmt == "q4_0" else (0, 0)
+    ss, sw = shadow
     m = fa()
     code = fmt_code(fmt)
     kp = m.alloc_planes(1, code, hkv, L, hd)
@@ -101,8 +111,9 @@ def test_prefill_in_chunks(oracle_mod, fmt):
                     torch.tensor([lo], dtype=torch.int32, device="cuda"), n_kv_heads=hkv,
                     head_dim=hd, max_seq=L, kv_fmt=code, shadow_sink=ss, shadow_win=sw)
         n = hi - lo
-        ws = torch.empty(m.prefill_chunk_workspace_bytes(lo, n, hq, hkv, hd), dtype=torch.uint8,
-                         device="cuda")
+        ws = torch.empty(m.prefill_chunk_workspace_bytes(lo, n, hq, hkv, hd, kv_fmt=code,
+                                                         shadow_win=sw),
+                         dtype=torch.uint8, device="cuda")
         out = torch.full((n, hq, hd), float("nan"), dtype=torch.float32, device="cuda")
         m.prefill_chunk(torch.from_numpy(np.ascontiguousarray(q[lo:hi])).cuda(), kp, vp, out, lo,
                         n, hq, hkv, hd, sink, win, code, max_seq=L, shadow_sink=ss,
