@@ -28,9 +28,8 @@
 //    order), for V a byte permute pairs two keys of one dim, and the output
 //    rows come out in the order 16c + 2r, 16c + 2r + 1 (undone on write).
 //    k_scale multiplies the score scale, v_scale the partial output: the
-//    products equal the oracle's float(byte) * scale operands up to rounding.
-#include <cuda_fp8.h>
-
+//    result is that of the float(byte) * scale values a reader of the cache
+//    sees, up to rounding.
 #include "decode_softmax.cuh"
 #include "fa_device.cuh"
 #include "fa_internal.h"
