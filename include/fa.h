@@ -344,7 +344,9 @@ fa_status fa_decode_combine(const void *workspace, float *out, int nslots, int n
  * The partials live in a fixed 8 MiB array in the library's device memory
  * (held by every GPU that loads the library until the process exits), laid
  * out as fa_decode's workspace with the entry stride equal to the number of
- * entries E. A problem whose partials need more than 8 MiB
+ * entries E (for fp16 and fp8 caches, whose streaming kernel can use any
+ * number of entries from 2 up, E is the largest count up to max_splits + 1
+ * that fits). A problem whose partials need more than 8 MiB
  * (256 + 2*nslots*n_q_heads*E*4 + nslots*n_q_heads*E*head_dim*4 bytes, parts
  * rounded up to 256) returns FA_ERR_WORKSPACE before any launch. The call
  * allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
