@@ -6,6 +6,12 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
+# The oracle mutation test (test_oracle_mutants.py) runs the pins again against
+# a copy of the oracle package with one planted mistake; the copy's parent
+# directory is named here and shadows the real package.
+_MUTANT_DIR = os.environ.get("FA_ORACLE_MUTANT_DIR")
+if _MUTANT_DIR:
+    sys.path.insert(0, _MUTANT_DIR)
 
 
 def pytest_configure(config):

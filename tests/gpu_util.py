@@ -9,6 +9,50 @@ import torch
 MAX_ABS = 5e-3
 REL_L2 = 2e-3
 
+# Redzones and poison (the substitute for a memory checker). Every buffer the
+# helpers hand to the library sits between two guards of GUARD_BYTES bytes of
+# GUARD_BYTE, and check_guards() asserts they are intact after the call: a
+# write outside a buffer fails the test. Outputs start as NaN and workspaces as
+# 0xff bytes (NaN in fp32 and fp16), so a value the kernels should have written
+# and did not, or scratch read before it was written, reaches the result.
+GUARD_BYTES = 4096
+GUARD_BYTE = 0xA5
+POISON_BYTE = 0xFF
+
+
+def guarded(shape, dtype, *, fill=None, fill_byte=None):
+    """A CUDA tensor of `shape` inside a guarded allocation; its data starts
+    GUARD_BYTES after the allocation's (so its alignment is the allocator's)."""
+    shape = (shape,) if isinstance(shape, int) else tuple(shape)
+    numel = int(np.prod(shape, dtype=np.int64))
+    esz = torch.empty(0, dtype=dtype).element_size()
+    g = GUARD_BYTES // esz
+    raw = torch.empty(numel + 2 * g, dtype=dtype, device="cuda")
+    raw.view(torch.uint8).fill_(GUARD_BYTE)
+    t = raw[g:g + numel]
+    if fill is not None:
+        t.fill_(fill)
+    elif fill_byte is not None:
+        t.view(torch.uint8).fill_(fill_byte)
+    return t.view(shape)
+
+
+def is_guarded(t) -> bool:
+    st = t.untyped_storage()
+    lo = t.storage_offset() * t.element_size()
+    return lo == GUARD_BYTES and st.nbytes() - lo - t.numel() * t.element_size() == GUARD_BYTES
+
+
+def check_guards(*named):
+    """named: (what, tensor) pairs from guarded(); asserts both guards intact."""
+    for what, t in named:
+        assert is_guarded(t), f"{what}: not a guarded buffer"
+        st = t.untyped_storage()
+        b = torch.empty(0, dtype=torch.uint8, device=t.device).set_(st, 0, (st.nbytes(),), (1,))
+        hi = GUARD_BYTES + t.numel() * t.element_size()
+        assert bool((b[:GUARD_BYTES] == GUARD_BYTE).all()), f"{what}: write below the buffer"
+        assert bool((b[hi:] == GUARD_BYTE).all()), f"{what}: write past the end of the buffer"
+
 
 def fa():
     import causal_gqa_flash_attn_gb300 as m
@@ -50,13 +94,21 @@ def build_cache(k, v, *, kv_fmt, shadow_sink=0, shadow_win=0, max_seq=None, pos0
     if max_seq is None:
         max_seq = n
     code = fmt_code(kv_fmt)
-    kp = m.alloc_planes(nslots, code, hkv, max_seq, hd, scale=k_scale)
-    vp = m.alloc_planes(nslots, code, hkv, max_seq, hd, scale=v_scale)
+    pb = m.kv_plane_bytes(code, hkv, max_seq, hd)
+    planes = []
+    for scale in (k_scale, v_scale):
+        t = guarded(nslots * pb, torch.uint8, fill_byte=POISON_BYTE)
+        m.kv_init(t, code, hkv, max_seq, hd)
+        if code == m.KV_FP8_E4M3 and scale != 1.0:
+            m.kv_set_scale(t, code, hkv, max_seq, hd, scale)
+        planes.append(t)
+    kp, vp = planes
     p0 = torch.zeros(nslots, dtype=torch.int32, device="cuda") if pos0 is None else \
         torch.as_tensor(np.asarray(pos0, np.int32), device="cuda")
     m.kv_append(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(), kp, vp, p0,
                 n_kv_heads=hkv, head_dim=hd, max_seq=max_seq, kv_fmt=code,
                 shadow_sink=shadow_sink, shadow_win=shadow_win)
+    check_guards(("k planes", kp), ("v planes", vp))
     return kp, vp, max_seq
 
 
@@ -70,18 +122,20 @@ def run_prefill(q, k, v, *, kv_fmt, sink, win, shadow_sink=0, shadow_win=0, tile
                                   shadow_win=shadow_win, max_seq=max_seq, k_scale=k_scale,
                                   v_scale=v_scale)
     qd = torch.from_numpy(np.ascontiguousarray(q)).cuda()
-    out = torch.full((n, hq, hd), float("nan"), dtype=torch.float32, device="cuda")
-    ws = torch.empty(m.prefill_workspace_bytes(n, hq, hkv, hd, kv_fmt=fmt_code(kv_fmt),
-                                               shadow_win=shadow_win),
-                     dtype=torch.uint8, device="cuda")
+    out = guarded((n, hq, hd), torch.float32, fill=float("nan"))
+    ws = guarded(m.prefill_workspace_bytes(n, hq, hkv, hd, kv_fmt=fmt_code(kv_fmt),
+                                           shadow_win=shadow_win),
+                 torch.uint8, fill_byte=POISON_BYTE)
     tm = None
     if tile_map:
         bq, bk = m.prefill_tile_shape(hd)
-        tm = torch.zeros((-(-n // bq)) * (-(-n // bk)), dtype=torch.uint8, device="cuda")
+        tm = guarded((-(-n // bq)) * (-(-n // bk)), torch.uint8, fill=0)
     m.prefill(qd, kp, vp, out, n, hq, hkv, hd, sink, win, fmt_code(kv_fmt), max_seq=max_seq,
               shadow_sink=shadow_sink, shadow_win=shadow_win, workspace=ws, tile_map=tm)
     st = m.get_device_error()
     assert st == m.OK, m.status_string(st)
+    check_guards(("out", out), ("workspace", ws), ("k planes", kp), ("v planes", vp),
+                 *((("tile map", tm),) if tm is not None else ()))
     res = out.cpu().numpy()
     if tile_map:
         return res, tm.cpu().numpy().reshape(-(-n // bq), -(-n // bk))
@@ -95,9 +149,9 @@ def run_decode(q, kp, vp, pos, *, hkv, hd, max_seq, sink, win, kv_fmt, shadow_si
     nslots, hq, _ = q.shape
     if max_splits is None:
         max_splits = max(1, -(-max_seq // split_keys))
-    ws = torch.empty(m.decode_workspace_bytes(nslots, hq, hd, max_splits), dtype=torch.uint8,
-                     device="cuda")
-    out = torch.full((nslots, hq, hd), float("nan"), dtype=torch.float32, device="cuda")
+    ws = guarded(m.decode_workspace_bytes(nslots, hq, hd, max_splits), torch.uint8,
+                 fill_byte=POISON_BYTE)
+    out = guarded((nslots, hq, hd), torch.float32, fill=float("nan"))
     qd = torch.from_numpy(np.ascontiguousarray(q)).cuda()
     pd = torch.as_tensor(np.asarray(pos, np.int32), device="cuda")
     m.decode(qd, kp, vp, pd, n_q_heads=hq, n_kv_heads=hkv, head_dim=hd, max_seq=max_seq,
@@ -106,4 +160,6 @@ def run_decode(q, kp, vp, pos, *, hkv, hd, max_seq, sink, win, kv_fmt, shadow_si
     m.decode_combine(ws, out, nslots=nslots, n_q_heads=hq, head_dim=hd, max_splits=max_splits)
     st = m.get_device_error()
     assert st == m.OK, m.status_string(st)
+    check_guards(("out", out), ("workspace", ws),
+                 *((w, t) for w, t in (("k planes", kp), ("v planes", vp)) if is_guarded(t)))
     return out.cpu().numpy()
