@@ -464,16 +464,13 @@ constexpr int kPRing = 2;      // P records in flight per pair
 #ifndef FA_Q4_TARGET_PER_SM
 #define FA_Q4_TARGET_PER_SM 4
 #endif
-// Unroll factors (1 or 2) of the loops over a tile's two 16-key halves in the
-// QK and PV warps: 2 interleaves the halves' dependency chains, 1 keeps the
-// registers and the code small.
-#ifndef FA_Q4_QK_HALVES
-#define FA_Q4_QK_HALVES 2
-#endif
+// Unroll factor (1 or 2) of the PV warp's loop over a tile's two 16-key
+// halves: 2 interleaves the halves' dependency chains, 1 keeps the registers
+// and the code small. (The QK warp walks the blocks outermost and both halves
+// inside, so that a block's Q fragments are read once per tile.)
 #ifndef FA_Q4_PV_HALVES
 #define FA_Q4_PV_HALVES 1
 #endif
-constexpr int kQKHalves = FA_Q4_QK_HALVES;
 constexpr int kPVHalves = FA_Q4_PV_HALVES;
 
 template <int HD>
@@ -674,16 +671,20 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
             if (!ok) break;
             const uint8_t *Ks = pbase + C::K_OFF + s * C::TILE_ALLOC;
             const int t0 = k_lo + kTileKeys * i;
-            // ---- scores: half h2 holds keys t0 + 16 h2 + {r, r+8}
-            float sc0[4], sc1[4];
-#pragma unroll kQKHalves
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const uint8_t *KA = Ks + (16 * h2 + r) * ROWB;
-                const uint8_t *KB = KA + 8 * ROWB;
-                float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            // ---- scores: half h2 holds keys t0 + 16 h2 + {r, r+8}; the
+            // block's Q fragments and biases are read once for both halves
+            float sc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
 #pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    const int o18 = kQ4BlockBytes * b;
+            for (int b = 0; b < NB; ++b) {
+                const int o18 = kQ4BlockBytes * b;
+                const uint4 qv = lds_v4(qfrag + b * 32 + lane);
+                const float4 bv = lds_f4(qbias + b * 32 + lane);
+                const float cb[4] = {bv.x, bv.y, bv.z, bv.w};
+                const uint32_t qlo[2] = {qv.x, qv.y}, qhi[2] = {qv.z, qv.w};
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const uint8_t *KA = Ks + (16 * h2 + r) * ROWB;
+                    const uint8_t *KB = KA + 8 * ROWB;
                     uint32_t wA, wB, dA, dB;
                     if ((b & 1) == 0) {
                         const uint32_t a0 = *reinterpret_cast<const uint32_t *>(KA + o18 + 4 + 4 * t);
@@ -706,26 +707,18 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
                                              and_or<0x000F000Fu>(wA8, magic), and_or<0x000F000Fu>(wB8, magic)};
                     const uint32_t ahi[4] = {and_or<0x00F000F0u>(wA, magic), and_or<0x00F000F0u>(wB, magic),
                                              and_or<0x00F000F0u>(wA8, magic), and_or<0x00F000F0u>(wB8, magic)};
-                    const uint4 qv = lds_v4(qfrag + b * 32 + lane);
-                    const float4 bv = lds_f4(qbias + b * 32 + lane);
-                    const float cb[4] = {bv.x, bv.y, bv.z, bv.w};
-                    const uint32_t qlo[2] = {qv.x, qv.y}, qhi[2] = {qv.z, qv.w};
                     float acc[4];
                     mma_16816_c(acc, alo, qlo, cb);
                     mma_16816(acc, ahi, qhi);
                     const float fA = __half2float(__ushort_as_half(static_cast<uint16_t>(dA)));
                     const float fB = __half2float(__ushort_as_half(static_cast<uint16_t>(dB)));
-                    s4[0] = fmaf(fA, acc[0], s4[0]);
-                    s4[1] = fmaf(fA, acc[1], s4[1]);
-                    s4[2] = fmaf(fB, acc[2], s4[2]);
-                    s4[3] = fmaf(fB, acc[3], s4[3]);
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    if (h2 == 0) sc0[k] = s4[k];
-                    else sc1[k] = s4[k];
+                    sc[h2][0] = fmaf(fA, acc[0], sc[h2][0]);
+                    sc[h2][1] = fmaf(fA, acc[1], sc[h2][1]);
+                    sc[h2][2] = fmaf(fB, acc[2], sc[h2][2]);
+                    sc[h2][3] = fmaf(fB, acc[3], sc[h2][3]);
                 }
             }
+            const float *sc0 = sc[0], *sc1 = sc[1];
             // The scores consumed every byte this warp read from the stage, so
             // the stage can take the K tile NK places further on.
             __syncwarp();
