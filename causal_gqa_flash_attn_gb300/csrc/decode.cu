@@ -472,6 +472,13 @@ constexpr int kPRing = 2;      // P records in flight per pair
 #define FA_Q4_PV_HALVES 1
 #endif
 constexpr int kPVHalves = FA_Q4_PV_HALVES;
+// Unroll factor of the QK warp's loop over pairs of 32-element blocks (an even
+// and an odd block per iteration; head_dim / 64 pairs): the full unroll gives
+// the scheduler the most independent work, a partial one smaller code.
+#ifndef FA_Q4_QK_PAIR_UNROLL
+#define FA_Q4_QK_PAIR_UNROLL 4
+#endif
+constexpr int kQKPairUnroll = FA_Q4_QK_PAIR_UNROLL;
 
 template <int HD>
 struct Q4Cfg {
@@ -674,8 +681,11 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
             // ---- scores: half h2 holds keys t0 + 16 h2 + {r, r+8}; the
             // block's Q fragments and biases are read once for both halves
             float sc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+#pragma unroll kQKPairUnroll
+            for (int bp = 0; bp < NB / 2; ++bp)
 #pragma unroll
-            for (int b = 0; b < NB; ++b) {
+            for (int j = 0; j < 2; ++j) {
+                const int b = 2 * bp + j;
                 const int o18 = kQ4BlockBytes * b;
                 const uint4 qv = lds_v4(qfrag + b * 32 + lane);
                 const float4 bv = lds_f4(qbias + b * 32 + lane);
@@ -686,7 +696,7 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
                     const uint8_t *KA = Ks + (16 * h2 + r) * ROWB;
                     const uint8_t *KB = KA + 8 * ROWB;
                     uint32_t wA, wB, dA, dB;
-                    if ((b & 1) == 0) {
+                    if (j == 0) {
                         const uint32_t a0 = *reinterpret_cast<const uint32_t *>(KA + o18 + 4 + 4 * t);
                         const uint32_t a1 = *reinterpret_cast<const uint32_t *>(KA + o18);
                         const uint32_t b0 = *reinterpret_cast<const uint32_t *>(KB + o18 + 4 + 4 * t);
