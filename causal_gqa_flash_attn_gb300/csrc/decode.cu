@@ -884,15 +884,21 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
                 const uint8_t *R1 = R0 + ROWB;                      // key 2t+1
                 const uint8_t *R2 = R0 + 8 * ROWB;                  // key 2t+8
                 const uint8_t *R3 = R2 + ROWB;                      // key 2t+9
+                // The scales of block b for these four keys are the same for
+                // the 8 lanes of a column group: lane (r, t) loads those of
+                // block r once, and block b's come from lane 4b + t.
+                const int om = kQ4BlockBytes * (r < NB ? r : 0);
+                const uint32_t dm01 = __byte_perm(*reinterpret_cast<const uint16_t *>(R0 + om),
+                                                  *reinterpret_cast<const uint16_t *>(R1 + om),
+                                                  0x5410);
+                const uint32_t dm23 = __byte_perm(*reinterpret_cast<const uint16_t *>(R2 + om),
+                                                  *reinterpret_cast<const uint16_t *>(R3 + om),
+                                                  0x5410);
 #pragma unroll
                 for (int b = 0; b < NB; ++b) {
                     const int o18 = kQ4BlockBytes * b;
-                    const uint32_t d01 = __byte_perm(*reinterpret_cast<const uint16_t *>(R0 + o18),
-                                                     *reinterpret_cast<const uint16_t *>(R1 + o18),
-                                                     0x5410);
-                    const uint32_t d23 = __byte_perm(*reinterpret_cast<const uint16_t *>(R2 + o18),
-                                                     *reinterpret_cast<const uint16_t *>(R3 + o18),
-                                                     0x5410);
+                    const uint32_t d01 = __shfl_sync(0xffffffffu, dm01, 4 * b + t);
+                    const uint32_t d23 = __shfl_sync(0xffffffffu, dm23, 4 * b + t);
                     const uint32_t bb[2] = {hmul2u(pb0, d01), hmul2u(pb1, d23)};
                     const int oc = o18 + 2 + 2 * r;
                     const uint32_t z01 = __byte_perm(*reinterpret_cast<const uint16_t *>(R0 + oc),
