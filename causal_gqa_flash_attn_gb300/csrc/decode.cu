@@ -635,7 +635,15 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
         if (sw > 0 && t0 > p - sw) return false;
         return true;
     };
+    // With no window and no shadow window the tiles worth loading are one run:
+    // every tile from the first whose keys reach past the shadow sinks. The
+    // next one at or after i in this pair's sequence (i, i + kPairs, ...) is
+    // then found without testing tiles one by one.
+    const bool one_run = P.win <= 0 && sw <= 0;
+    const int first_ok = k_hi <= ss ? ntiles : max(0, (ss - k_lo) / kTileKeys);
     auto next_tile = [&](int i) -> int {
+        if (one_run)
+            return i >= first_ok ? i : i + (first_ok - i + kPairs - 1) / kPairs * kPairs;
         while (i < ntiles && !tile_ok(i)) i += kPairs;
         return i;
     };
