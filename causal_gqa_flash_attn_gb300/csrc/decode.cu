@@ -443,9 +443,11 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(const DecodeParams 
 // (one bulk copy each). Warp w (QK) scores a tile, folds it into the online
 // softmax and hands P^T fragments plus the O rescale factor of that tile to
 // warp w+4 (PV) through a ring of P records; warp w+4 multiplies them into O.
-// The QK warp's lane 0 issues every copy: a K tile as soon as the QK warp
-// itself has scored the tile before it in that stage, a V tile as soon as the
-// PV warp has released that stage, so that the two warps overlap.
+// Each warp copies the tiles it reads (lane 0, one bulk copy per tile): the QK
+// warp a K tile as soon as it has scored the tile before it in that stage, the
+// PV warp a V tile as soon as it has finished the tile before it in that
+// stage. So a stage frees without a barrier between the warps, and the QK
+// warp, which sets the pace, does no V bookkeeping.
 constexpr int kTileKeys = 32;  // keys per tile
 constexpr int kPairs = 4;      // warp pairs per block
 constexpr int kPRing = 2;      // P records in flight per pair
@@ -501,8 +503,8 @@ struct Q4Cfg {
     static constexpr int QF_OFF = kPairs * PAIR_BYTES;
     static constexpr int QB_OFF = QF_OFF + NB * 32 * 16;
     static constexpr int BAR_OFF = QB_OFF + NB * 32 * 16;
-    // per pair: kfull[NK], vfull[NV], vempty[NV], pfull[kPRing], pempty[kPRing]
-    static constexpr int BARS_PER_PAIR = NK + 2 * NV + 2 * kPRing;
+    // per pair: kfull[NK], vfull[NV], pfull[kPRing], pempty[kPRing]
+    static constexpr int BARS_PER_PAIR = NK + NV + 2 * kPRing;
     static constexpr int SMEM_PIPE = BAR_OFF + kPairs * BARS_PER_PAIR * 8 + 16;
     static constexpr int SMEM_GENERIC = kWarps * 2 * kChunk * (HD + 8) * 2;
     static constexpr int SMEM_MERGE = kWarps * 16 * (4 + HD) * 4;
@@ -603,8 +605,8 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
     uint4 *qfrag = reinterpret_cast<uint4 *>(dsmem + C::QF_OFF);
     float4 *qbias = reinterpret_cast<float4 *>(dsmem + C::QB_OFF);
     uint64_t *bars = reinterpret_cast<uint64_t *>(dsmem + C::BAR_OFF) + pair * C::BARS_PER_PAIR;
-    uint64_t *kfull = bars, *vfull = bars + NK, *vempty = bars + NK + NV,
-             *pfull = bars + NK + 2 * NV, *pempty = bars + NK + 2 * NV + kPRing;
+    uint64_t *kfull = bars, *vfull = bars + NK, *pfull = bars + NK + NV,
+             *pempty = bars + NK + NV + kPRing;
     volatile int *abort =
         reinterpret_cast<volatile int *>(dsmem + C::BAR_OFF + kPairs * C::BARS_PER_PAIR * 8);
 
@@ -612,10 +614,7 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
     if (threadIdx.x == 0) *abort = 0;
     if (qk_role && lane == 0) {
         for (int s = 0; s < NK; ++s) mbar_init(&kfull[s], 1);
-        for (int s = 0; s < NV; ++s) {
-            mbar_init(&vfull[s], 1);
-            mbar_init(&vempty[s], 1);
-        }
+        for (int s = 0; s < NV; ++s) mbar_init(&vfull[s], 1);
         for (int s = 0; s < kPRing; ++s) {
             mbar_init(&pfull[s], 1);
             mbar_init(&pempty[s], 1);
@@ -648,35 +647,38 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
         return i;
     };
     bool ok = true;
+    // one bulk copy of tile i's rows (rounded up to 16 bytes) into dst
+    auto issue = [&](const uint8_t *body, int i, uint8_t *dst, uint64_t *bar) {
+        const int t0 = k_lo + kTileKeys * i;
+        const int nk = min(kTileKeys, k_hi - t0);
+        const uint32_t bytes = (static_cast<uint32_t>(nk * ROWB) + 15u) & ~15u;
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_copy_g2s(dst, body + static_cast<size_t>(t0) * ROWB, bytes, bar);
+    };
+    // wait (bounded, ignoring the abort flag) for the last copy issued into
+    // each of a ring's stages, so that no copy lands after the block is gone
+    auto drain = [&](uint64_t *full, int nst, int issued) {
+        for (int st = 0; st < nst; ++st)
+            if (issued > st) {
+                const long long c0 = clock64();
+                while (!mbar_try_wait(&full[st], ((issued - 1 - st) / nst) & 1) &&
+                       clock64() - c0 < kSpinCycles) {
+                }
+            }
+    };
 
     if (qk_role) {
         // ================================================= QK + softmax warp
         const uint8_t *kbody = P.k_planes + static_cast<size_t>(u) * P.plane_bytes + P.body_off +
                                static_cast<size_t>(g) * P.max_seq * ROWB;
-        const uint8_t *vbody = P.v_planes + static_cast<size_t>(u) * P.plane_bytes + P.body_off +
-                               static_cast<size_t>(g) * P.max_seq * ROWB;
-        // one bulk copy of tile i's rows (rounded up to 16 bytes) into dst
-        auto issue = [&](const uint8_t *body, int i, uint8_t *dst, uint64_t *bar) {
-            const int t0 = k_lo + kTileKeys * i;
-            const int nk = min(kTileKeys, k_hi - t0);
-            const uint32_t bytes = (static_cast<uint32_t>(nk * ROWB) + 15u) & ~15u;
-            mbar_arrive_expect_tx(bar, bytes);
-            bulk_copy_g2s(dst, body + static_cast<size_t>(t0) * ROWB, bytes, bar);
-        };
         float mu0 = -INFINITY, mu1 = -INFINITY, mt0 = -INFINITY, mt1 = -INFINITY;
         float ls0 = 0.0f, ls1 = 0.0f;
-        // Prologue: the first NK K tiles and the first NV - 1 V tiles. V stays
-        // one tile behind so that refilling a V stage waits on the PV warp's
-        // previous tile, not on the one just handed over.
-        int kt = next_tile(pair), vt = kt;  // next tile index to copy
-        int kn = 0, vn = 0;                 // copies issued so far
+        // Prologue: the first NK K tiles (the PV warp copies the V tiles).
+        int kt = next_tile(pair);  // next tile index to copy
+        int kn = 0;                // copies issued so far
         for (; kn < NK && kt < ntiles; ++kn) {
             if (lane == 0) issue(kbody, kt, pbase + C::K_OFF + kn * C::TILE_ALLOC, &kfull[kn]);
             kt = next_tile(kt + kPairs);
-        }
-        for (; vn < NV - 1 && vt < ntiles; ++vn) {
-            if (lane == 0) issue(vbody, vt, pbase + C::V_OFF + vn * C::TILE_ALLOC, &vfull[vn]);
-            vt = next_tile(vt + kPairs);
         }
         const uint32_t magic = opaque(kMagic);
         int seq = 0;  // position of the tile in this pair's sequence
@@ -783,19 +785,6 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
                                         static_cast<uint32_t>(i), 0u);
             __syncwarp();
             if (lane == 0) mbar_arrive(&pfull[ps]);  // release: the record is visible
-            // ---- V tile NV - 1 places ahead, into the stage the PV warp frees
-            // when it finishes the tile before this one
-            if (vt < ntiles) {
-                const int sv_ = vn % NV;
-                if (vn >= NV) {
-                    ok = __all_sync(0xffffffffu,
-                                    mbar_wait(&vempty[sv_], ((vn / NV) - 1) & 1, abort, P.err));
-                    if (!ok) break;
-                }
-                if (lane == 0) issue(vbody, vt, pbase + C::V_OFF + sv_ * C::TILE_ALLOC, &vfull[sv_]);
-                vt = next_tile(vt + kPairs);
-                ++vn;
-            }
         }
         // end of the sequence for the PV warp
         if (ok) {
@@ -810,24 +799,7 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
                 if (lane == 0) mbar_arrive(&pfull[ps]);
             }
         }
-        if (!ok) {
-            // let the copies already issued land before the shared memory is
-            // reused: wait (bounded) for the last phase of every stage used
-            for (int st = 0; st < NK; ++st)
-                if (kn > st) {
-                    const long long c0 = clock64();
-                    while (!mbar_try_wait(&kfull[st], ((kn - 1 - st) / NK) & 1) &&
-                           clock64() - c0 < kSpinCycles) {
-                    }
-                }
-            for (int st = 0; st < NV; ++st)
-                if (vn > st) {
-                    const long long c0 = clock64();
-                    while (!mbar_try_wait(&vfull[st], ((vn - 1 - st) / NV) & 1) &&
-                           clock64() - c0 < kSpinCycles) {
-                    }
-                }
-        }
+        if (!ok) drain(kfull, NK, kn);  // let this warp's copies land first
         float m_used[1][2] = {{mu0, mu1}}, m_true[1][2] = {{mt0, mt1}}, lsum[1][2] = {{ls0, ls1}};
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
@@ -849,6 +821,16 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
         const uint32_t magic = opaque(kMagic);
         const uint32_t ncorr[4] = {opaque(kHNeg1032), opaque(kHNeg1152), opaque(kHNeg1032),
                                    opaque(kHNeg1152)};
+        // This warp copies the V tiles: the first NV now, then each stage again
+        // as soon as it has finished the tile in it (NV tiles ahead).
+        const uint8_t *vbody = P.v_planes + static_cast<size_t>(u) * P.plane_bytes + P.body_off +
+                               static_cast<size_t>(g) * P.max_seq * ROWB;
+        int vt = next_tile(pair);  // next tile index to copy
+        int vn = 0;                // copies issued so far
+        for (; vn < NV && vt < ntiles; ++vn) {
+            if (lane == 0) issue(vbody, vt, pbase + C::V_OFF + vn * C::TILE_ALLOC, &vfull[vn]);
+            vt = next_tile(vt + kPairs);
+        }
         for (int seq = 0;; ++seq) {
             const int ps = seq % kPRing;
             ok = __all_sync(0xffffffffu, mbar_wait(&pfull[ps], (seq / kPRing) & 1, abort, P.err));
@@ -930,9 +912,17 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
                     mma_16816(o[2 * b + 1][0], ncorr, bb);
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&vempty[s]);
+            __syncwarp();  // every lane has read the stage
+            if (vt < ntiles) {
+                if (lane == 0) {
+                    fence_proxy_async_smem();  // those reads come before the copy's writes
+                    issue(vbody, vt, Vs, &vfull[s]);
+                }
+                vt = next_tile(vt + kPairs);
+                ++vn;
+            }
         }
+        if (!ok) drain(vfull, NV, vn);  // let this warp's copies land first
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {  // rows r + 8 carry 16 (c - 8)
             o[mt][0][2] *= 0.0625f;
