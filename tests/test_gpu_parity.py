@@ -181,6 +181,10 @@ DECODE_CASES = [
     ((999, 5), 8, 1, 64, 0, 0, "f32", (0, 0), 100, 1000),
     ((1234,), 16, 1, 256, 3, 17, "f32", (0, 0), 256, 1300),
     ((640, 640, 640, 640), 4, 4, 64, 0, 0, "q4_0", (8, 256), 256, 700),
+    # no window and no shadow window (the Q4_0 tiles are one run), including
+    # slots whose every key is an fp16 sink (lengths 3 and 5 <= 8 sinks)
+    ((3, 9, 40, 777), 8, 2, 128, 0, 0, "q4_0", (8, 0), 256, 800),
+    ((5, 1300), 4, 1, 64, 2, 0, "q4_0", (8, 0), 128, 1400),
 ]
 
 
