@@ -48,7 +48,7 @@ constexpr float kRescaleDense = 8.0f;  // lazy-rescale threshold (log2 units)
 #define FA_DENSE_NW_SMALL 8
 #endif
 #ifndef FA_DENSE_NW_FP8
-#define FA_DENSE_NW_FP8 6
+#define FA_DENSE_NW_FP8 7
 #endif
 // Keys per tile of the fp8 kernel (16 or 32; fp16 uses 16): a longer tile
 // spreads each tile's fixed work (waits, copies, masks, the softmax step)
@@ -71,7 +71,9 @@ struct DenseCfg {
     static constexpr int NW = FMT == kFmtFp8      ? FA_DENSE_NW_FP8
                               : STAGE >= 16384 ? FA_DENSE_NW_BIG
                                                : FA_DENSE_NW_SMALL;
-    static constexpr int NS0 = 196608 / (NW * STAGE);
+    // ring stages from a 224 KB budget (the 227 KB a block may have, less the
+    // barriers and the alignment slack)
+    static constexpr int NS0 = 229376 / (NW * STAGE);
     static constexpr int NS = NS0 > 8 ? 8 : NS0;       // ring stages per warp
     static constexpr int MT = HD / 16;
     static constexpr int WARP_BYTES = NS * STAGE;
