@@ -21,6 +21,10 @@ PINS = os.path.join(ROOT, "tests", "test_oracle_pins.py")
 
 # (name, file, exact text, replacement): each a mistake a restatement of the
 # pages could plausibly make.
+# Left out because they are equivalent to the oracle (no input tells them
+# apart): dropping the id = 0 guard of an all-zero Q4_0 block (0 * inf is NaN,
+# whose code is 0 + 8, the same code) and dropping the shadow_win > 0 test of the
+# read rule (with shadow_win 0, s > p - 0 never holds for a key s <= p).
 MUTANTS = [
     # binary16 conversion
     ("f16_ties_away", "oracle.c", "(rem == 0x1000u && (h & 1u))", "(rem == 0x1000u)"),
@@ -94,6 +98,28 @@ MUTANTS = [
     ("combine_no_rescale_of_l", "oracle.c", "den += w * l[s];", "den += l[s];"),
     ("combine_inverted_weight", "oracle.c", "const double w = exp(m[s] - M);",
      "const double w = exp(M - m[s]);"),
+    # edge branches
+    ("f16_overflow_not_inf", "oracle.c", "    if (E > 15)\n        return (uint16_t)(sign | 0x7c00u);",
+     "    if (E > 15)\n        return (uint16_t)(sign | 0x7bffu);"),
+    ("f16_nan_becomes_inf", "oracle.c", "(man ? 0x7e00u : 0x7c00u)", "(0x7c00u)"),
+    ("e4m3_nan_saturates", "oracle.c", "    if (isnan(f))\n        return 0x7f;",
+     "    if (isnan(f))\n        return 0x7e;"),
+    ("e4m3_neg_zero_positive", "oracle.c", "    if (a == 0.0)\n        return sign;",
+     "    if (a == 0.0)\n        return 0;"),
+    ("q4_no_low_clamp", "oracle.c", "    if (c < 0)\n        return 0;", "    if (c < 0)\n        return c & 15;"),
+    ("q4_no_high_clamp", "oracle.c", "    if (c > 15)\n        return 15;", "    if (c > 15)\n        return c & 15;"),
+    ("q4_nan_not_zero", "oracle.c", "    if (isnan(t))\n        return 0;", "    if (isnan(t))\n        return 7;"),
+    ("tile_map_ignores_offset", "oracle.c", "if (oracle_visible(pos0 + t, j, sink, win))",
+     "if (oracle_visible(t, j, sink, win))"),
+    ("partial_empty_not_zeroed", "oracle.c", "        for (int e = 0; e < hd; e++)\n            acc[e] = 0.0;",
+     "        for (int e = 1; e < hd; e++)\n            acc[e] = 0.0;"),
+    ("combine_all_empty_ok", "oracle.c", "    if (M == -INFINITY)\n        return -1;",
+     "    if (M == -INFINITY)\n        return 0;"),
+    ("merge_both_empty_takes_suffix", "oracle.c",
+     "                for (int d = 0; d < D; d++)\n                    out[row + d] = prefix[row + d];\n                out_lse[li] = -INFINITY;",
+     "                for (int d = 0; d < D; d++)\n                    out[row + d] = suffix[row + d];\n                out_lse[li] = -INFINITY;"),
+    ("attention_sees_only_window", "oracle.c", "return (j < sink) || (j >= p - win + 1);",
+     "return (j >= p - win + 1);"),
     # the numpy front end
     ("chunk_offset_dropped", "oracle.py", "return attention(q[rows], rows + pos0, kk, vv,",
      "return attention(q[rows], rows, kk, vv,"),

@@ -43,6 +43,18 @@ def test_f16_matches_numpy_conversion(oracle_mod):
         assert np.array_equal(oracle_mod.f16_rne(arr), ref)
 
 
+def test_f16_nan_stays_nan(oracle_mod):
+    """A NaN becomes a binary16 NaN of the same sign (exponent all ones, mantissa
+    not zero), and the canonical quiet NaN the value numpy's cast gives."""
+    bits = np.array([0x7fc00000, 0xffc00000, 0x7f800001, 0xff800001, 0x7fffffff, 0x7fa00000],
+                    dtype=np.uint32)
+    h = oracle_mod.f16_rne(bits.view(np.float32)).astype(np.uint32)
+    assert np.all((h & 0x7c00) == 0x7c00) and np.all((h & 0x03ff) != 0)
+    assert np.array_equal(h >> 15, bits >> 31)
+    ref = np.array([np.nan], np.float32).astype(np.float16).view(np.uint16)
+    assert oracle_mod.f16_rne(np.array([np.nan], np.float32))[0] == ref[0]
+
+
 def test_f16_decode_matches_numpy(oracle_mod):
     h = np.arange(0, 65536, dtype=np.uint32).astype(np.uint16)
     ref = h.view(np.float16).astype(np.float64)
