@@ -120,6 +120,15 @@ MUTANTS = [
      "                for (int d = 0; d < D; d++)\n                    out[row + d] = suffix[row + d];\n                out_lse[li] = -INFINITY;"),
     ("attention_sees_only_window", "oracle.c", "return (j < sink) || (j >= p - win + 1);",
      "return (j >= p - win + 1);"),
+    ("q4_high_saturation_zero", "oracle.c", "    if (td >= 2147483648.0)\n        return INT32_MAX;",
+     "    if (td >= 2147483648.0)\n        return 0;"),
+    ("q4_offset_saturates", "oracle.c", "(int32_t)((uint32_t)qv + 8u)",
+     "(qv > 2147483639 ? 2147483647 : qv + 8)"),
+    ("plan_cap_ignored", "oracle.c", "    if (ns > cap)\n        ns = cap;", "    (void)cap;"),
+    ("merge_suffix_pos_inf_kept", "oracle.c", "if (ls == INFINITY)\n                ls = -INFINITY;",
+     "if (ls == INFINITY)\n                ls = INFINITY;"),
+    ("partial_max_not_subtracted", "oracle.c", "const double w = exp(scale * dot - m);",
+     "const double w = exp(scale * dot);"),
     # the numpy front end
     ("chunk_offset_dropped", "oracle.py", "return attention(q[rows], rows + pos0, kk, vv,",
      "return attention(q[rows], rows, kk, vv,"),
