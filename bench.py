@@ -5,6 +5,9 @@ Default run (one JSON line on stdout):
     fp32 KV cache, full causal. One step = fa_kv_append (K, V rows into the
     cache) + fa_prefill (fp16 staging + tensor-core kernel). value = causal
     attention TFLOP/s (4 * head_dim * n_q_heads * sum_p |S(p)| per step).
+    The prefill steps (headline and prefill workloads) are captured once in a
+    CUDA graph and replayed, one replay per timed step; the decode steps are
+    timed as plain calls (replay measured 2-3% slower for them).
   * "workloads": the windowed prefill (sink 4, win 1024), the Q4_0-KV prefill
     (fp16 shadow of 4 sinks + 256 recent rows) and the multi-slot decode
     (32 slots x 32768 keys, Q4_0, 4 fp16 sinks, 256-key splits + combine),
@@ -167,19 +170,33 @@ class GpuBench:
         self.stream = torch.cuda.current_stream(dev)
         self.flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
         self.launches = 0
+        self.graph_steps = None  # True once a step was timed as graph replays
+        self.graph_error = None
 
     def flush_l2(self):
         self.flush_buf.zero_()
 
-    def timed_steps(self, step, warmup, steps, kernel_events=True):
+    def timed_steps(self, step, warmup, steps, kernel_events=True, graph=False):
         """Run warmup + steps of `step`; each timed step between CUDA events on
         the launching stream, L2 flushed in between (outside the events).
-        Returns (step ms list, dominant-kernel ms list)."""
+        With graph, the step is captured once in a CUDA graph and each timed
+        step is one replay (the same launches, without the host's launch gaps);
+        if the capture fails the steps run as plain calls. Returns (step ms
+        list, dominant-kernel ms list)."""
         torch, fa = self.torch, self.fa
         for _ in range(warmup):
             self.flush_l2()
             step()
         torch.cuda.synchronize(self.dev)
+        if graph:
+            try:
+                out = self._timed_graph(step, steps, kernel_events)
+                self.graph_steps = True
+                return out
+            except Exception as exc:  # a refused capture: time the plain calls
+                self.graph_steps = False
+                self.graph_error = str(exc)[:200]
+                torch.cuda.synchronize(self.dev)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
                torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(steps)]
@@ -201,6 +218,37 @@ class GpuBench:
             raise RuntimeError(f"device error {fa.status_string(st)}")
         step_ms = [a.elapsed_time(b) for a, b, _, _ in ev]
         kern_ms = [a.elapsed_time(b) for _, _, a, b in ev] if kernel_events else []
+        return step_ms, kern_ms
+
+    def _timed_graph(self, step, steps, kernel_events):
+        torch, fa = self.torch, self.fa
+        s0, s1, k0, k1 = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+        for x in (s0, s1, k0, k1):  # create the underlying CUDA events
+            x.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        g = torch.cuda.CUDAGraph()
+        if kernel_events:  # recorded as event nodes on every replay
+            fa.set_kernel_events(k0, k1)
+        try:
+            with torch.cuda.graph(g):
+                step()
+        finally:
+            fa.set_kernel_events(None, None)
+        g.replay()  # one untimed replay
+        torch.cuda.synchronize(self.dev)
+        step_ms, kern_ms = [], []
+        for _ in range(steps):
+            self.flush_l2()
+            s0.record(self.stream)
+            g.replay()
+            s1.record(self.stream)
+            torch.cuda.synchronize(self.dev)
+            step_ms.append(s0.elapsed_time(s1))
+            if kernel_events:
+                kern_ms.append(k0.elapsed_time(k1))
+        st = fa.get_device_error()
+        if st != fa.OK:
+            raise RuntimeError(f"device error {fa.status_string(st)}")
         return step_ms, kern_ms
 
     # ---- prefill workloads
@@ -511,7 +559,8 @@ def main():
     barrier()
     t_wall = time.perf_counter()
     with ClockSampler(local) as clk:
-        step_ms, kern_ms = B.timed_steps(lambda: B.prefill_step(S), args.warmup, args.steps)
+        step_ms, kern_ms = B.timed_steps(lambda: B.prefill_step(S), args.warmup, args.steps,
+                                         graph=True)
     barrier()
     wall = time.perf_counter() - t_wall
     ms = max_over_ranks(statistics.mean(step_ms))
@@ -548,10 +597,11 @@ def main():
         w = BY_NAME[name]
         S = B.prefill_setup(w)
         f = 4.0 * w.head_dim * w.n_q_heads * visible_pairs(w.n, w.sink, w.win)
-        sm, km = B.timed_steps(lambda: B.prefill_step(S), args.warmup, args.steps)
+        sm, km = B.timed_steps(lambda: B.prefill_step(S), args.warmup, args.steps, graph=True)
         a = f / (statistics.mean(km) * 1e-3) / 1e12
         extra[name] = {"value": f / (statistics.mean(sm) * 1e-3) / 1e12, "unit": "TFLOP/s",
                        "ms_per_step": statistics.mean(sm), "flop_per_step": f,
+                       "launch": "graph replay" if B.graph_steps else "plain calls",
                        "roofline": {"kernel": "prefill_tc_kernel<256>", "bound": "tensor",
                                     "achieved": a, "peak": peaks["bf16_tflops"],
                                     "unit": "TFLOP/s", "frac": a / peaks["bf16_tflops"],
@@ -581,12 +631,13 @@ def main():
                            w.head_dim, w.sink, w.win, S["code"], max_seq=w.n, workspace=wsc)
     f = 4.0 * w.head_dim * w.n_q_heads * (visible_pairs(w.n, w.sink, w.win)
                                           - visible_pairs(pos0, w.sink, w.win))
-    sm, km = B.timed_steps(chunk_step, args.warmup, args.steps)
+    sm, km = B.timed_steps(chunk_step, args.warmup, args.steps, graph=True)
     a = f / (statistics.mean(km) * 1e-3) / 1e12
     extra["prefill_chunk_f32_pos4096_n4096_h16x2_d256"] = {
         "value": f / (statistics.mean(sm) * 1e-3) / 1e12, "unit": "TFLOP/s",
         "ms_per_step": statistics.mean(sm), "flop_per_step": f,
         "step": "kv_append of the chunk + fa_prefill_chunk",
+        "launch": "graph replay" if B.graph_steps else "plain calls",
         "roofline": {"kernel": "prefill_tc_kernel<256>", "bound": "tensor", "achieved": a,
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": a / peaks["bf16_tflops"], "kernel_ms": statistics.mean(km)}}
@@ -607,6 +658,7 @@ def main():
         extra[w.name] = {"value": kvb / (statistics.mean(sm) * 1e-3) / 1e9, "unit": "GB/s",
                          "ms_per_step": statistics.mean(sm), "kv_bytes_per_step": kvb,
                          "step": "append 1 row/slot + split decode + combine",
+                         "launch": "plain calls",
                          "roofline": {"kernel": kname, "bound": "hbm",
                                       "achieved": a, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                       "frac": a / peaks["hbm_gbs"], "frac_of_8tbs": a / 8000.0,
@@ -652,6 +704,9 @@ def main():
                        "head_dim": headline.head_dim, "sink": headline.sink, "win": headline.win,
                        "kv_fmt": headline.kv_fmt, "flop_per_step": flops_step,
                        "step": "kv_append + prefill", "l2": "flushed between steps (256 MB write)",
+                       "launch": ("the step captured once in a CUDA graph, each timed step one "
+                                  "replay" if B.graph_steps else
+                                  f"plain calls (graph capture failed: {B.graph_error})"),
                        "parallelism": "replicas" if world > 1 else "1 GPU"},
             "roofline": roofline,
             "cpu_baseline": cpu,
