@@ -166,11 +166,9 @@ fa_status prefill_split(const float *q, const void *k, const void *v, float *out
     unsigned *ctr2 = reinterpret_cast<unsigned *>(ws + w.ctr2_off);
     // the ring holds the 256 newest rows (ring liveness): near keys start at F
     const int F = nk - FA_Q4_RING_ROWS > shadow_sink ? nk - FA_Q4_RING_ROWS : shadow_sink;
-    cudaError_t e = fa::launch_stage_kv(static_cast<const uint8_t *>(k), kh2, nk, g, shadow_sink,
-                                        FA_Q4_RING_ROWS, s);
-    if (e == cudaSuccess)
-        e = fa::launch_stage_kv(static_cast<const uint8_t *>(v), vh2, nk, g, shadow_sink,
-                                FA_Q4_RING_ROWS, s);
+    cudaError_t e = fa::launch_stage_kv(static_cast<const uint8_t *>(k),
+                                        static_cast<const uint8_t *>(v), kh2, vh2, nk, g,
+                                        shadow_sink, FA_Q4_RING_ROWS, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(ctr2, 0, sizeof(unsigned), s);
     fa::PrefillArgs a;
     a.qh = qh;
@@ -445,10 +443,8 @@ fa_status fa_prefill_chunk(const float *q, const void *k, const void *v, float *
         // paths read what the shadow geometry gives every query
         const int sw_stage = split ? 0 : shadow_win;
         if (e == cudaSuccess)
-            e = fa::launch_stage_kv(static_cast<const uint8_t *>(k), kh, nk, g, shadow_sink,
-                                    sw_stage, s);
-        if (e == cudaSuccess)
-            e = fa::launch_stage_kv(static_cast<const uint8_t *>(v), vh, nk, g, shadow_sink,
+            e = fa::launch_stage_kv(static_cast<const uint8_t *>(k),
+                                    static_cast<const uint8_t *>(v), kh, vh, nk, g, shadow_sink,
                                     sw_stage, s);
     }
     if (e != cudaSuccess) return FA_ERR_CUDA;

@@ -53,8 +53,10 @@ cudaError_t launch_kv_append(const float *k_new, const float *v_new, uint8_t *k_
 // Converts q and zeroes *counter (the prefill kernel's work queue).
 cudaError_t launch_stage_q(const float *q, __half *qh, size_t count, unsigned *counter,
                            cudaStream_t stream);
-cudaError_t launch_stage_kv(const uint8_t *plane, __half *dst, int n, const PlaneGeom &g,
-                            int shadow_sink, int shadow_win, cudaStream_t stream);
+// Stages rows 0..n-1 of the K and the V plane into kdst and vdst in one launch.
+cudaError_t launch_stage_kv(const uint8_t *kplane, const uint8_t *vplane, __half *kdst,
+                            __half *vdst, int n, const PlaneGeom &g, int shadow_sink,
+                            int shadow_win, cudaStream_t stream);
 
 // ---- prefill_tc.cu
 struct PrefillArgs {

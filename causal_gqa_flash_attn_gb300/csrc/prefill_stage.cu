@@ -35,10 +35,15 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// The K and V planes are staged by one launch: blockIdx.y picks the plane.
+
 // fp32 cache rows -> fp16, one thread per 4 values.
 __global__ void __launch_bounds__(kThreads)
-    stage_kv_f32_kernel(const uint8_t *__restrict__ plane, uint2 *__restrict__ dst, int n,
-                        int n_kv, int hd, int max_seq, size_t body_off) {
+    stage_kv_f32_kernel(const uint8_t *__restrict__ kplane, const uint8_t *__restrict__ vplane,
+                        uint2 *__restrict__ kdst, uint2 *__restrict__ vdst, int n, int n_kv,
+                        int hd, int max_seq, size_t body_off) {
+    const uint8_t *__restrict__ plane = blockIdx.y ? vplane : kplane;
+    uint2 *__restrict__ dst = blockIdx.y ? vdst : kdst;
     const int q4 = hd / 4;
     const long long total = static_cast<long long>(n_kv) * n * q4;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
@@ -55,8 +60,11 @@ __global__ void __launch_bounds__(kThreads)
 
 // fp8 e4m3fn cache rows -> fp16, one thread per 8 values (8 bytes in, 16 out).
 __global__ void __launch_bounds__(kThreads)
-    stage_kv_fp8_kernel(const uint8_t *__restrict__ plane, uint4 *__restrict__ dst, int n,
-                        int n_kv, int hd, int max_seq, size_t body_off, size_t scale_off) {
+    stage_kv_fp8_kernel(const uint8_t *__restrict__ kplane, const uint8_t *__restrict__ vplane,
+                        uint4 *__restrict__ kdst, uint4 *__restrict__ vdst, int n, int n_kv,
+                        int hd, int max_seq, size_t body_off, size_t scale_off) {
+    const uint8_t *__restrict__ plane = blockIdx.y ? vplane : kplane;
+    uint4 *__restrict__ dst = blockIdx.y ? vdst : kdst;
     const int q8 = hd / 8;
     const long long total = static_cast<long long>(n_kv) * n * q8;
     const float c = __ldg(reinterpret_cast<const float *>(plane + scale_off));
@@ -75,9 +83,12 @@ __global__ void __launch_bounds__(kThreads)
 // Q4_0 cache rows -> fp16 value seen by every query of the prefill; one
 // thread per 32-value block (4 x 16-byte stores).
 __global__ void __launch_bounds__(kThreads)
-    stage_kv_q4_kernel(const uint8_t *__restrict__ plane, uint4 *__restrict__ dst, int n,
-                       int n_kv, int hd, int max_seq, size_t body_off, size_t row_bytes,
-                       size_t sink_off, size_t ring_off, int shadow_sink, int shadow_win) {
+    stage_kv_q4_kernel(const uint8_t *__restrict__ kplane, const uint8_t *__restrict__ vplane,
+                       uint4 *__restrict__ kdst, uint4 *__restrict__ vdst, int n, int n_kv,
+                       int hd, int max_seq, size_t body_off, size_t row_bytes, size_t sink_off,
+                       size_t ring_off, int shadow_sink, int shadow_win) {
+    const uint8_t *__restrict__ plane = blockIdx.y ? vplane : kplane;
+    uint4 *__restrict__ dst = blockIdx.y ? vdst : kdst;
     const int nb = hd / kQ4Block;
     const long long total = static_cast<long long>(n_kv) * n * nb;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
@@ -144,24 +155,27 @@ cudaError_t launch_stage_q(const float *q, __half *qh, size_t count, unsigned *c
     return cudaGetLastError();
 }
 
-cudaError_t launch_stage_kv(const uint8_t *plane, __half *dst, int n, const PlaneGeom &g,
-                            int shadow_sink, int shadow_win, cudaStream_t stream) {
+cudaError_t launch_stage_kv(const uint8_t *kplane, const uint8_t *vplane, __half *kdst,
+                            __half *vdst, int n, const PlaneGeom &g, int shadow_sink,
+                            int shadow_win, cudaStream_t stream) {
     if (g.fmt == kFmtF32) {
         const long long items = static_cast<long long>(g.n_kv) * n * (g.hd / 4);
-        stage_kv_f32_kernel<<<grid_for(items), kThreads, 0, stream>>>(
-            plane, reinterpret_cast<uint2 *>(dst), n, g.n_kv, g.hd, g.max_seq, g.body_off);
+        stage_kv_f32_kernel<<<dim3(grid_for(items), 2), kThreads, 0, stream>>>(
+            kplane, vplane, reinterpret_cast<uint2 *>(kdst), reinterpret_cast<uint2 *>(vdst), n,
+            g.n_kv, g.hd, g.max_seq, g.body_off);
     } else if (g.fmt == kFmtFp8) {
         const long long items = static_cast<long long>(g.n_kv) * n * (g.hd / 8);
-        stage_kv_fp8_kernel<<<grid_for(items), kThreads, 0, stream>>>(
-            plane, reinterpret_cast<uint4 *>(dst), n, g.n_kv, g.hd, g.max_seq, g.body_off,
-            g.scale_off);
+        stage_kv_fp8_kernel<<<dim3(grid_for(items), 2), kThreads, 0, stream>>>(
+            kplane, vplane, reinterpret_cast<uint4 *>(kdst), reinterpret_cast<uint4 *>(vdst), n,
+            g.n_kv, g.hd, g.max_seq, g.body_off, g.scale_off);
     } else if (g.fmt != kFmtQ4) {
         return cudaErrorInvalidValue;  // fp16 planes are read in place
     } else {
         const long long items = static_cast<long long>(g.n_kv) * n * (g.hd / kQ4Block);
-        stage_kv_q4_kernel<<<grid_for(items), kThreads, 0, stream>>>(
-            plane, reinterpret_cast<uint4 *>(dst), n, g.n_kv, g.hd, g.max_seq, g.body_off,
-            g.row_bytes, g.sink_off, g.ring_off, shadow_sink, shadow_win);
+        stage_kv_q4_kernel<<<dim3(grid_for(items), 2), kThreads, 0, stream>>>(
+            kplane, vplane, reinterpret_cast<uint4 *>(kdst), reinterpret_cast<uint4 *>(vdst), n,
+            g.n_kv, g.hd, g.max_seq, g.body_off, g.row_bytes, g.sink_off, g.ring_off,
+            shadow_sink, shadow_win);
     }
     return cudaGetLastError();
 }
