@@ -199,3 +199,45 @@ def test_kv_init_validation(fa):
     assert L.fa_kv_init(None, 1, fa.KV_F16, 2, 64, 64, 0, 0, None) == fa.ERR_INVALID
     assert L.fa_kv_init(24, 1, fa.KV_F16, 2, 64, 64, 0, 0, None) == fa.ERR_INVALID   # misaligned
     assert L.fa_kv_init(16, 0, fa.KV_Q4_0, 2, 64, 64, 4, 256, None) == fa.OK         # no planes
+
+
+def test_chunk_noalloc_layout_and_tile_shape_validation(fa):
+    """Argument checks that return before any launch, and the plane layout and
+    tile shape in closed form (include/fa.h)."""
+    import ctypes
+    L = fa.lib()
+
+    def chunk(pos0=0, n=16, max_seq=32, wsb=1 << 30, q=16, lse=None):
+        return L.fa_prefill_chunk(q, 16, 16, 16, lse, pos0, n, 8, 2, 64, 0, 0, 0, max_seq, 0, 0,
+                                  16, wsb, None, None)
+    assert chunk(pos0=-1) == fa.ERR_INVALID
+    assert chunk(pos0=20, n=16) == fa.ERR_INVALID      # pos0 + n > max_seq
+    assert chunk(wsb=10) == fa.ERR_WORKSPACE
+    assert chunk(q=None) == fa.ERR_INVALID
+    assert chunk(lse=18) == fa.ERR_INVALID             # misaligned lse
+    assert chunk(n=0) == fa.OK                         # nothing to do
+
+    def noalloc(nslots=2, hd=256, max_seq=100, kps=256, cap=4, pos=16):
+        return L.fa_decode_noalloc(16, 16, 16, pos, nslots, 16, 2, hd, max_seq, 0, 0, 1, 4, 0,
+                                   kps, cap, 16, None)
+    assert noalloc(kps=0) == fa.ERR_INVALID
+    assert noalloc(cap=0) == fa.ERR_INVALID
+    assert noalloc(pos=None) == fa.ERR_INVALID
+    assert noalloc(hd=96) == fa.ERR_UNSUPPORTED
+    assert noalloc(nslots=0) == fa.OK
+    # partials beyond the library's fixed 8 MiB array
+    assert noalloc(nslots=4096, max_seq=1 << 20, cap=4096) == fa.ERR_WORKSPACE
+
+    vals = [ctypes.c_size_t() for _ in range(4)]
+    refs = [ctypes.byref(v) for v in vals]
+    # Q4_0, 2 kv heads, 1024 rows, head_dim 256: 144-byte rows; the sink block
+    # [2][8][256] fp16 after the body, the ring after the sinks (256-byte aligned)
+    assert L.fa_kv_plane_layout(1, 2, 1024, 256, *refs) == fa.OK
+    assert [v.value for v in vals] == [144, 0, 2 * 1024 * 144, 2 * 1024 * 144 + 2 * 8 * 256 * 2]
+    assert L.fa_kv_plane_layout(2, 2, 1024, 128, *refs) == fa.OK  # fp16: rows only
+    assert [v.value for v in vals[:2]] == [256, 0]
+    assert L.fa_kv_plane_layout(1, 2, 1024, 100, *refs) == fa.ERR_INVALID
+    bq, bk = ctypes.c_int(), ctypes.c_int()
+    assert L.fa_prefill_tile_shape(256, ctypes.byref(bq), ctypes.byref(bk)) == fa.OK
+    assert (bq.value, bk.value) == (128, 128)
+    assert L.fa_prefill_tile_shape(96, ctypes.byref(bq), ctypes.byref(bk)) == fa.ERR_UNSUPPORTED
