@@ -577,7 +577,7 @@ def main():
     e2e_serial = job_throughput(flops_step, max_over_ranks(statistics.mean(e2e_ms)), world) / 1e12
     e2e_pipe_ms = max_over_ranks(B.prefill_e2e_pipelined(S, args.warmup, args.steps))
     e2e_val = job_throughput(flops_step, e2e_pipe_ms, world) / 1e12
-    launches_per_step = 4  # append, stage Q, stage K and V, tensor-core kernel
+    launches_per_step = 3  # append, stage Q, K and V, tensor-core kernel
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

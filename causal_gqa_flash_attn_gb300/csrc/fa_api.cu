@@ -168,7 +168,8 @@ fa_status prefill_split(const float *q, const void *k, const void *v, float *out
     const int F = nk - FA_Q4_RING_ROWS > shadow_sink ? nk - FA_Q4_RING_ROWS : shadow_sink;
     cudaError_t e = fa::launch_stage_kv(static_cast<const uint8_t *>(k),
                                         static_cast<const uint8_t *>(v), kh2, vh2, nk, g,
-                                        shadow_sink, FA_Q4_RING_ROWS, s);
+                                        shadow_sink, FA_Q4_RING_ROWS, nullptr, nullptr, 0,
+                                        nullptr, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(ctr2, 0, sizeof(unsigned), s);
     fa::PrefillArgs a;
     a.qh = qh;
@@ -430,22 +431,22 @@ fa_status fa_prefill_chunk(const float *q, const void *k, const void *v, float *
     __half *kh = reinterpret_cast<__half *>(ws + w.k_off);
     __half *vh = reinterpret_cast<__half *>(ws + w.v_off);
     unsigned *ctr = reinterpret_cast<unsigned *>(ws + w.ctr_off);
-    cudaError_t e =
-        fa::launch_stage_q(q, qh, static_cast<size_t>(n) * n_q_heads * head_dim, ctr, s);
+    const size_t q_count = static_cast<size_t>(n) * n_q_heads * head_dim;
+    cudaError_t e = cudaSuccess;
     // An fp16 cache body is already the kernel's operand layout ([Hkv][rows]
     // [hd] binary16): the kernel's tensor maps read the planes in place.
     const bool direct = kv_fmt == FA_KV_F16;
     if (direct) {
         kh = reinterpret_cast<__half *>(static_cast<uint8_t *>(const_cast<void *>(k)) + g.body_off);
         vh = reinterpret_cast<__half *>(static_cast<uint8_t *>(const_cast<void *>(v)) + g.body_off);
+        e = fa::launch_stage_q(q, qh, q_count, ctr, s);
     } else {
-        // the split's far part reads sinks and Q4_0 rows (no ring); the other
-        // paths read what the shadow geometry gives every query
+        // one launch stages Q (and zeroes the work counter), K and V; the
+        // split's far part reads sinks and Q4_0 rows (no ring), the other
+        // paths what the shadow geometry gives every query
         const int sw_stage = split ? 0 : shadow_win;
-        if (e == cudaSuccess)
-            e = fa::launch_stage_kv(static_cast<const uint8_t *>(k),
-                                    static_cast<const uint8_t *>(v), kh, vh, nk, g, shadow_sink,
-                                    sw_stage, s);
+        e = fa::launch_stage_kv(static_cast<const uint8_t *>(k), static_cast<const uint8_t *>(v),
+                                kh, vh, nk, g, shadow_sink, sw_stage, q, qh, q_count, ctr, s);
     }
     if (e != cudaSuccess) return FA_ERR_CUDA;
     if (split) return prefill_split(q, k, v, out, lse, pos0, n, n_q_heads, n_kv_heads, head_dim,

@@ -53,10 +53,13 @@ cudaError_t launch_kv_append(const float *k_new, const float *v_new, uint8_t *k_
 // Converts q and zeroes *counter (the prefill kernel's work queue).
 cudaError_t launch_stage_q(const float *q, __half *qh, size_t count, unsigned *counter,
                            cudaStream_t stream);
-// Stages rows 0..n-1 of the K and the V plane into kdst and vdst in one launch.
+// Stages rows 0..n-1 of the K and the V plane into kdst and vdst in one launch;
+// when q is not null the same launch also does launch_stage_q's work (q_count
+// values of q into qh, *counter zeroed).
 cudaError_t launch_stage_kv(const uint8_t *kplane, const uint8_t *vplane, __half *kdst,
                             __half *vdst, int n, const PlaneGeom &g, int shadow_sink,
-                            int shadow_win, cudaStream_t stream);
+                            int shadow_win, const float *q, __half *qh, size_t q_count,
+                            unsigned *counter, cudaStream_t stream);
 
 // ---- prefill_tc.cu
 struct PrefillArgs {

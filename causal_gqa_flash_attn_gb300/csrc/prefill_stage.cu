@@ -24,9 +24,9 @@ namespace {
 
 constexpr int kThreads = 256;
 
-__global__ void __launch_bounds__(kThreads)
-    stage_q_kernel(const float4 *__restrict__ q, uint2 *__restrict__ qh, long long count4,
-                   unsigned *counter) {
+// Q fp32 -> fp16 over the blocks of one grid row; zeroes *counter.
+__device__ __forceinline__ void stage_q_rows(const float4 *__restrict__ q, uint2 *__restrict__ qh,
+                                             long long count4, unsigned *counter) {
     if (blockIdx.x == 0 && threadIdx.x == 0) *counter = 0u;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < count4;
          i += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -35,15 +35,37 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+__global__ void __launch_bounds__(kThreads)
+    stage_q_kernel(const float4 *__restrict__ q, uint2 *__restrict__ qh, long long count4,
+                   unsigned *counter) {
+    stage_q_rows(q, qh, count4, counter);
+}
+
+// Q staged in the same launch as K and V (when q is not null).
+struct QStage {
+    const float4 *q;
+    uint2 *qh;
+    long long count4;
+    unsigned *counter;
+};
+
 // The K and V planes are staged by one launch: blockIdx.y picks the plane.
+// When Q comes along it takes grid row 0 and K, V rows 1 and 2, so that the
+// blocks that run last write K and V: those tiles, read again and again by the
+// prefill, are then the freshest lines in L2.
 
 // fp32 cache rows -> fp16, one thread per 4 values.
 __global__ void __launch_bounds__(kThreads)
     stage_kv_f32_kernel(const uint8_t *__restrict__ kplane, const uint8_t *__restrict__ vplane,
                         uint2 *__restrict__ kdst, uint2 *__restrict__ vdst, int n, int n_kv,
-                        int hd, int max_seq, size_t body_off) {
-    const uint8_t *__restrict__ plane = blockIdx.y ? vplane : kplane;
-    uint2 *__restrict__ dst = blockIdx.y ? vdst : kdst;
+                        int hd, int max_seq, size_t body_off, QStage qs) {
+    const int prow = static_cast<int>(blockIdx.y) - (qs.q ? 1 : 0);
+    if (prow < 0) {
+        stage_q_rows(qs.q, qs.qh, qs.count4, qs.counter);
+        return;
+    }
+    const uint8_t *__restrict__ plane = prow ? vplane : kplane;
+    uint2 *__restrict__ dst = prow ? vdst : kdst;
     const int q4 = hd / 4;
     const long long total = static_cast<long long>(n_kv) * n * q4;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
@@ -62,9 +84,14 @@ __global__ void __launch_bounds__(kThreads)
 __global__ void __launch_bounds__(kThreads)
     stage_kv_fp8_kernel(const uint8_t *__restrict__ kplane, const uint8_t *__restrict__ vplane,
                         uint4 *__restrict__ kdst, uint4 *__restrict__ vdst, int n, int n_kv,
-                        int hd, int max_seq, size_t body_off, size_t scale_off) {
-    const uint8_t *__restrict__ plane = blockIdx.y ? vplane : kplane;
-    uint4 *__restrict__ dst = blockIdx.y ? vdst : kdst;
+                        int hd, int max_seq, size_t body_off, size_t scale_off, QStage qs) {
+    const int prow = static_cast<int>(blockIdx.y) - (qs.q ? 1 : 0);
+    if (prow < 0) {
+        stage_q_rows(qs.q, qs.qh, qs.count4, qs.counter);
+        return;
+    }
+    const uint8_t *__restrict__ plane = prow ? vplane : kplane;
+    uint4 *__restrict__ dst = prow ? vdst : kdst;
     const int q8 = hd / 8;
     const long long total = static_cast<long long>(n_kv) * n * q8;
     const float c = __ldg(reinterpret_cast<const float *>(plane + scale_off));
@@ -86,9 +113,14 @@ __global__ void __launch_bounds__(kThreads)
     stage_kv_q4_kernel(const uint8_t *__restrict__ kplane, const uint8_t *__restrict__ vplane,
                        uint4 *__restrict__ kdst, uint4 *__restrict__ vdst, int n, int n_kv,
                        int hd, int max_seq, size_t body_off, size_t row_bytes, size_t sink_off,
-                       size_t ring_off, int shadow_sink, int shadow_win) {
-    const uint8_t *__restrict__ plane = blockIdx.y ? vplane : kplane;
-    uint4 *__restrict__ dst = blockIdx.y ? vdst : kdst;
+                       size_t ring_off, int shadow_sink, int shadow_win, QStage qs) {
+    const int prow = static_cast<int>(blockIdx.y) - (qs.q ? 1 : 0);
+    if (prow < 0) {
+        stage_q_rows(qs.q, qs.qh, qs.count4, qs.counter);
+        return;
+    }
+    const uint8_t *__restrict__ plane = prow ? vplane : kplane;
+    uint4 *__restrict__ dst = prow ? vdst : kdst;
     const int nb = hd / kQ4Block;
     const long long total = static_cast<long long>(n_kv) * n * nb;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
@@ -157,25 +189,32 @@ cudaError_t launch_stage_q(const float *q, __half *qh, size_t count, unsigned *c
 
 cudaError_t launch_stage_kv(const uint8_t *kplane, const uint8_t *vplane, __half *kdst,
                             __half *vdst, int n, const PlaneGeom &g, int shadow_sink,
-                            int shadow_win, cudaStream_t stream) {
+                            int shadow_win, const float *q, __half *qh, size_t q_count,
+                            unsigned *counter, cudaStream_t stream) {
+    const QStage qs{reinterpret_cast<const float4 *>(q), reinterpret_cast<uint2 *>(qh),
+                    static_cast<long long>(q_count / 4), counter};
+    const unsigned rows = q ? 3u : 2u;
+    auto grid = [&](long long items) {
+        return dim3(grid_for(q && qs.count4 > items ? qs.count4 : items), rows);
+    };
     if (g.fmt == kFmtF32) {
         const long long items = static_cast<long long>(g.n_kv) * n * (g.hd / 4);
-        stage_kv_f32_kernel<<<dim3(grid_for(items), 2), kThreads, 0, stream>>>(
+        stage_kv_f32_kernel<<<grid(items), kThreads, 0, stream>>>(
             kplane, vplane, reinterpret_cast<uint2 *>(kdst), reinterpret_cast<uint2 *>(vdst), n,
-            g.n_kv, g.hd, g.max_seq, g.body_off);
+            g.n_kv, g.hd, g.max_seq, g.body_off, qs);
     } else if (g.fmt == kFmtFp8) {
         const long long items = static_cast<long long>(g.n_kv) * n * (g.hd / 8);
-        stage_kv_fp8_kernel<<<dim3(grid_for(items), 2), kThreads, 0, stream>>>(
+        stage_kv_fp8_kernel<<<grid(items), kThreads, 0, stream>>>(
             kplane, vplane, reinterpret_cast<uint4 *>(kdst), reinterpret_cast<uint4 *>(vdst), n,
-            g.n_kv, g.hd, g.max_seq, g.body_off, g.scale_off);
+            g.n_kv, g.hd, g.max_seq, g.body_off, g.scale_off, qs);
     } else if (g.fmt != kFmtQ4) {
         return cudaErrorInvalidValue;  // fp16 planes are read in place
     } else {
         const long long items = static_cast<long long>(g.n_kv) * n * (g.hd / kQ4Block);
-        stage_kv_q4_kernel<<<dim3(grid_for(items), 2), kThreads, 0, stream>>>(
+        stage_kv_q4_kernel<<<grid(items), kThreads, 0, stream>>>(
             kplane, vplane, reinterpret_cast<uint4 *>(kdst), reinterpret_cast<uint4 *>(vdst), n,
             g.n_kv, g.hd, g.max_seq, g.body_off, g.row_bytes, g.sink_off, g.ring_off,
-            shadow_sink, shadow_win);
+            shadow_sink, shadow_win, qs);
     }
     return cudaGetLastError();
 }
