@@ -428,6 +428,18 @@ def decode_kv_bytes(w):
     return w.nslots * w.n_kv_heads * per
 
 
+def append_q4_bytes(w):
+    """Bytes fa_kv_append must move to append all n rows of a Q4_0 workload:
+    the fp32 K and V rows read, their Q4_0 blocks written, and the fp16
+    mirrors of the shadow sink rows and of the ring's rows written."""
+    rows = w.n * w.n_kv_heads
+    read = 2 * rows * w.head_dim * 4
+    body = 2 * rows * (w.head_dim // 32 * 18)
+    mirrored = min(w.shadow_sink, w.n) + (min(256, w.n) if w.shadow_win > 0 else 0)
+    shadows = 2 * w.n_kv_heads * mirrored * w.head_dim * 2
+    return read + body + shadows
+
+
 # ---------------------------------------------------------- CPU baseline
 
 def oracle_prefill_sample(q, k, v, w, budget_s=12.0):
@@ -669,6 +681,29 @@ def main():
         del S
         torch.cuda.empty_cache()
 
+    # Q4_0 append alone: 8192 new rows x 2 kv heads x head_dim 256 of K and V
+    # quantised into Q4_0 blocks, with the fp16 mirrors of the 4 sink rows and
+    # of the 256 newest rows (the Q4_0 prefill workload's cache)
+    w = BY_NAME["prefill_q4_n8192_h16x2_d256_shadow4_256"]
+    S = B.prefill_setup(w)
+    abytes = append_q4_bytes(w)
+
+    def append_step():
+        B.fa.kv_append(S["k"], S["v"], S["kp"], S["vp"], S["pos0"], n_kv_heads=w.n_kv_heads,
+                       head_dim=w.head_dim, max_seq=w.n, kv_fmt=S["code"],
+                       shadow_sink=w.shadow_sink, shadow_win=w.shadow_win)
+    sm, _ = B.timed_steps(append_step, args.warmup, args.steps, kernel_events=False)
+    a = abytes / (statistics.mean(sm) * 1e-3) / 1e9
+    extra["append_q4_n8192_h2_d256_shadow4_256"] = {
+        "value": a, "unit": "GB/s", "ms_per_step": statistics.mean(sm),
+        "bytes_per_step": abytes, "step": "fa_kv_append (one launch)",
+        "roofline": {"kernel": "kv_append_q4_kernel", "bound": "hbm", "achieved": a,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": a / peaks["hbm_gbs"],
+                     "traffic": profiled_traffic("kv_append_q4_kernel", src_hash("kv_append.cu")),
+                     "kernel_ms": statistics.mean(sm)}}
+    del S
+    torch.cuda.empty_cache()
+
     if not args.no_decode:
         # merge of two attention states (fp32 outputs [T][H][D], lses [H][T]):
         # the context-chunk + new-tokens combination of chunked prefill
@@ -721,6 +756,10 @@ def main():
             "clocks": clk.summary(),
             "wall_s_timed": wall,
             "workloads": extra,
+            "workload_fracs": {k: {"value": round(v["value"], 1), "unit": v["unit"],
+                                   "kernel": v["roofline"]["kernel"],
+                                   "frac": round(v["roofline"]["frac"], 3)}
+                               for k, v in extra.items()},
         }))
     if world > 1:
         torch.distributed.destroy_process_group()

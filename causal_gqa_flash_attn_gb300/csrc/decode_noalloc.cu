@@ -28,25 +28,35 @@ __device__ __align__(256) uint8_t g_fa_decode_scratch[kFaDecodeScratchBytes];
 
 constexpr int kMaxDevices = 64;
 
-// Device address of g_fa_decode_scratch, looked up once per device with that
-// device current. In host code the symbol itself is only a host-side stand-in.
+// Device address of g_fa_decode_scratch, looked up per device with that
+// device current. In host code the symbol itself is only a host-side
+// stand-in. A successful lookup is kept for the life of the process; a failed
+// one (for instance a first call made during a stream capture) is not: its
+// error is taken off the runtime's last-error slot, so that it cannot be
+// reported by a later unrelated check, and the next call looks again.
 struct ScratchSlot {
-    std::once_flag once;
     void *ptr = nullptr;
-    cudaError_t status = cudaSuccess;
 };
 ScratchSlot g_scratch[kMaxDevices];
+std::mutex g_scratch_mutex;
 
 void *scratch_ptr() {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
     ScratchSlot *s = &g_scratch[dev];
-    std::call_once(s->once, [s]() {
+    if (!s->ptr) {
         void *p = nullptr;
-        s->status = cudaGetSymbolAddress(&p, g_fa_decode_scratch);
-        if (s->status == cudaSuccess) s->ptr = p;
-    });
-    return s->status == cudaSuccess ? s->ptr : nullptr;
+        if (cudaGetSymbolAddress(&p, g_fa_decode_scratch) == cudaSuccess) {
+            s->ptr = p;
+        } else {
+            cudaGetLastError();  // leave no sticky error behind; retry next call
+        }
+    }
+    return s->ptr;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

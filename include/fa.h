@@ -354,7 +354,9 @@ fa_status fa_decode_combine(const void *workspace, float *out, int nslots, int n
  * that overlap on the GPU (other streams, other host threads on the device)
  * race on it, so serialise them. The first call on each device looks up the
  * array's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture. */
+ * make that first call before any stream capture. If that lookup fails the
+ * call returns FA_ERR_CUDA, clears the runtime's last error, and the next
+ * call looks again. */
 fa_status fa_decode_noalloc(const float *q, const void *k_planes, const void *v_planes,
                             const int32_t *pos, int nslots, int n_q_heads, int n_kv_heads,
                             int head_dim, int max_seq, int sink, int win, int kv_fmt,

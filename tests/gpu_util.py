@@ -2,6 +2,9 @@
 binding (which calls the C ABI) and measure its distance to the oracle."""
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -113,8 +116,10 @@ def build_cache(k, v, *, kv_fmt, shadow_sink=0, shadow_win=0, max_seq=None, pos0
 
 
 def run_prefill(q, k, v, *, kv_fmt, sink, win, shadow_sink=0, shadow_win=0, tile_map=False,
-                max_seq=None, k_scale=1.0, v_scale=1.0):
-    """Append then prefill on the GPU; returns out (numpy) and the tile map."""
+                max_seq=None, k_scale=1.0, v_scale=1.0, lse=False):
+    """Append then prefill on the GPU (fa_prefill, or fa_prefill_lse with
+    lse); returns out (numpy), then lse [Hq][n] with lse, then the tile map
+    with tile_map."""
     m = fa()
     n, hq, hd = q.shape
     hkv = k.shape[1]
@@ -130,16 +135,66 @@ def run_prefill(q, k, v, *, kv_fmt, sink, win, shadow_sink=0, shadow_win=0, tile
     if tile_map:
         bq, bk = m.prefill_tile_shape(hd)
         tm = guarded((-(-n // bq)) * (-(-n // bk)), torch.uint8, fill=0)
+    lo = guarded((hq, n), torch.float32, fill=float("nan")) if lse else None
     m.prefill(qd, kp, vp, out, n, hq, hkv, hd, sink, win, fmt_code(kv_fmt), max_seq=max_seq,
-              shadow_sink=shadow_sink, shadow_win=shadow_win, workspace=ws, tile_map=tm)
+              shadow_sink=shadow_sink, shadow_win=shadow_win, workspace=ws, tile_map=tm, lse=lo)
     st = m.get_device_error()
     assert st == m.OK, m.status_string(st)
     check_guards(("out", out), ("workspace", ws), ("k planes", kp), ("v planes", vp),
-                 *((("tile map", tm),) if tm is not None else ()))
-    res = out.cpu().numpy()
+                 *((("tile map", tm),) if tm is not None else ()),
+                 *((("lse", lo),) if lo is not None else ()))
+    res = [out.cpu().numpy()]
+    if lse:
+        res.append(lo.cpu().numpy())
     if tile_map:
-        return res, tm.cpu().numpy().reshape(-(-n // bq), -(-n // bk))
-    return res
+        res.append(tm.cpu().numpy().reshape(-(-n // bq), -(-n // bk)))
+    return res[0] if len(res) == 1 else tuple(res)
+
+
+def run_chunk(q, k, v, pos0, *, hq, hkv, hd, sink, win, kv_fmt, shadow, want_map=False):
+    """A cache filled as a caller continuing a sequence fills it (the context
+    rows 0..pos0-1 in one append, the chunk's rows in a second), then
+    fa_prefill_chunk with lse; returns out, lse [Hq][n] and the tile map."""
+    m = fa()
+    n = q.shape[0]
+    L = pos0 + n
+    code = fmt_code(kv_fmt)
+    kp = m.alloc_planes(1, code, hkv, L, hd)
+    vp = m.alloc_planes(1, code, hkv, L, hd)
+    ss, sw = shadow
+    for lo, hi in ((0, pos0), (pos0, L)):  # context, then the chunk
+        if hi > lo:
+            m.kv_append(torch.from_numpy(np.ascontiguousarray(k[None, lo:hi])).cuda(),
+                        torch.from_numpy(np.ascontiguousarray(v[None, lo:hi])).cuda(), kp, vp,
+                        torch.tensor([lo], dtype=torch.int32, device="cuda"), n_kv_heads=hkv,
+                        head_dim=hd, max_seq=L, kv_fmt=code, shadow_sink=ss, shadow_win=sw)
+    ws = guarded(m.prefill_chunk_workspace_bytes(pos0, n, hq, hkv, hd, kv_fmt=code,
+                                                 shadow_win=sw),
+                 torch.uint8, fill_byte=POISON_BYTE)
+    out = guarded((n, hq, hd), torch.float32, fill=float("nan"))
+    lse = guarded((hq, n), torch.float32, fill=float("nan"))
+    tm = None
+    if want_map:
+        bq, bk = m.prefill_tile_shape(hd)
+        tm = guarded((-(-n // bq), -(-L // bk)), torch.uint8, fill=0)
+    m.prefill_chunk(torch.from_numpy(np.ascontiguousarray(q)).cuda(), kp, vp, out, pos0, n, hq,
+                    hkv, hd, sink, win, code, max_seq=L, shadow_sink=ss, shadow_win=sw,
+                    workspace=ws, tile_map=tm, lse=lse)
+    st = m.get_device_error()
+    assert st == m.OK, m.status_string(st)
+    check_guards(("out", out), ("lse", lse), ("workspace", ws),
+                 *((("tile map", tm),) if tm is not None else ()))
+    return out.cpu().numpy(), lse.cpu().numpy(), (tm.cpu().numpy() if want_map else None)
+
+
+def record_parity(test, **values):
+    """Append one JSON line of measured errors to the file named by the
+    FA_PARITY_LOG environment variable (nothing when it is unset)."""
+    path = os.environ.get("FA_PARITY_LOG")
+    if not path:
+        return
+    with open(path, "a") as f:
+        f.write(json.dumps({"test": test, **values}) + "\n")
 
 
 def run_decode(q, kp, vp, pos, *, hkv, hd, max_seq, sink, win, kv_fmt, shadow_sink=0,

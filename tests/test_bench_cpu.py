@@ -51,6 +51,17 @@ def test_decode_kv_bytes(bench):
     assert bench.decode_kv_bytes(w8) == 32 * 2 * 32768 * 2 * 256
 
 
+def test_append_q4_bytes(bench, oracle_mod):
+    import numpy as np
+    from workloads import BY_NAME
+    w = BY_NAME["prefill_q4_n8192_h16x2_d256_shadow4_256"]
+    rows = np.zeros((w.n, w.n_kv_heads, w.head_dim), np.float32)
+    read = 2 * rows.nbytes                                  # K and V fp32 rows
+    body = 2 * oracle_mod.q4_encode(rows).nbytes            # their Q4_0 blocks
+    shadows = 2 * (4 + 256) * w.n_kv_heads * w.head_dim * 2  # fp16 sinks and ring
+    assert bench.append_q4_bytes(w) == read + body + shadows == 38805504
+
+
 def test_job_throughput_counts_every_rank(bench):
     # two replicas each doing 1e12 flop in 1 ms: 2e15 flop/s for the job
     assert bench.job_throughput(1e12, 1.0, 2) == pytest.approx(2e15)

@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import assert_close, fa, fmt_code
+from gpu_util import assert_close, fa, fmt_code, run_chunk
 from workloads import prefill_inputs
 
 pytestmark = pytest.mark.gpu
@@ -36,37 +36,6 @@ CHUNK_CASES = [
     (64, 700, 4, 1, 128, 9, 3, "q4_0", (4, 17)),
     (300, 1, 8, 2, 64, 0, 0, "q4_0", (4, 128)),
 ]
-
-
-def run_chunk(q, k, v, pos0, *, hq, hkv, hd, sink, win, kv_fmt, shadow, want_map=False):
-    m = fa()
-    n = q.shape[0]
-    L = pos0 + n
-    code = fmt_code(kv_fmt)
-    kp = m.alloc_planes(1, code, hkv, L, hd)
-    vp = m.alloc_planes(1, code, hkv, L, hd)
-    ss, sw = shadow
-    for lo, hi in ((0, pos0), (pos0, L)):  # context, then the chunk
-        if hi > lo:
-            m.kv_append(torch.from_numpy(np.ascontiguousarray(k[None, lo:hi])).cuda(),
-                        torch.from_numpy(np.ascontiguousarray(v[None, lo:hi])).cuda(), kp, vp,
-                        torch.tensor([lo], dtype=torch.int32, device="cuda"), n_kv_heads=hkv,
-                        head_dim=hd, max_seq=L, kv_fmt=code, shadow_sink=ss, shadow_win=sw)
-    ws = torch.empty(m.prefill_chunk_workspace_bytes(pos0, n, hq, hkv, hd, kv_fmt=code,
-                                                     shadow_win=sw),
-                     dtype=torch.uint8, device="cuda")
-    out = torch.full((n, hq, hd), float("nan"), dtype=torch.float32, device="cuda")
-    lse = torch.full((hq, n), float("nan"), dtype=torch.float32, device="cuda")
-    tm = None
-    if want_map:
-        bq, bk = m.prefill_tile_shape(hd)
-        tm = torch.zeros(-(-n // bq), -(-L // bk), dtype=torch.uint8, device="cuda")
-    m.prefill_chunk(torch.from_numpy(np.ascontiguousarray(q)).cuda(), kp, vp, out, pos0, n, hq,
-                    hkv, hd, sink, win, code, max_seq=L, shadow_sink=ss, shadow_win=sw,
-                    workspace=ws, tile_map=tm, lse=lse)
-    st = m.get_device_error()
-    assert st == m.OK, m.status_string(st)
-    return out.cpu().numpy(), lse.cpu().numpy(), (tm.cpu().numpy() if want_map else None)
 
 
 @pytest.mark.parametrize("case", CHUNK_CASES, ids=lambda c: "-".join(map(str, c)))

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 from gpu_util import assert_close, build_cache, fa, fmt_code
-from workloads import BY_NAME, prefill_inputs, workload_inputs
+from workloads import prefill_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -61,21 +61,6 @@ def test_prefill_lse_small(oracle_mod, case):
     assert_close(out, want, str(case))
     err = np.max(np.abs(lse - want_lse.T))
     assert np.all(np.isfinite(lse)) and err <= LSE_ATOL, f"{case}: lse max-abs {err:.3g}"
-
-
-def test_prefill_lse_workload_sampled(oracle_mod):
-    """8192 tokens, full causal, fp32 KV: lse of sampled rows, the
-    configuration the benchmark times."""
-    w = BY_NAME["prefill_f32_n8192_h16x2_d256"]
-    q, k, v = workload_inputs(w)
-    out, lse = run_prefill_lse(q, k, v, hq=w.n_q_heads, hkv=w.n_kv_heads, hd=w.head_dim,
-                               sink=w.sink, win=w.win, kv_fmt=w.kv_fmt)
-    rows = np.array([0, 1, 127, 128, 4095, 8190, 8191], np.int32)
-    want, want_lse = oracle_mod.prefill(q, k, v, kv_fmt=w.kv_fmt, sink=w.sink, win=w.win,
-                                        rows=rows, with_lse=True)
-    assert_close(out[rows], want, "rows")
-    err = np.max(np.abs(lse[:, rows] - want_lse.T))
-    assert err <= LSE_ATOL, f"lse max-abs {err:.3g}"
 
 
 def run_merge(po, pl, so, sl, with_context=-1, want_lse=True):
