@@ -461,11 +461,6 @@ constexpr int kPRing = 2;      // P records in flight per pair
 #ifndef FA_Q4_MIN_BLOCKS
 #define FA_Q4_MIN_BLOCKS 2
 #endif
-// Blocks per SM the Q4_0 work split aims at (runs of splits per block are
-// sized so that the grid has about this many blocks per SM).
-#ifndef FA_Q4_TARGET_PER_SM
-#define FA_Q4_TARGET_PER_SM 4
-#endif
 // Unroll factor (1 or 2) of the PV warp's loop over a tile's two 16-key
 // halves: 2 interleaves the halves' dependency chains, 1 keeps the registers
 // and the code small. (The QK warp walks the blocks outermost and both halves
@@ -589,9 +584,48 @@ __device__ __forceinline__ void build_q_frags(const DecodeParams &P, size_t head
     }
 }
 
+// The 32-key tiles of one (slot, kv head) that the Q4_0 path loads, in
+// order: tile kt covers keys [32 kt, 32 kt + 32) clipped to [0, p]. They are
+// two runs, [a0, a0 + na) and [b0, b0 + nb): with a window, the tiles holding
+// attended sinks and then the window's tiles; without one, a single run.
+// Tiles whose every key is an fp16 shadow (sink rows below shadow_sink,
+// recent rows above p - shadow_win) are left out: the shadow entry reads those.
+struct Q4Tiles {
+    int a0, na, b0, nb;
+    __device__ __forceinline__ int count() const { return na + nb; }
+    __device__ __forceinline__ int kt(int i) const { return i < na ? a0 + i : b0 + (i - na); }
+};
+
+__device__ __forceinline__ Q4Tiles q4_tiles(const DecodeParams &P, int p) {
+    Q4Tiles T{0, 0, 0, 0};
+    if (p < 0 || p >= P.max_seq || p < P.shadow_sink) return T;
+    const int nt = p / kTileKeys + 1;       // tiles holding keys 0 .. p
+    const int lo = P.shadow_sink / kTileKeys;  // first tile with a key >= shadow_sink
+    int hi = nt;
+    if (P.shadow_win > 0) {
+        const int last = p - P.shadow_win;  // the largest key read from the Q4_0 rows
+        hi = last >= 0 ? min(hi, last / kTileKeys + 1) : 0;
+    }
+    if (P.win <= 0) {
+        T.a0 = lo;
+        T.na = max(0, hi - lo);
+        return T;
+    }
+    // attended: sinks [0, min(sink, p + 1)) and the window [p - win + 1, p]
+    const int ns = (min(P.sink, p + 1) + kTileKeys - 1) / kTileKeys;
+    const int w0 = max(max(0, p - P.win + 1) / kTileKeys, ns);
+    T.a0 = lo;
+    T.na = max(0, min(ns, hi) - lo);
+    T.b0 = max(w0, lo);
+    T.nb = max(0, hi - T.b0);
+    return T;
+}
+
+// One piece of work: tiles j0 .. j1-1 of (slot u, kv head g) in the order of
+// q4_tiles, written as partial entry e.
 template <int HD>
 __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, int e, int g,
-                                        int u, int p, int k_lo, int k_hi) {
+                                        int u, int p, const Q4Tiles &tl, int j0, int j1) {
     using C = Q4Cfg<HD>;
     constexpr int NB = C::NB, MT = C::MT, ROWB = C::ROWB, NK = C::NK, NV = C::NV;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -624,33 +658,14 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
     __syncthreads();
 
     const int ss = P.shadow_sink, sw = P.shadow_win;
-    const int ntiles = (k_hi - k_lo + kTileKeys - 1) / kTileKeys;
-    // A tile is worth loading if some key in it is visible and not a shadow key.
-    auto tile_ok = [&](int i) -> bool {
-        const int t0 = k_lo + kTileKeys * i;
-        const int t1 = min(k_hi, t0 + kTileKeys) - 1;
-        if (P.win > 0 && !(t0 < P.sink || t1 >= p - P.win + 1)) return false;
-        if (t1 < ss) return false;
-        if (sw > 0 && t0 > p - sw) return false;
-        return true;
-    };
-    // With no window and no shadow window the tiles worth loading are one run:
-    // every tile from the first whose keys reach past the shadow sinks. The
-    // next one at or after i in this pair's sequence (i, i + kPairs, ...) is
-    // then found without testing tiles one by one.
-    const bool one_run = P.win <= 0 && sw <= 0;
-    const int first_ok = k_hi <= ss ? ntiles : max(0, (ss - k_lo) / kTileKeys);
-    auto next_tile = [&](int i) -> int {
-        if (one_run)
-            return i >= first_ok ? i : i + (first_ok - i + kPairs - 1) / kPairs * kPairs;
-        while (i < ntiles && !tile_ok(i)) i += kPairs;
-        return i;
-    };
+    const int ntiles = j1 - j0;  // sequence index i is tile tl.kt(j0 + i)
+    const int k_end = p + 1;     // keys past p are never read
+    auto tile_key0 = [&](int i) -> int { return kTileKeys * tl.kt(j0 + i); };
     bool ok = true;
     // one bulk copy of tile i's rows (rounded up to 16 bytes) into dst
     auto issue = [&](const uint8_t *body, int i, uint8_t *dst, uint64_t *bar) {
-        const int t0 = k_lo + kTileKeys * i;
-        const int nk = min(kTileKeys, k_hi - t0);
+        const int t0 = tile_key0(i);
+        const int nk = min(kTileKeys, k_end - t0);
         const uint32_t bytes = (static_cast<uint32_t>(nk * ROWB) + 15u) & ~15u;
         mbar_arrive_expect_tx(bar, bytes);
         bulk_copy_g2s(dst, body + static_cast<size_t>(t0) * ROWB, bytes, bar);
@@ -674,20 +689,20 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
         float mu0 = -INFINITY, mu1 = -INFINITY, mt0 = -INFINITY, mt1 = -INFINITY;
         float ls0 = 0.0f, ls1 = 0.0f;
         // Prologue: the first NK K tiles (the PV warp copies the V tiles).
-        int kt = next_tile(pair);  // next tile index to copy
-        int kn = 0;                // copies issued so far
+        int kt = pair;  // next tile index to copy
+        int kn = 0;     // copies issued so far
         for (; kn < NK && kt < ntiles; ++kn) {
             if (lane == 0) issue(kbody, kt, pbase + C::K_OFF + kn * C::TILE_ALLOC, &kfull[kn]);
-            kt = next_tile(kt + kPairs);
+            kt += kPairs;
         }
         const uint32_t magic = opaque(kMagic);
         int seq = 0;  // position of the tile in this pair's sequence
-        for (int i = next_tile(pair); i < ntiles; i = next_tile(i + kPairs), ++seq) {
+        for (int i = pair; i < ntiles; i += kPairs, ++seq) {
             const int s = seq % NK;
             ok = __all_sync(0xffffffffu, mbar_wait(&kfull[s], (seq / NK) & 1, abort, P.err));
             if (!ok) break;
             const uint8_t *Ks = pbase + C::K_OFF + s * C::TILE_ALLOC;
-            const int t0 = k_lo + kTileKeys * i;
+            const int t0 = tile_key0(i);
             // ---- scores: half h2 holds keys t0 + 16 h2 + {r, r+8}; the
             // block's Q fragments and biases are read once for both halves
             float sc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
@@ -744,12 +759,12 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
             __syncwarp();
             if (kt < ntiles) {
                 if (lane == 0) issue(kbody, kt, pbase + C::K_OFF + s * C::TILE_ALLOC, &kfull[s]);
-                kt = next_tile(kt + kPairs);
+                kt += kPairs;
                 ++kn;
             }
             // ---- mask and fold: sv[hh][2 h2 + half] is key t0 + 16 h2 + r + 8 half.
             const int t1 = t0 + kTileKeys - 1;
-            const bool whole = t1 < k_hi && t0 >= ss && (sw <= 0 || t1 <= p - sw) &&
+            const bool whole = t1 < k_end && t0 >= ss && (sw <= 0 || t1 <= p - sw) &&
                                (P.win <= 0 || t0 >= p - P.win + 1);
             float sv[2][4], pv[2][4];
 #pragma unroll
@@ -757,7 +772,7 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     const int key = t0 + 16 * h2 + r + 8 * half;
-                    const bool vis = whole || (key < k_hi && key_visible(p, key, P.sink, P.win) &&
+                    const bool vis = whole || (key < k_end && key_visible(p, key, P.sink, P.win) &&
                                                !(key < ss || (sw > 0 && key > p - sw)));
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh)
@@ -825,11 +840,11 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
         // as soon as it has finished the tile in it (NV tiles ahead).
         const uint8_t *vbody = P.v_planes + static_cast<size_t>(u) * P.plane_bytes + P.body_off +
                                static_cast<size_t>(g) * P.max_seq * ROWB;
-        int vt = next_tile(pair);  // next tile index to copy
-        int vn = 0;                // copies issued so far
+        int vt = pair;  // next tile index to copy
+        int vn = 0;     // copies issued so far
         for (; vn < NV && vt < ntiles; ++vn) {
             if (lane == 0) issue(vbody, vt, pbase + C::V_OFF + vn * C::TILE_ALLOC, &vfull[vn]);
-            vt = next_tile(vt + kPairs);
+            vt += kPairs;
         }
         for (int seq = 0;; ++seq) {
             const int ps = seq % kPRing;
@@ -855,7 +870,7 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
                 }
             }
             uint8_t *Vs = pbase + C::V_OFF + s * C::TILE_ALLOC;
-            const int nk = k_hi - (k_lo + kTileKeys * static_cast<int>(w1.z));
+            const int nk = k_end - tile_key0(static_cast<int>(w1.z));
             if (nk < kTileKeys) {
                 // Rows past the range hold bytes of earlier tiles, bytes the copy
                 // rounded up into, or nothing written yet. Their P is 0; zero
@@ -918,7 +933,7 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
                     fence_proxy_async_smem();  // those reads come before the copy's writes
                     issue(vbody, vt, Vs, &vfull[s]);
                 }
-                vt = next_tile(vt + kPairs);
+                vt += kPairs;
                 ++vn;
             }
         }
@@ -934,30 +949,172 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
     merge_finish<HD>(P, dsmem, head0, G, e);
 }
 
+// Stream-K work split of the Q4_0 path. The loaded tiles of all (slot, kv
+// head) pairs, pair after pair, are cut into equal runs of C tiles, one run
+// per body block, so that every block streams the same number of bytes and
+// none waits for a straggler wave. A block writes one partial per pair piece
+// it covers, as entry (block - the block holding the pair's first tile); the
+// block holding a pair's last piece marks the pair's later body entries empty.
+// Entry Eb of every head is the fp16-shadow entry when the cache has shadows.
+struct Q4Job {
+    long long T;  // tiles of all pairs
+    long long C;  // tiles per body block
+    int Eb;       // body entries per head
+    int E;        // entries per head (Eb, plus the shadow entry)
+};
+
+// Warp-wide (every lane gets the same result). nb: body blocks.
+__device__ __forceinline__ Q4Job q4_job(const DecodeParams &P, int nb) {
+    const int lane = threadIdx.x & 31;
+    long long T = 0;
+    int maxt = 0;
+    for (int u0 = 0; u0 < P.nslots; u0 += 32) {
+        const int u = u0 + lane;
+        const int nt = u < P.nslots ? q4_tiles(P, P.pos[u]).count() : 0;
+        long long sum = nt;
+        int mx = nt;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        }
+        T += sum * P.Hkv;
+        maxt = max(maxt, mx);
+    }
+    const int shadow = (P.shadow_sink > 0 || P.shadow_win > 0) ? 1 : 0;
+    const int sb = P.stride - shadow;  // body entries available (>= 2)
+    Q4Job J;
+    J.T = T;
+    J.C = nb > 0 ? (T + nb - 1) / nb : T;
+    // at most sb pieces per pair: C > (maxt - 1) / (sb - 1)
+    const long long cmin = maxt > 0 ? (maxt - 1) / (sb - 1) + 1 : 1;
+    if (J.C < cmin) J.C = cmin;
+    J.Eb = maxt > 0 ? static_cast<int>(min(static_cast<long long>(sb), (maxt - 1) / J.C + 2)) : 1;
+    J.E = J.Eb + shadow;
+    return J;
+}
+
+// Entries [e0, e1) of the G heads from head0 on: empty (m = -inf, l = 0).
+__device__ __forceinline__ void write_empty_range(const DecodeParams &P, size_t head0, int G,
+                                                  int e0, int e1) {
+    for (int i = threadIdx.x; i < G * (e1 - e0); i += blockDim.x) {
+        const size_t idx = (head0 + i % G) * P.stride + e0 + i / G;
+        P.ws_m[idx] = -INFINITY;
+        P.ws_l[idx] = 0.0f;
+    }
+}
+
+// Blocks [0, nslots * Hkv) are the pairs' auxiliary blocks: the fp16-shadow
+// entry, the empty entries of a pair with no Q4_0 tile, and the report of a
+// position out of range. The blocks after them are the body blocks.
 template <int HD>
 __global__ void __launch_bounds__(2 * kPairs * 32, FA_Q4_MIN_BLOCKS)
     decode_q4_kernel(const DecodeParams P) {
     extern __shared__ __align__(128) uint8_t dsmem[];
-    const int e = blockIdx.x, g = blockIdx.y, u = blockIdx.z;
+    __shared__ Q4Job sjob;
+    __shared__ long long sloc[3];  // first pair's tile base, slot, kv head of the block's run
     const int G = P.Hq / P.Hkv;
-    write_header(P, HD);
-    const int p = P.pos[u];
-    const size_t head0 = static_cast<size_t>(u) * P.Hq + static_cast<size_t>(g) * G;
-    if (p < 0 || p >= P.max_seq) {
-        if (threadIdx.x == 0 && e == 0 && g == 0) flag_error(P.err, FA_ERRBIT_DEVICE);
-        write_empty(P, head0, G, e);
+    const int n_aux = P.nslots * P.Hkv;
+    const int nb = static_cast<int>(gridDim.x) - n_aux;
+    if (threadIdx.x < 32) {
+        const Q4Job J = q4_job(P, nb);
+        if (threadIdx.x == 0) {
+            sjob = J;
+            if (blockIdx.x == 0) {
+                P.ws_header[0] = kDecodeMagic;
+                P.ws_header[1] = static_cast<uint32_t>(P.nslots);
+                P.ws_header[2] = static_cast<uint32_t>(P.Hq);
+                P.ws_header[3] = static_cast<uint32_t>(HD);
+                P.ws_header[4] = static_cast<uint32_t>(J.E);
+            }
+        }
+    }
+    __syncthreads();
+    const Q4Job J = sjob;
+
+    if (static_cast<int>(blockIdx.x) < n_aux) {
+        // ---------------------------------------------------- auxiliary block
+        const int u = blockIdx.x / P.Hkv, g = blockIdx.x % P.Hkv;
+        const size_t head0 = static_cast<size_t>(u) * P.Hq + static_cast<size_t>(g) * G;
+        const int p = P.pos[u];
+        if (p < 0 || p >= P.max_seq) {
+            if (threadIdx.x == 0 && g == 0) flag_error(P.err, FA_ERRBIT_DEVICE);
+            write_empty_range(P, head0, G, 0, J.E);
+            return;
+        }
+        if (q4_tiles(P, p).count() == 0) write_empty_range(P, head0, G, 0, J.Eb);
+        if (J.E > J.Eb) shadow_entry<HD, 1>(P, dsmem, J.Eb, g, u, p);
         return;
     }
-    if (e == P.shadow_entry) {
-        shadow_entry<HD, 1>(P, dsmem, e, g, u, p);
-        return;
+
+    // ------------------------------------------------------------ body block
+    const long long bid = static_cast<long long>(blockIdx.x) - n_aux;
+    const long long T0 = bid * J.C;
+    const long long T1 = min(J.T, T0 + J.C);
+    if (T0 >= T1) return;
+    if (threadIdx.x < 32) {
+        // the pair holding tile T0: scan the slots' tile counts
+        const int lane = threadIdx.x;
+        long long base = 0, slot_base = 0;
+        int u_hit = -1;
+        for (int u0 = 0; u0 < P.nslots && u_hit < 0; u0 += 32) {
+            const int uu = u0 + lane;
+            const long long cnt =
+                uu < P.nslots ? static_cast<long long>(q4_tiles(P, P.pos[uu]).count()) * P.Hkv : 0;
+            long long inc = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const long long y = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += y;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, base + inc > T0);
+            if (hit) {
+                const int L = __ffs(hit) - 1;
+                u_hit = u0 + L;
+                slot_base = base + __shfl_sync(0xffffffffu, inc - cnt, L);
+            } else {
+                base += __shfl_sync(0xffffffffu, inc, 31);
+            }
+        }
+        if (lane == 0) {
+            sloc[0] = slot_base;
+            sloc[1] = u_hit;
+        }
     }
-    int k_lo, k_hi;
-    if (!entry_range(P, e, p, &k_lo, &k_hi)) {
-        write_empty(P, head0, G, e);
-        return;
+    __syncthreads();
+    int u = static_cast<int>(sloc[1]);
+    if (u < 0) return;  // unreachable: T0 < T
+    int p = P.pos[u];
+    Q4Tiles tl = q4_tiles(P, p);
+    const long long local = T0 - sloc[0];
+    int g = static_cast<int>(local / tl.count());
+    int j = static_cast<int>(local % tl.count());
+    long long A = sloc[0] + static_cast<long long>(g) * tl.count();  // the pair's first tile
+    volatile int *abort = reinterpret_cast<volatile int *>(
+        dsmem + Q4Cfg<HD>::BAR_OFF + kPairs * Q4Cfg<HD>::BARS_PER_PAIR * 8);
+    for (long long Tc = T0; Tc < T1;) {
+        const int cnt = tl.count();
+        const int j1 = static_cast<int>(min(static_cast<long long>(cnt), j + (T1 - Tc)));
+        const int e = static_cast<int>(bid - A / J.C);
+        q4_body<HD>(P, dsmem, e, g, u, p, tl, j, j1);
+        const size_t head0 = static_cast<size_t>(u) * P.Hq + static_cast<size_t>(g) * G;
+        if (j1 == cnt) write_empty_range(P, head0, G, e + 1, J.Eb);
+        Tc += j1 - j;
+        __syncthreads();  // the next piece re-initialises the shared state
+        if (*abort) return;
+        if (Tc >= T1) break;
+        // the next pair with tiles
+        A = Tc;
+        j = 0;
+        do {
+            if (++g == P.Hkv) {
+                g = 0;
+                ++u;
+                p = P.pos[u];
+                tl = q4_tiles(P, p);
+            }
+        } while (tl.count() == 0);
     }
-    q4_body<HD>(P, dsmem, e, g, u, p, k_lo, k_hi);
 }
 
 // One warp per (slot, q head). The lanes take the entries 32 at a time to
@@ -1053,8 +1210,12 @@ cudaError_t launch_q4(const DecodeParams &P, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(decode_q4_kernel<HD>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid(P.entries, P.Hkv, P.nslots);
-    decode_q4_kernel<HD><<<grid, 2 * kPairs * 32, C::SMEM, stream>>>(P);
+    // one auxiliary block per (slot, kv head), then the body blocks: as many
+    // as stay resident together (a single wave)
+    const long long aux = static_cast<long long>(P.nslots) * P.Hkv;
+    const long long blocks = aux + static_cast<long long>(FA_Q4_MIN_BLOCKS) * device_sm_count();
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    decode_q4_kernel<HD><<<static_cast<unsigned>(blocks), 2 * kPairs * 32, C::SMEM, stream>>>(P);
     return cudaGetLastError();
 }
 
@@ -1077,19 +1238,26 @@ DecodeShape decode_shape(int nslots, int n_q_heads, int n_kv_heads, int kv_fmt, 
         d.entries = max_splits + 1;
         return d;
     }
-    // Blocks to aim at: the Q4_0 path keeps 2 blocks per SM, so 4 per SM is
-    // about two waves (measured at 32 slots x 32768 keys: 160 us against 163 us
-    // at 8 per SM, 195 us at 2, with fewer partials for the combine); the
-    // generic path, 4 per SM.
+    // The Q4_0 kernel cuts its work itself (stream-K) and needs two body
+    // entries per head besides the shadow entry.
+    const int shadow = (shadow_sink > 0 || shadow_win > 0) ? 1 : 0;
+    if (d.fast && max_splits + 1 < 2 + shadow) d.fast = false;
+    if (d.fast) {
+        d.splits_per_cta = 1;
+        d.body_entries = max_splits + 1 - shadow;
+        d.shadow_entry = -1;  // decided in the kernel (entry Eb)
+        d.entries = max_splits + 1;
+        return d;
+    }
+    // Blocks to aim at for the generic path: 4 per SM.
     const long long pairs = static_cast<long long>(nslots) * n_kv_heads;
-    const long long target =
-        (d.fast ? static_cast<long long>(FA_Q4_TARGET_PER_SM) : 4LL) * device_sm_count();
+    const long long target = 4LL * device_sm_count();
     long long cpc = (pairs * max_splits + target - 1) / target;
     if (cpc < 1) cpc = 1;
     if (cpc > max_splits) cpc = max_splits;
     d.splits_per_cta = static_cast<int>(cpc);
     d.body_entries = static_cast<int>((max_splits + cpc - 1) / cpc);
-    d.shadow_entry = (d.fast && (shadow_sink > 0 || shadow_win > 0)) ? d.body_entries : -1;
+    d.shadow_entry = -1;
     d.entries = d.body_entries + (d.shadow_entry >= 0 ? 1 : 0);
     return d;
 }

@@ -101,9 +101,11 @@ extern "C" fa_status fa_decode_noalloc(const float *q, const void *k_planes,
                                                    shadow_sink, shadow_win, max_splits, max_seq,
                                                    g.row_bytes);
     int entries = shape.entries;
-    if (shape.dense) {
-        // the streaming kernel adapts its work split to the entries it has
-        while (entries > 2 &&
+    if (shape.dense || shape.fast) {
+        // the streaming kernels adapt their work split to the entries they
+        // have: at least 2, plus the Q4_0 kernel's fp16-shadow entry
+        const int least = 2 + (shape.fast && (shadow_sink > 0 || shadow_win > 0) ? 1 : 0);
+        while (entries > least &&
                fa::decode_ws_bytes(nslots, n_q_heads, head_dim, entries) > kFaDecodeScratchBytes)
             --entries;
     }

@@ -288,11 +288,16 @@ fa_status fa_merge_attn_states(float *out, float *out_lse, const float *prefix,
  * Multi-slot split-KV decode ("attention.cu", "Decode-mode flash attention"
  * and "Multi-user decode attention"). Slot u has one query at position
  * pos[u] and attends rows 0..pos[u] of its own cache, whose last appended row
- * must be pos[u]. Its keys are cut by the split plan
+ * must be pos[u]. Its keys are cut into pieces, and fa_decode writes one
+ * partial per (slot, q head, entry) into the workspace. Over fp32 caches (and
+ * for groups of 16 q heads) the pieces are runs of consecutive splits of the
+ * split plan
  *     ns = clamp(ceil(L / split_keys), 1, max_splits), L = pos[u] + 1,
- *     split_len = roundup16(ceil(L / ns)),
- * fa_decode merges runs of consecutive splits inside one thread block, and
- * writes one partial per (slot, q head, entry) into the workspace:
+ *     split_len = roundup16(ceil(L / ns)).
+ * Over Q4_0, fp16 and fp8 caches the visible keys of all slots are instead
+ * cut into equal shares, one per thread block (or warp), so that every block
+ * streams the same number of bytes; a (slot, kv head) then has as many
+ * entries as shares it spans, never more than max_splits + 1. Each partial is
  *     m   = max over the entry's visible keys of s_j = scale * q . k_j
  *     l   = sum exp(s_j - m),   acc = sum exp(s_j - m) v_j      (fp32)
  * An entry with no visible key has m = -inf and l = 0 (its acc is not
@@ -301,8 +306,8 @@ fa_status fa_merge_attn_states(float *out, float *out_lse, const float *prefix,
  * out = sum w_e acc_e / sum w_e l_e.
  *
  * A Q4_0 cache's fp16 shadow keys (sinks, recent ring) go to one extra entry
- * per head. Workspace layout (S = max_splits + 1): a 256-byte header of uint32
- * words {0x46414443, nslots, n_q_heads, head_dim, E} where E <= S is the
+ * per head (the last one). Workspace layout (S = max_splits + 1): a 256-byte
+ * header of uint32 words {0x46414443, nslots, n_q_heads, head_dim, E} where E <= S is the
  * number of entries fa_decode wrote per head, then m [nslots*n_q_heads][S] fp32,
  * l [nslots*n_q_heads][S] fp32 and acc [nslots*n_q_heads][S][head_dim] fp32,
  * each part starting 256-byte aligned; entry e of a head is at index e < E.
@@ -344,9 +349,9 @@ fa_status fa_decode_combine(const void *workspace, float *out, int nslots, int n
  * The partials live in a fixed 8 MiB array in the library's device memory
  * (held by every GPU that loads the library until the process exits), laid
  * out as fa_decode's workspace with the entry stride equal to the number of
- * entries E (for fp16 and fp8 caches, whose streaming kernel can use any
- * number of entries from 2 up, E is the largest count up to max_splits + 1
- * that fits). A problem whose partials need more than 8 MiB
+ * entries E (for Q4_0, fp16 and fp8 caches, whose kernels can use any number
+ * of entries from 2 up (3 with fp16 shadows), E is the largest count up to
+ * max_splits + 1 that fits). A problem whose partials need more than 8 MiB
  * (256 + 2*nslots*n_q_heads*E*4 + nslots*n_q_heads*E*head_dim*4 bytes, parts
  * rounded up to 256) returns FA_ERR_WORKSPACE before any launch. The call
  * allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
