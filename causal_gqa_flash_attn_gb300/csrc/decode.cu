@@ -621,11 +621,40 @@ __device__ __forceinline__ Q4Tiles q4_tiles(const DecodeParams &P, int p) {
     return T;
 }
 
+// How far a warp pair's rings have run: K tiles and V tiles copied (and
+// consumed), P records passed. A block initialises its barriers once and
+// runs its pieces one after another through the same rings, so the stage and
+// phase of each copy or record follow from these running counts.
+struct Q4Ring {
+    int k = 0, v = 0, r = 0;
+};
+
+// The barriers of every warp pair (one thread per pair) and the abort flag;
+// the caller synchronises the block afterwards.
+template <int HD>
+__device__ __forceinline__ void q4_init(uint8_t *dsmem) {
+    using C = Q4Cfg<HD>;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0)
+        *reinterpret_cast<volatile int *>(dsmem + C::BAR_OFF + kPairs * C::BARS_PER_PAIR * 8) = 0;
+    if (warp < kPairs && lane == 0) {
+        uint64_t *bars = reinterpret_cast<uint64_t *>(dsmem + C::BAR_OFF) + warp * C::BARS_PER_PAIR;
+        for (int s = 0; s < C::NK + C::NV; ++s) mbar_init(&bars[s], 1);
+        for (int s = 0; s < kPRing; ++s) {
+            mbar_init(&bars[C::NK + C::NV + s], 1);           // pfull
+            mbar_init(&bars[C::NK + C::NV + kPRing + s], 1);  // pempty
+        }
+        mbar_fence_init();
+    }
+}
+
 // One piece of work: tiles j0 .. j1-1 of (slot u, kv head g) in the order of
-// q4_tiles, written as partial entry e.
+// q4_tiles, written as partial entry e. rg: this warp's ring counts (the QK
+// warp runs K and records, the PV warp V and records).
 template <int HD>
 __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, int e, int g,
-                                        int u, int p, const Q4Tiles &tl, int j0, int j1) {
+                                        int u, int p, const Q4Tiles &tl, int j0, int j1,
+                                        Q4Ring &rg) {
     using C = Q4Cfg<HD>;
     constexpr int NB = C::NB, MT = C::MT, ROWB = C::ROWB, NK = C::NK, NV = C::NV;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -645,16 +674,6 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
         reinterpret_cast<volatile int *>(dsmem + C::BAR_OFF + kPairs * C::BARS_PER_PAIR * 8);
 
     build_q_frags<HD>(P, head0, G, warp, 2 * kPairs, qfrag, qbias);
-    if (threadIdx.x == 0) *abort = 0;
-    if (qk_role && lane == 0) {
-        for (int s = 0; s < NK; ++s) mbar_init(&kfull[s], 1);
-        for (int s = 0; s < NV; ++s) mbar_init(&vfull[s], 1);
-        for (int s = 0; s < kPRing; ++s) {
-            mbar_init(&pfull[s], 1);
-            mbar_init(&pempty[s], 1);
-        }
-        mbar_fence_init();
-    }
     __syncthreads();
 
     const int ss = P.shadow_sink, sw = P.shadow_win;
@@ -690,16 +709,18 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
         float ls0 = 0.0f, ls1 = 0.0f;
         // Prologue: the first NK K tiles (the PV warp copies the V tiles).
         int kt = pair;  // next tile index to copy
-        int kn = 0;     // copies issued so far
+        int kn = 0;     // copies issued in this piece (ring count rg.k + kn)
         for (; kn < NK && kt < ntiles; ++kn) {
-            if (lane == 0) issue(kbody, kt, pbase + C::K_OFF + kn * C::TILE_ALLOC, &kfull[kn]);
+            const int st = (rg.k + kn) % NK;
+            if (lane == 0) issue(kbody, kt, pbase + C::K_OFF + st * C::TILE_ALLOC, &kfull[st]);
             kt += kPairs;
         }
         const uint32_t magic = opaque(kMagic);
         int seq = 0;  // position of the tile in this pair's sequence
         for (int i = pair; i < ntiles; i += kPairs, ++seq) {
-            const int s = seq % NK;
-            ok = __all_sync(0xffffffffu, mbar_wait(&kfull[s], (seq / NK) & 1, abort, P.err));
+            const int s = (rg.k + seq) % NK;
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(&kfull[s], ((rg.k + seq) / NK) & 1, abort, P.err));
             if (!ok) break;
             const uint8_t *Ks = pbase + C::K_OFF + s * C::TILE_ALLOC;
             const int t0 = tile_key0(i);
@@ -758,7 +779,10 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
             // the stage can take the K tile NK places further on.
             __syncwarp();
             if (kt < ntiles) {
-                if (lane == 0) issue(kbody, kt, pbase + C::K_OFF + s * C::TILE_ALLOC, &kfull[s]);
+                if (lane == 0) {
+                    fence_proxy_async_smem();  // those reads come before the copy's writes
+                    issue(kbody, kt, pbase + C::K_OFF + s * C::TILE_ALLOC, &kfull[s]);
+                }
                 kt += kPairs;
                 ++kn;
             }
@@ -785,10 +809,11 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
             const float c0 = (mu0 != old0) ? ex2(old0 - mu0) : 1.0f;
             const float c1 = (mu1 != old1) ? ex2(old1 - mu1) : 1.0f;
             // ---- hand P^T (both halves) and the rescale to the PV warp
-            const int ps = seq % kPRing;
-            if (seq >= kPRing) {
+            const int rn = rg.r + seq;  // this record's ring count
+            const int ps = rn % kPRing;
+            if (rn >= kPRing) {
                 ok = __all_sync(0xffffffffu,
-                                mbar_wait(&pempty[ps], ((seq / kPRing) - 1) & 1, abort, P.err));
+                                mbar_wait(&pempty[ps], ((rn / kPRing) - 1) & 1, abort, P.err));
                 if (!ok) break;
             }
             uint4 *rec = reinterpret_cast<uint4 *>(prec + ps * C::PREC);
@@ -803,10 +828,11 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
         }
         // end of the sequence for the PV warp
         if (ok) {
-            const int ps = seq % kPRing;
-            if (seq >= kPRing)
+            const int rn = rg.r + seq;
+            const int ps = rn % kPRing;
+            if (rn >= kPRing)
                 ok = __all_sync(0xffffffffu,
-                                mbar_wait(&pempty[ps], ((seq / kPRing) - 1) & 1, abort, P.err));
+                                mbar_wait(&pempty[ps], ((rn / kPRing) - 1) & 1, abort, P.err));
             if (ok) {
                 uint4 *rec = reinterpret_cast<uint4 *>(prec + ps * C::PREC);
                 rec[32 + lane] = make_uint4(0u, 0u, 0xFFFFFFFFu, 0u);  // tile index: none
@@ -814,7 +840,9 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
                 if (lane == 0) mbar_arrive(&pfull[ps]);
             }
         }
-        if (!ok) drain(kfull, NK, kn);  // let this warp's copies land first
+        if (!ok) drain(kfull, NK, rg.k + kn);  // let this warp's copies land first
+        rg.k += kn;
+        rg.r += seq + 1;  // the records, and the end-of-sequence record
         float m_used[1][2] = {{mu0, mu1}}, m_true[1][2] = {{mt0, mt1}}, lsum[1][2] = {{ls0, ls1}};
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
@@ -841,14 +869,17 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
         const uint8_t *vbody = P.v_planes + static_cast<size_t>(u) * P.plane_bytes + P.body_off +
                                static_cast<size_t>(g) * P.max_seq * ROWB;
         int vt = pair;  // next tile index to copy
-        int vn = 0;     // copies issued so far
+        int vn = 0;     // copies issued in this piece (ring count rg.v + vn)
         for (; vn < NV && vt < ntiles; ++vn) {
-            if (lane == 0) issue(vbody, vt, pbase + C::V_OFF + vn * C::TILE_ALLOC, &vfull[vn]);
+            const int st = (rg.v + vn) % NV;
+            if (lane == 0) issue(vbody, vt, pbase + C::V_OFF + st * C::TILE_ALLOC, &vfull[st]);
             vt += kPairs;
         }
-        for (int seq = 0;; ++seq) {
-            const int ps = seq % kPRing;
-            ok = __all_sync(0xffffffffu, mbar_wait(&pfull[ps], (seq / kPRing) & 1, abort, P.err));
+        int seq = 0;
+        for (;; ++seq) {
+            const int rn = rg.r + seq;  // this record's ring count
+            const int ps = rn % kPRing;
+            ok = __all_sync(0xffffffffu, mbar_wait(&pfull[ps], (rn / kPRing) & 1, abort, P.err));
             if (!ok) break;
             const uint4 *rec = reinterpret_cast<const uint4 *>(prec + ps * C::PREC);
             const uint4 w0 = rec[lane];
@@ -856,8 +887,18 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
             __syncwarp();
             if (lane == 0) mbar_arrive(&pempty[ps]);
             if (w1.z == 0xFFFFFFFFu) break;  // end of the sequence
-            const int s = seq % NV;
-            ok = __all_sync(0xffffffffu, mbar_wait(&vfull[s], (seq / NV) & 1, abort, P.err));
+            if (w1.z != static_cast<uint32_t>(pair + kPairs * seq)) {
+                // not the tile this record must carry: report, stop the block
+                if (lane == 0) {
+                    flag_error(P.err, FA_ERRBIT_DEVICE);
+                    *abort = 1;
+                }
+                ok = false;
+                break;
+            }
+            const int s = (rg.v + seq) % NV;
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(&vfull[s], ((rg.v + seq) / NV) & 1, abort, P.err));
             if (!ok) break;
             const float c0 = __uint_as_float(w1.x), c1 = __uint_as_float(w1.y);
             if (__any_sync(0xffffffffu, c0 != 1.0f || c1 != 1.0f)) {
@@ -937,7 +978,9 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
                 ++vn;
             }
         }
-        if (!ok) drain(vfull, NV, vn);  // let this warp's copies land first
+        if (!ok) drain(vfull, NV, rg.v + vn);  // let this warp's copies land first
+        rg.v += vn;
+        rg.r += seq + 1;  // the records, and the end-of-sequence record
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {  // rows r + 8 carry 16 (c - 8)
             o[mt][0][2] *= 0.0625f;
@@ -1092,15 +1135,21 @@ __global__ void __launch_bounds__(2 * kPairs * 32, FA_Q4_MIN_BLOCKS)
     long long A = sloc[0] + static_cast<long long>(g) * tl.count();  // the pair's first tile
     volatile int *abort = reinterpret_cast<volatile int *>(
         dsmem + Q4Cfg<HD>::BAR_OFF + kPairs * Q4Cfg<HD>::BARS_PER_PAIR * 8);
+    q4_init<HD>(dsmem);
+    __syncthreads();
+    Q4Ring rg;
     for (long long Tc = T0; Tc < T1;) {
         const int cnt = tl.count();
         const int j1 = static_cast<int>(min(static_cast<long long>(cnt), j + (T1 - Tc)));
         const int e = static_cast<int>(bid - A / J.C);
-        q4_body<HD>(P, dsmem, e, g, u, p, tl, j, j1);
+        q4_body<HD>(P, dsmem, e, g, u, p, tl, j, j1, rg);
         const size_t head0 = static_cast<size_t>(u) * P.Hq + static_cast<size_t>(g) * G;
         if (j1 == cnt) write_empty_range(P, head0, G, e + 1, J.Eb);
         Tc += j1 - j;
-        __syncthreads();  // the next piece re-initialises the shared state
+        // The merge wrote the stages and records with ordinary stores; the
+        // next piece's copies write them through the async proxy.
+        fence_proxy_async_smem();
+        __syncthreads();
         if (*abort) return;
         if (Tc >= T1) break;
         // the next pair with tiles

@@ -108,74 +108,129 @@ __global__ void kv_set_scale_kernel(uint8_t *planes, int nslots, size_t plane_by
             scale;
 }
 
-// Quantise the 32 values held by the lanes of a warp (lane j holds element j
-// of the block) into the 18 bytes at blk.
-__device__ __forceinline__ void q4_quant_block_warp(float x, uint8_t *blk, int lane) {
-    // amax: max |x| from +0, NaN never raises it (fmaxf returns the non-NaN operand).
-    float a = fmaxf(0.0f, fabsf(x));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    const float d = __fdiv_rn(a, -8.0f);
-    const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+// Quantise one Q4_0 block held by an 8-lane group of the warp (lane li of the
+// group holds elements 4 li .. 4 li + 3 in x) into the 18 bytes at img.
+// Every lane of the warp must call it (the group reductions shuffle).
+__device__ __forceinline__ void q4_quant_block8(float4 x, int li, uint8_t *img) {
+    // amax: max |x| from +0; NaN never raises it (fmaxf returns the non-NaN operand)
+    float a = fmaxf(fmaxf(fmaxf(0.0f, fabsf(x.x)), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+    // d = amax / -8: a scaling by a power of two, so the product by -1/8 is
+    // the same correctly rounded value as the division.
+    const float d = __fmul_rn(a, -0.125f);
+    const float id = (d != 0.0f) ? __frcp_rn(d) : 0.0f;  // IEEE reciprocal, nearest
     // One fp32 multiply (no contraction), a saturating round-half-even
-    // conversion (NaN -> 0), a wrapping +8, then the clamp.
-    const int qv = __float2int_rn(__fmul_rn(x, id));
-    int c = static_cast<int>(static_cast<unsigned>(qv) + 8u);
-    c = c < 0 ? 0 : (c > 15 ? 15 : c);
-    const int hi = __shfl_down_sync(0xffffffffu, c, 16);
-    if (lane < 16) blk[2 + lane] = static_cast<uint8_t>(c | (hi << 4));
-    if (lane == 0) *reinterpret_cast<uint16_t *>(blk) = __half_as_ushort(__float2half_rn(d));
+    // conversion (NaN -> 0), a wrapping +8, then the clamp to [0, 15].
+    const float xs[4] = {x.x, x.y, x.z, x.w};
+    uint32_t codes = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int q = __float2int_rn(__fmul_rn(xs[k], id));
+        int c = static_cast<int>(static_cast<unsigned>(q) + 8u);
+        c = c < 0 ? 0 : (c > 15 ? 15 : c);
+        codes |= static_cast<uint32_t>(c) << (8 * k);
+    }
+    // byte j of the block: element j (low nibble) | element j + 16 (high)
+    const uint32_t hi = __shfl_down_sync(0xffffffffu, codes, 4);
+    if (li < 4) {
+        const uint32_t w = codes | (hi << 4);
+        uint16_t *dst = reinterpret_cast<uint16_t *>(img + 2 + 4 * li);  // 2-byte aligned
+        dst[0] = static_cast<uint16_t>(w);
+        dst[1] = static_cast<uint16_t>(w >> 16);
+    }
+    if (li == 0) *reinterpret_cast<uint16_t *>(img) = __half_as_ushort(__float2half_rn(d));
 }
 
-// One warp per Q4_0 block of an input row, K and V.
-__global__ void __launch_bounds__(kThreads)
-    kv_append_q4_kernel(const float *__restrict__ k_new, const float *__restrict__ v_new,
+// One warp per 4 consecutive Q4_0 blocks of the input rows (K and V): lane l
+// holds 4 values of block l / 8. The two pairs of blocks (36 bytes each, a
+// 4-byte aligned run of a plane row, since rows hold an even number of
+// blocks) are assembled in shared memory and leave as whole 32-bit words.
+constexpr int kAppendWarps = 8;
+
+__global__ void __launch_bounds__(kAppendWarps * 32)
+    kv_append_q4_kernel(const float4 *__restrict__ k_new, const float4 *__restrict__ v_new,
                         uint8_t *__restrict__ k_planes, uint8_t *__restrict__ v_planes,
                         const int32_t *__restrict__ pos0, int nslots, int n, int n_kv, int hd,
                         int max_seq, size_t plane_bytes, size_t body_off, size_t row_bytes,
                         size_t sink_off, size_t ring_off, int shadow_sink, int shadow_win,
                         unsigned *err) {
-    const int lane = threadIdx.x & 31;
+    __shared__ __align__(16) uint32_t img[kAppendWarps][2][18];  // K, V: 4 blocks each
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const int gq = lane >> 3, li = lane & 7;
     const int nb = hd / kQ4Block;
-    const long long total = static_cast<long long>(nslots) * n * n_kv * nb;
-    const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
-    for (long long w = blockIdx.x * static_cast<long long>(blockDim.x / 32) + (threadIdx.x >> 5);
-         w < total; w += warps) {
-        const int b = static_cast<int>(w % nb);
-        long long r = w / nb;
-        const int h = static_cast<int>(r % n_kv);
-        r /= n_kv;
-        const int t = static_cast<int>(r % n);
-        const int u = static_cast<int>(r / n);
+    const long long total = static_cast<long long>(nslots) * n * n_kv * nb;  // blocks
+    const long long groups = (total + 3) / 4;
+    uint8_t *ik = reinterpret_cast<uint8_t *>(img[wib][0]);
+    uint8_t *iv = reinterpret_cast<uint8_t *>(img[wib][1]);
+    // Destination of block blk (first of its pair for the word stores):
+    // false if blk is past the input or its row's position is out of range.
+    auto locate = [&](long long blk, size_t *plane, long long *pos, int *h, int *t) -> bool {
+        if (blk >= total) return false;
+        const long long row = blk / nb;
+        *h = static_cast<int>(row % n_kv);
+        const long long r2 = row / n_kv;
+        *t = static_cast<int>(r2 % n);
+        const int u = static_cast<int>(r2 / n);
         const int p0 = pos0[u];
-        const long long pos = static_cast<long long>(p0) + t;
-        if (p0 < 0 || pos >= max_seq) {
-            if (lane == 0 && b == 0) flag_error(err, FA_ERRBIT_DEVICE);
-            continue;
+        *pos = static_cast<long long>(p0) + *t;
+        *plane = static_cast<size_t>(u) * plane_bytes;
+        return p0 >= 0 && *pos < max_seq;
+    };
+    for (long long w = static_cast<long long>(blockIdx.x) * kAppendWarps + wib; w < groups;
+         w += static_cast<long long>(gridDim.x) * kAppendWarps) {
+        const long long blk = 4 * w + gq;
+        size_t plane = 0;
+        long long pos = 0;
+        int h = 0, t = 0;
+        const bool live = blk < total;
+        const bool ok = locate(blk, &plane, &pos, &h, &t);
+        if (live && !ok && li == 0 && blk % nb == 0) flag_error(err, FA_ERRBIT_DEVICE);
+        float4 xk = make_float4(0.0f, 0.0f, 0.0f, 0.0f), xv = xk;
+        if (live) {
+            xk = __ldg(k_new + blk * 8 + li);
+            xv = __ldg(v_new + blk * 8 + li);
         }
-        const float xk = __ldg(k_new + w * kQ4Block + lane);
-        const float xv = __ldg(v_new + w * kQ4Block + lane);
-        const size_t plane = static_cast<size_t>(u) * plane_bytes;
-        const size_t blk_off =
-            body_off + (static_cast<size_t>(h) * max_seq + pos) * row_bytes + b * kQ4BlockBytes;
-        q4_quant_block_warp(xk, k_planes + plane + blk_off, lane);
-        q4_quant_block_warp(xv, v_planes + plane + blk_off, lane);
-
-        const int e = b * kQ4Block + lane;
-        if (pos < shadow_sink) {
-            const size_t so =
-                plane + sink_off + ((static_cast<size_t>(h) * kSinkMax + pos) * hd + e) * 2;
-            *reinterpret_cast<__half *>(k_planes + so) = __float2half_rn(xk);
-            *reinterpret_cast<__half *>(v_planes + so) = __float2half_rn(xv);
+        q4_quant_block8(xk, li, ik + 18 * gq);
+        q4_quant_block8(xv, li, iv + 18 * gq);
+        if (ok) {
+            // fp16 mirrors: the shadow sink rows, and the rows that stay among
+            // the 256 newest after this call (no two rows of a call share a
+            // ring slot)
+            const int e = static_cast<int>(blk % nb) * kQ4Block + 4 * li;
+            const uint2 hk = make_uint2(pack_half2(xk.x, xk.y), pack_half2(xk.z, xk.w));
+            const uint2 hv = make_uint2(pack_half2(xv.x, xv.y), pack_half2(xv.z, xv.w));
+            if (pos < shadow_sink) {
+                const size_t so =
+                    plane + sink_off + ((static_cast<size_t>(h) * kSinkMax + pos) * hd + e) * 2;
+                *reinterpret_cast<uint2 *>(k_planes + so) = hk;
+                *reinterpret_cast<uint2 *>(v_planes + so) = hv;
+            }
+            if (shadow_win > 0 && t >= n - kRingRows) {
+                const size_t ro = plane + ring_off +
+                                  ((static_cast<size_t>(h) * kRingRows + (pos % kRingRows)) * hd +
+                                   e) * 2;
+                *reinterpret_cast<uint2 *>(k_planes + ro) = hk;
+                *reinterpret_cast<uint2 *>(v_planes + ro) = hv;
+            }
         }
-        // Only rows that stay among the 256 newest after this call are
-        // mirrored into the ring, so no two rows of one call share a slot.
-        if (shadow_win > 0 && t >= n - kRingRows) {
-            const size_t ro = plane + ring_off +
-                              ((static_cast<size_t>(h) * kRingRows + (pos % kRingRows)) * hd + e) * 2;
-            *reinterpret_cast<__half *>(k_planes + ro) = __float2half_rn(xk);
-            *reinterpret_cast<__half *>(v_planes + ro) = __float2half_rn(xv);
+        __syncwarp();
+        if (lane < 18) {
+            // word lane % 9 of pair lane / 9 (its first block: 4 w + 2 (lane / 9))
+            const long long pb = 4 * w + 2 * (lane / 9);
+            size_t pplane = 0;
+            long long ppos = 0;
+            int ph = 0, pt = 0;
+            if (locate(pb, &pplane, &ppos, &ph, &pt)) {
+                const size_t off = pplane + body_off +
+                                   (static_cast<size_t>(ph) * max_seq + ppos) * row_bytes +
+                                   static_cast<size_t>(pb % nb) * kQ4BlockBytes + 4 * (lane % 9);
+                *reinterpret_cast<uint32_t *>(k_planes + off) = img[wib][0][lane];
+                *reinterpret_cast<uint32_t *>(v_planes + off) = img[wib][1][lane];
+            }
         }
+        __syncwarp();
     }
 }
 
@@ -209,9 +264,10 @@ cudaError_t launch_kv_append(const float *k_new, const float *v_new, uint8_t *k_
             k4, v4, k_planes, v_planes, pos0, nslots, n, g.n_kv, g.hd, g.max_seq, g.bytes,
             g.body_off, g.scale_off, err);
     } else {
-        const long long items = static_cast<long long>(nslots) * n * g.n_kv * (g.hd / kQ4Block);
-        kv_append_q4_kernel<<<grid_for(items, kThreads / 32), kThreads, 0, stream>>>(
-            k_new, v_new, k_planes, v_planes, pos0, nslots, n, g.n_kv, g.hd, g.max_seq, g.bytes,
+        const long long groups =
+            (static_cast<long long>(nslots) * n * g.n_kv * (g.hd / kQ4Block) + 3) / 4;
+        kv_append_q4_kernel<<<grid_for(groups, kAppendWarps), kAppendWarps * 32, 0, stream>>>(
+            k4, v4, k_planes, v_planes, pos0, nslots, n, g.n_kv, g.hd, g.max_seq, g.bytes,
             g.body_off, g.row_bytes, g.sink_off, g.ring_off, shadow_sink, shadow_win, err);
     }
     return cudaGetLastError();

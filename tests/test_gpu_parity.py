@@ -161,6 +161,11 @@ DECODE_CASES = [
     # slots whose every key is an fp16 sink (lengths 3 and 5 <= 8 sinks)
     ((3, 9, 40, 777), 8, 2, 128, 0, 0, "q4_0", (8, 0), 256, 800),
     ((5, 1300), 4, 1, 64, 2, 0, "q4_0", (8, 0), 128, 1400),
+    # more tiles than body blocks, so that blocks run pieces of two or more
+    # (slot, kv head) pairs one after another; with a window and shadows too
+    ((4000, 3001, 2500, 17), 16, 2, 128, 4, 0, "q4_0", (4, 0), 256, 4096),
+    ((6000, 5000, 33), 8, 2, 256, 4, 1024, "q4_0", (4, 256), 256, 6144),
+    ((9000, 9000), 8, 1, 64, 0, 0, "q4_0", (0, 0), 256, 9000),
     # group 16 over Q4_0 (the generic kernel): sinks, a recent fp16 ring, a
     # window, and a narrow shadow window
     ((1, 17, 300, 1000), 16, 1, 256, 4, 0, "q4_0", (4, 0), 256, 1024),
