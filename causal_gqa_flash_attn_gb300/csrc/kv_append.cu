@@ -10,6 +10,8 @@
 // with coalesced loads and every output byte written once.
 #include <cuda_fp8.h>
 
+#include <algorithm>
+
 #include "fa_device.cuh"
 #include "fa_internal.h"
 
@@ -147,6 +149,8 @@ __device__ __forceinline__ void q4_quant_block8(float4 x, int li, uint8_t *img) 
 // holds 4 values of block l / 8. The two pairs of blocks (36 bytes each, a
 // 4-byte aligned run of a plane row, since rows hold an even number of
 // blocks) are assembled in shared memory and leave as whole 32-bit words.
+// Block indices are 32-bit (the host splits larger appends by slots) and
+// blocks per row (head_dim / 32) a power of two.
 constexpr int kAppendWarps = 8;
 
 __global__ void __launch_bounds__(kAppendWarps * 32)
@@ -159,38 +163,33 @@ __global__ void __launch_bounds__(kAppendWarps * 32)
     __shared__ __align__(16) uint32_t img[kAppendWarps][2][18];  // K, V: 4 blocks each
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
     const int gq = lane >> 3, li = lane & 7;
-    const int nb = hd / kQ4Block;
-    const long long total = static_cast<long long>(nslots) * n * n_kv * nb;  // blocks
-    const long long groups = (total + 3) / 4;
+    const uint32_t nb_shift = hd == 64 ? 1u : (hd == 128 ? 2u : 3u);  // log2(hd / 32)
+    const uint32_t total = static_cast<uint32_t>(nslots) * n * n_kv << nb_shift;  // blocks
+    const uint32_t groups = (total + 3) / 4;
     uint8_t *ik = reinterpret_cast<uint8_t *>(img[wib][0]);
     uint8_t *iv = reinterpret_cast<uint8_t *>(img[wib][1]);
-    // Destination of block blk (first of its pair for the word stores):
-    // false if blk is past the input or its row's position is out of range.
-    auto locate = [&](long long blk, size_t *plane, long long *pos, int *h, int *t) -> bool {
-        if (blk >= total) return false;
-        const long long row = blk / nb;
-        *h = static_cast<int>(row % n_kv);
-        const long long r2 = row / n_kv;
-        *t = static_cast<int>(r2 % n);
-        const int u = static_cast<int>(r2 / n);
-        const int p0 = pos0[u];
-        *pos = static_cast<long long>(p0) + *t;
-        *plane = static_cast<size_t>(u) * plane_bytes;
-        return p0 >= 0 && *pos < max_seq;
-    };
-    for (long long w = static_cast<long long>(blockIdx.x) * kAppendWarps + wib; w < groups;
-         w += static_cast<long long>(gridDim.x) * kAppendWarps) {
-        const long long blk = 4 * w + gq;
-        size_t plane = 0;
-        long long pos = 0;
-        int h = 0, t = 0;
+    for (uint32_t w = blockIdx.x * kAppendWarps + wib; w < groups;
+         w += gridDim.x * kAppendWarps) {
+        const uint32_t blk = 4 * w + gq;
         const bool live = blk < total;
-        const bool ok = locate(blk, &plane, &pos, &h, &t);
-        if (live && !ok && li == 0 && blk % nb == 0) flag_error(err, FA_ERRBIT_DEVICE);
+        // this lane's block: row (u, t, h) and its destination
+        const uint32_t row = blk >> nb_shift, b = blk & ((1u << nb_shift) - 1);
+        const uint32_t r2 = row / static_cast<uint32_t>(n_kv);
+        const int h = static_cast<int>(row - r2 * n_kv);
+        const uint32_t uu = r2 / static_cast<uint32_t>(n);
+        const int t = static_cast<int>(r2 - uu * n);
+        const int p0 = live ? pos0[uu] : 0;
+        const long long pos = static_cast<long long>(p0) + t;
+        const bool ok = live && p0 >= 0 && pos < max_seq;
+        if (live && !ok && li == 0 && b == 0) flag_error(err, FA_ERRBIT_DEVICE);
+        const size_t plane = static_cast<size_t>(uu) * plane_bytes;
+        const size_t dst = plane + body_off +
+                           (static_cast<size_t>(h) * max_seq + (ok ? pos : 0)) * row_bytes +
+                           b * kQ4BlockBytes;
         float4 xk = make_float4(0.0f, 0.0f, 0.0f, 0.0f), xv = xk;
         if (live) {
-            xk = __ldg(k_new + blk * 8 + li);
-            xv = __ldg(v_new + blk * 8 + li);
+            xk = __ldg(k_new + static_cast<size_t>(blk) * 8 + li);
+            xv = __ldg(v_new + static_cast<size_t>(blk) * 8 + li);
         }
         q4_quant_block8(xk, li, ik + 18 * gq);
         q4_quant_block8(xv, li, iv + 18 * gq);
@@ -198,7 +197,7 @@ __global__ void __launch_bounds__(kAppendWarps * 32)
             // fp16 mirrors: the shadow sink rows, and the rows that stay among
             // the 256 newest after this call (no two rows of a call share a
             // ring slot)
-            const int e = static_cast<int>(blk % nb) * kQ4Block + 4 * li;
+            const int e = static_cast<int>(b) * kQ4Block + 4 * li;
             const uint2 hk = make_uint2(pack_half2(xk.x, xk.y), pack_half2(xk.z, xk.w));
             const uint2 hv = make_uint2(pack_half2(xv.x, xv.y), pack_half2(xv.z, xv.w));
             if (pos < shadow_sink) {
@@ -215,20 +214,16 @@ __global__ void __launch_bounds__(kAppendWarps * 32)
                 *reinterpret_cast<uint2 *>(v_planes + ro) = hv;
             }
         }
+        // word lane % 9 of pair lane / 9 goes out; the pair's first block is
+        // held by the lanes of group 2 (lane / 9), which pass its destination
+        const int src = 16 * (lane >= 9 ? 1 : 0);
+        const size_t pdst = __shfl_sync(0xffffffffu, dst, src);
+        const bool pok = __shfl_sync(0xffffffffu, ok, src);
         __syncwarp();
-        if (lane < 18) {
-            // word lane % 9 of pair lane / 9 (its first block: 4 w + 2 (lane / 9))
-            const long long pb = 4 * w + 2 * (lane / 9);
-            size_t pplane = 0;
-            long long ppos = 0;
-            int ph = 0, pt = 0;
-            if (locate(pb, &pplane, &ppos, &ph, &pt)) {
-                const size_t off = pplane + body_off +
-                                   (static_cast<size_t>(ph) * max_seq + ppos) * row_bytes +
-                                   static_cast<size_t>(pb % nb) * kQ4BlockBytes + 4 * (lane % 9);
-                *reinterpret_cast<uint32_t *>(k_planes + off) = img[wib][0][lane];
-                *reinterpret_cast<uint32_t *>(v_planes + off) = img[wib][1][lane];
-            }
+        if (lane < 18 && pok) {
+            const size_t off = pdst + 4 * (lane % 9);
+            *reinterpret_cast<uint32_t *>(k_planes + off) = img[wib][0][lane];
+            *reinterpret_cast<uint32_t *>(v_planes + off) = img[wib][1][lane];
         }
         __syncwarp();
     }
@@ -264,11 +259,20 @@ cudaError_t launch_kv_append(const float *k_new, const float *v_new, uint8_t *k_
             k4, v4, k_planes, v_planes, pos0, nslots, n, g.n_kv, g.hd, g.max_seq, g.bytes,
             g.body_off, g.scale_off, err);
     } else {
-        const long long groups =
-            (static_cast<long long>(nslots) * n * g.n_kv * (g.hd / kQ4Block) + 3) / 4;
-        kv_append_q4_kernel<<<grid_for(groups, kAppendWarps), kAppendWarps * 32, 0, stream>>>(
-            k4, v4, k_planes, v_planes, pos0, nslots, n, g.n_kv, g.hd, g.max_seq, g.bytes,
-            g.body_off, g.row_bytes, g.sink_off, g.ring_off, shadow_sink, shadow_win, err);
+        // block indices stay 32-bit: slots in chunks of at most 2^30 blocks
+        const long long per_slot = static_cast<long long>(n) * g.n_kv * (g.hd / kQ4Block);
+        const long long chunk = per_slot > 0 ? std::max(1LL, (1LL << 30) / per_slot) : nslots;
+        if (per_slot > (1LL << 30)) return cudaErrorInvalidValue;
+        for (long long u0 = 0; u0 < nslots; u0 += chunk) {
+            const int ns = static_cast<int>(std::min<long long>(chunk, nslots - u0));
+            const size_t in_off = static_cast<size_t>(u0) * per_slot * 8;  // float4s
+            const long long groups = (ns * per_slot + 3) / 4;
+            kv_append_q4_kernel<<<grid_for(groups, kAppendWarps), kAppendWarps * 32, 0, stream>>>(
+                k4 + in_off, v4 + in_off, k_planes + static_cast<size_t>(u0) * g.bytes,
+                v_planes + static_cast<size_t>(u0) * g.bytes, pos0 + u0, ns, n, g.n_kv, g.hd,
+                g.max_seq, g.bytes, g.body_off, g.row_bytes, g.sink_off, g.ring_off, shadow_sink,
+                shadow_win, err);
+        }
     }
     return cudaGetLastError();
 }
