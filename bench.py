@@ -169,12 +169,19 @@ class GpuBench:
         self.torch, self.fa, self.dev = torch, fa, dev
         self.stream = torch.cuda.current_stream(dev)
         self.flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.flush_read = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.flush_sink = torch.empty(1, dtype=torch.float32, device=dev)
         self.launches = 0
         self.graph_steps = None  # True once a step was timed as graph replays
         self.graph_error = None
 
     def flush_l2(self):
+        """Outside the timed region: write a 256 MB buffer (every line of the
+        129 MB L2 replaced), then read another 256 MB buffer, so that the lines
+        the write left dirty are written back here and the timed step starts
+        with an L2 of clean lines that hold none of its data."""
         self.flush_buf.zero_()
+        self.torch.sum(self.flush_read, dim=0, out=self.flush_sink)
 
     def timed_steps(self, step, warmup, steps, kernel_events=True, graph=False):
         """Run warmup + steps of `step`; each timed step between CUDA events on
@@ -738,7 +745,8 @@ def main():
                        "n_q_heads": headline.n_q_heads, "n_kv_heads": headline.n_kv_heads,
                        "head_dim": headline.head_dim, "sink": headline.sink, "win": headline.win,
                        "kv_fmt": headline.kv_fmt, "flop_per_step": flops_step,
-                       "step": "kv_append + prefill", "l2": "flushed between steps (256 MB write)",
+                       "step": "kv_append + prefill", "l2": "flushed between steps: 256 MB written, then another 256 MB read "
+                             "(the flush's dirty lines are written back before the step)",
                        "launch": ("the step captured once in a CUDA graph, each timed step one "
                                   "replay" if B.graph_steps else
                                   f"plain calls (graph capture failed: {B.graph_error})"),
