@@ -28,6 +28,7 @@
 //  * decode_kernel (fp32 caches, group 16, and that shadow entry): stages
 //    16-key fp16 tiles in shared memory, reads fragments with ldmatrix.
 // Each block merges its warps; fa_decode_combine merges the entries.
+#include "decode_common.cuh"
 #include "decode_softmax.cuh"
 #include "fa_device.cuh"
 #include "fa_internal.h"
@@ -43,23 +44,6 @@ constexpr int kChunk = 16;     // keys per step of the generic path
 // any |d| < 8192 (inputs within the fp16 range).
 constexpr float kRescaleGeneric = 8.0f;
 constexpr float kRescaleQ4 = 2.0f;
-
-struct DecodeParams {
-    const float *q;
-    const uint8_t *k_planes;
-    const uint8_t *v_planes;
-    const int32_t *pos;
-    float *ws_m, *ws_l, *ws_acc;
-    uint32_t *ws_header;
-    int nslots, Hq, Hkv, max_seq, sink, win, fmt, shadow_sink, shadow_win;
-    int split_keys, max_splits, cpc;
-    int entries;       // entries written per (slot, head)
-    int stride;        // entry stride of the workspace
-    int shadow_entry;  // entry index of the fp16-shadow keys, or -1
-    size_t plane_bytes, body_off, row_bytes, sink_off, ring_off, scale_off;
-    float sl2;  // scale * log2(e)
-    unsigned *err;
-};
 
 __device__ __forceinline__ int dec_plan(int seq_len, int kps, int cap, int *split_len) {
     int ns = (seq_len + kps - 1) / kps;
@@ -584,43 +568,6 @@ __device__ __forceinline__ void build_q_frags(const DecodeParams &P, size_t head
     }
 }
 
-// The 32-key tiles of one (slot, kv head) that the Q4_0 path loads, in
-// order: tile kt covers keys [32 kt, 32 kt + 32) clipped to [0, p]. They are
-// two runs, [a0, a0 + na) and [b0, b0 + nb): with a window, the tiles holding
-// attended sinks and then the window's tiles; without one, a single run.
-// Tiles whose every key is an fp16 shadow (sink rows below shadow_sink,
-// recent rows above p - shadow_win) are left out: the shadow entry reads those.
-struct Q4Tiles {
-    int a0, na, b0, nb;
-    __device__ __forceinline__ int count() const { return na + nb; }
-    __device__ __forceinline__ int kt(int i) const { return i < na ? a0 + i : b0 + (i - na); }
-};
-
-__device__ __forceinline__ Q4Tiles q4_tiles(const DecodeParams &P, int p) {
-    Q4Tiles T{0, 0, 0, 0};
-    if (p < 0 || p >= P.max_seq || p < P.shadow_sink) return T;
-    const int nt = p / kTileKeys + 1;       // tiles holding keys 0 .. p
-    const int lo = P.shadow_sink / kTileKeys;  // first tile with a key >= shadow_sink
-    int hi = nt;
-    if (P.shadow_win > 0) {
-        const int last = p - P.shadow_win;  // the largest key read from the Q4_0 rows
-        hi = last >= 0 ? min(hi, last / kTileKeys + 1) : 0;
-    }
-    if (P.win <= 0) {
-        T.a0 = lo;
-        T.na = max(0, hi - lo);
-        return T;
-    }
-    // attended: sinks [0, min(sink, p + 1)) and the window [p - win + 1, p]
-    const int ns = (min(P.sink, p + 1) + kTileKeys - 1) / kTileKeys;
-    const int w0 = max(max(0, p - P.win + 1) / kTileKeys, ns);
-    T.a0 = lo;
-    T.na = max(0, min(ns, hi) - lo);
-    T.b0 = max(w0, lo);
-    T.nb = max(0, hi - T.b0);
-    return T;
-}
-
 // How far a warp pair's rings have run: K tiles and V tiles copied (and
 // consumed), P records passed. A block initialises its barriers once and
 // runs its pieces one after another through the same rings, so the stage and
@@ -992,61 +939,6 @@ __device__ __forceinline__ void q4_body(const DecodeParams &P, uint8_t *dsmem, i
     merge_finish<HD>(P, dsmem, head0, G, e);
 }
 
-// Stream-K work split of the Q4_0 path. The loaded tiles of all (slot, kv
-// head) pairs, pair after pair, are cut into equal runs of C tiles, one run
-// per body block, so that every block streams the same number of bytes and
-// none waits for a straggler wave. A block writes one partial per pair piece
-// it covers, as entry (block - the block holding the pair's first tile); the
-// block holding a pair's last piece marks the pair's later body entries empty.
-// Entry Eb of every head is the fp16-shadow entry when the cache has shadows.
-struct Q4Job {
-    long long T;  // tiles of all pairs
-    long long C;  // tiles per body block
-    int Eb;       // body entries per head
-    int E;        // entries per head (Eb, plus the shadow entry)
-};
-
-// Warp-wide (every lane gets the same result). nb: body blocks.
-__device__ __forceinline__ Q4Job q4_job(const DecodeParams &P, int nb) {
-    const int lane = threadIdx.x & 31;
-    long long T = 0;
-    int maxt = 0;
-    for (int u0 = 0; u0 < P.nslots; u0 += 32) {
-        const int u = u0 + lane;
-        const int nt = u < P.nslots ? q4_tiles(P, P.pos[u]).count() : 0;
-        long long sum = nt;
-        int mx = nt;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            sum += __shfl_xor_sync(0xffffffffu, sum, o);
-            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        }
-        T += sum * P.Hkv;
-        maxt = max(maxt, mx);
-    }
-    const int shadow = (P.shadow_sink > 0 || P.shadow_win > 0) ? 1 : 0;
-    const int sb = P.stride - shadow;  // body entries available (>= 2)
-    Q4Job J;
-    J.T = T;
-    J.C = nb > 0 ? (T + nb - 1) / nb : T;
-    // at most sb pieces per pair: C > (maxt - 1) / (sb - 1)
-    const long long cmin = maxt > 0 ? (maxt - 1) / (sb - 1) + 1 : 1;
-    if (J.C < cmin) J.C = cmin;
-    J.Eb = maxt > 0 ? static_cast<int>(min(static_cast<long long>(sb), (maxt - 1) / J.C + 2)) : 1;
-    J.E = J.Eb + shadow;
-    return J;
-}
-
-// Entries [e0, e1) of the G heads from head0 on: empty (m = -inf, l = 0).
-__device__ __forceinline__ void write_empty_range(const DecodeParams &P, size_t head0, int G,
-                                                  int e0, int e1) {
-    for (int i = threadIdx.x; i < G * (e1 - e0); i += blockDim.x) {
-        const size_t idx = (head0 + i % G) * P.stride + e0 + i / G;
-        P.ws_m[idx] = -INFINITY;
-        P.ws_l[idx] = 0.0f;
-    }
-}
-
 // Blocks [0, nslots * Hkv) are the pairs' auxiliary blocks: the fp16-shadow
 // entry, the empty entries of a pair with no Q4_0 tile, and the report of a
 // position out of range. The blocks after them are the body blocks.
@@ -1058,9 +950,8 @@ __global__ void __launch_bounds__(2 * kPairs * 32, FA_Q4_MIN_BLOCKS)
     __shared__ long long sloc[3];  // first pair's tile base, slot, kv head of the block's run
     const int G = P.Hq / P.Hkv;
     const int n_aux = P.nslots * P.Hkv;
-    const int nb = static_cast<int>(gridDim.x) - n_aux;
     if (threadIdx.x < 32) {
-        const Q4Job J = q4_job(P, nb);
+        const Q4Job J = q4_job(P, P.q4_body_blocks);
         if (threadIdx.x == 0) {
             sjob = J;
             if (blockIdx.x == 0) {
@@ -1096,30 +987,10 @@ __global__ void __launch_bounds__(2 * kPairs * 32, FA_Q4_MIN_BLOCKS)
     const long long T1 = min(J.T, T0 + J.C);
     if (T0 >= T1) return;
     if (threadIdx.x < 32) {
-        // the pair holding tile T0: scan the slots' tile counts
-        const int lane = threadIdx.x;
-        long long base = 0, slot_base = 0;
-        int u_hit = -1;
-        for (int u0 = 0; u0 < P.nslots && u_hit < 0; u0 += 32) {
-            const int uu = u0 + lane;
-            const long long cnt =
-                uu < P.nslots ? static_cast<long long>(q4_tiles(P, P.pos[uu]).count()) * P.Hkv : 0;
-            long long inc = cnt;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const long long y = __shfl_up_sync(0xffffffffu, inc, o);
-                if (lane >= o) inc += y;
-            }
-            const unsigned hit = __ballot_sync(0xffffffffu, base + inc > T0);
-            if (hit) {
-                const int L = __ffs(hit) - 1;
-                u_hit = u0 + L;
-                slot_base = base + __shfl_sync(0xffffffffu, inc - cnt, L);
-            } else {
-                base += __shfl_sync(0xffffffffu, inc, 31);
-            }
-        }
-        if (lane == 0) {
+        int u_hit;
+        long long slot_base;
+        q4_locate(P, T0, &u_hit, &slot_base);
+        if (threadIdx.x == 0) {
             sloc[0] = slot_base;
             sloc[1] = u_hit;
         }
@@ -1254,15 +1125,15 @@ cudaError_t launch_generic(const DecodeParams &P, cudaStream_t stream) {
 }
 
 template <int HD>
-cudaError_t launch_q4(const DecodeParams &P, cudaStream_t stream) {
+cudaError_t launch_q4(const DecodeParams &P, bool body, cudaStream_t stream) {
     using C = Q4Cfg<HD>;
     cudaError_t e = cudaFuncSetAttribute(decode_q4_kernel<HD>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    // one auxiliary block per (slot, kv head), then the body blocks: as many
-    // as stay resident together (a single wave)
+    // one auxiliary block per (slot, kv head), then P.q4_body_blocks body
+    // blocks (none when another kernel computes the body entries)
     const long long aux = static_cast<long long>(P.nslots) * P.Hkv;
-    const long long blocks = aux + static_cast<long long>(FA_Q4_MIN_BLOCKS) * device_sm_count();
+    const long long blocks = aux + (body ? P.q4_body_blocks : 0);
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     decode_q4_kernel<HD><<<static_cast<unsigned>(blocks), 2 * kPairs * 32, C::SMEM, stream>>>(P);
     return cudaGetLastError();
@@ -1368,12 +1239,22 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodeWs &ws, const DecodeS
     if (d.entries > ws.stride) return cudaErrorInvalidValue;
     const int G = a.n_q_heads / a.n_kv_heads;
     if (d.fast) {
+        // The tensor-core kernel computes the body entries over 128-key tiles,
+        // one block per SM; the warp-MMA kernel's auxiliary blocks write the
+        // header, the fp16-shadow and empty entries first. Otherwise the
+        // warp-MMA kernel does everything (32-key tiles, two blocks per SM).
+        const bool tc = q4_tc_supported(a.g.hd, G);
+        P.q4_tile_keys = tc ? q4_tc_tile_keys() : kTileKeys;
+        P.q4_body_blocks = (tc ? 1 : FA_Q4_MIN_BLOCKS) * device_sm_count();
+        cudaError_t e;
         switch (a.g.hd) {
-            case 64: return launch_q4<64>(P, stream);
-            case 128: return launch_q4<128>(P, stream);
-            case 256: return launch_q4<256>(P, stream);
+            case 64: e = launch_q4<64>(P, !tc, stream); break;
+            case 128: e = launch_q4<128>(P, !tc, stream); break;
+            case 256: e = launch_q4<256>(P, !tc, stream); break;
             default: return cudaErrorInvalidValue;
         }
+        if (e == cudaSuccess && tc) e = launch_q4_tc(P, a.g.hd, stream);
+        return e;
     }
     const bool two = G > 8;
     switch (a.g.hd) {
