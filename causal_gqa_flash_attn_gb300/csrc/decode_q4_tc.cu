@@ -57,12 +57,12 @@ struct TcCfg {
     static constexpr int ROWW = ROWB / 4;     // 32-bit words per row
     static constexpr int NKS = 3 * NB;        // k-steps of Q'^T: lo, hi of each block, then biases
     // TMEM columns
-    static constexpr uint32_t KA = 0;                      // K': 16 per block
-    static constexpr uint32_t BA = NB * 16;                // bias A operand: 8
-    static constexpr uint32_t S0 = (BA + 8 + 31) / 32 * 32;  // S^T buffers: 16 per block pair
+    static constexpr uint32_t KW = NB * 16;                // K': 16 per block
+    static constexpr uint32_t KA0 = 0, KA1 = KW;           // two K' buffers
+    static constexpr uint32_t BA = 2 * KW;                 // bias A operand: 8
+    static constexpr uint32_t S = (BA + 8 + 31) / 32 * 32;   // S^T: 16 per block pair
     static constexpr uint32_t SW = NP * 16;
-    static constexpr uint32_t S1 = (S0 + SW + 31) / 32 * 32;
-    static constexpr uint32_t O = (S1 + SW + 31) / 32 * 32;  // O^T: 64 per M tile
+    static constexpr uint32_t O = (S + SW + 31) / 32 * 32;   // O^T: 64 per M tile
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(O + MT * 64 <= TMEM_COLS, "TMEM columns");
     // shared memory (offsets from a 1024-byte aligned base)
@@ -74,8 +74,10 @@ struct TcCfg {
     static constexpr uint32_t QCHUNK = 16 * 128;           // 16 rows x 64 k elements
     static constexpr uint32_t QBUF = NKS / 4 * QCHUNK;
     static constexpr uint32_t OFF_Q = OFF_P + 2 * PSTAGE;  // 2 buffers of Q'^T
-    static constexpr uint32_t OFF_RED = OFF_Q + 2 * QBUF;  // [4 warps][8] fp32 + flags
-    static constexpr uint32_t OFF_BAR = OFF_RED + 4 * 8 * 4 + 64;
+    static constexpr uint32_t OFF_SC = OFF_Q + 2 * QBUF;   // 2 stages of V scales [128][NB] fp16
+    static constexpr uint32_t SCSTAGE = kTK * NB * 2;
+    static constexpr uint32_t OFF_RED = OFF_SC + 2 * SCSTAGE;  // [2][4 warps][8] fp32, [2][4] flags
+    static constexpr uint32_t OFF_BAR = OFF_RED + 2 * 4 * 8 * 4 + 64;
     static constexpr uint32_t USED = OFF_BAR + 256;
     static constexpr uint32_t SMEM = USED + 1024;
     static_assert(NKS % 4 == 0, "k-steps per chunk");
@@ -85,12 +87,14 @@ struct TcCfg {
 };
 
 struct TcBars {
-    uint64_t kp_full, kp_free;
-    uint64_t s_full[2], s_free[2];
+    uint64_t kp_full[2];
+    uint64_t s_full, s_free;
     uint64_t v_full[2], p_full[2], pv_done[2];
     uint64_t q_full[2];
     uint64_t o_free;
-    uint64_t red[2];  // K-group exchanges (flag, then maxima)
+    // K-group exchanges, by tile parity: the rescale flags, the maxima; and
+    // the row sums of a piece's epilogue
+    uint64_t xf[2], xm[2], xl;
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -195,6 +199,23 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void reg_fence16(uint32_t *r) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
+}
+
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t *r) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
@@ -204,21 +225,20 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t *r) {
 }
 
 // The sequence of (piece, tile) a block walks, the same in every role: the
-// pieces of its run [T0, T1) of the job, and the tiles of each piece.
+// pieces of its run [bid C, min(T, bid C + C)) of the job, and the tiles of
+// each piece.
 struct TcSeq {
-    long long Tc, T1, A;
-    int u, g, p, j, j1, e, bid;
+    long long Tc;  // job index of the current tile
+    int u, g, p, j, j1, e;
     Q4Tiles tl;
     int piece;  // pieces started so far - 1
     int i;      // tile index within the piece
     bool valid;
 
-    __device__ void start(const DecodeParams &P, const Q4Job &J, int bid_, long long slot_base,
+    __device__ void start(const DecodeParams &P, const Q4Job &J, int bid, long long slot_base,
                           int u0) {
-        bid = bid_;
-        T1 = min(J.T, static_cast<long long>(bid) * J.C + J.C);
         Tc = static_cast<long long>(bid) * J.C;
-        valid = Tc < T1 && u0 >= 0;
+        valid = Tc < J.T && u0 >= 0;
         piece = -1;
         if (!valid) return;
         u = u0;
@@ -227,10 +247,11 @@ struct TcSeq {
         const long long local = Tc - slot_base;
         g = static_cast<int>(local / tl.count());
         j = static_cast<int>(local % tl.count());
-        A = slot_base + static_cast<long long>(g) * tl.count();
-        begin_piece(J);
+        begin_piece(J, bid, slot_base + static_cast<long long>(g) * tl.count());
     }
-    __device__ void begin_piece(const Q4Job &J) {
+    // a.k.a. the piece's pair starts at job index A
+    __device__ void begin_piece(const Q4Job &J, int bid, long long A) {
+        const long long T1 = min(J.T, static_cast<long long>(bid) * J.C + J.C);
         j1 = static_cast<int>(min(static_cast<long long>(tl.count()), j + (T1 - Tc)));
         e = static_cast<int>(bid - A / J.C);
         ++piece;
@@ -240,8 +261,9 @@ struct TcSeq {
     __device__ bool last() const { return j + i + 1 == j1; }
     __device__ int key0() const { return kTK * tl.kt(j + i); }
     // next tile; false at the end of the run
-    __device__ bool next(const DecodeParams &P, const Q4Job &J) {
+    __device__ bool next(const DecodeParams &P, const Q4Job &J, int bid) {
         ++Tc;
+        const long long T1 = min(J.T, static_cast<long long>(bid) * J.C + J.C);
         if (Tc >= T1) {
             valid = false;
             return false;
@@ -251,7 +273,6 @@ struct TcSeq {
             return true;
         }
         // the next pair with tiles
-        A = Tc;
         j = 0;
         do {
             if (++g == P.Hkv) {
@@ -261,7 +282,7 @@ struct TcSeq {
                 tl = q4_tiles(P, p);
             }
         } while (tl.count() == 0);
-        begin_piece(J);
+        begin_piece(J, bid, Tc);
         return true;
     }
 };
@@ -282,8 +303,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     TcBars *bars = reinterpret_cast<TcBars *>(smem + C::OFF_BAR);
-    float *red = reinterpret_cast<float *>(smem + C::OFF_RED);  // [4][8]
-    int *flags = reinterpret_cast<int *>(smem + C::OFF_RED + 4 * 8 * 4);
+    // By tile parity: the group's exchanged maxima (or row sums) [2][4 warps][8]
+    // and rescale flags [2][4]. A K-group thread runs at most one tile ahead
+    // of another (a tile's S^T needs every thread's K' of that tile, written
+    // after the previous tile's exchanges), so two copies never collide.
+    float *red2 = reinterpret_cast<float *>(smem + C::OFF_RED);
+    int *flags2 = reinterpret_cast<int *>(smem + C::OFF_RED + 2 * 4 * 8 * 4);
     __shared__ Q4Job sjob;
     __shared__ long long sbase;
     __shared__ int su;
@@ -308,18 +333,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
     if (static_cast<long long>(bid) * J.C >= J.T || su < 0) return;  // no work for this block
 
     if (threadIdx.x == 0) {
-        mbar_init(&bars->kp_full, 128);
-        mbar_init(&bars->kp_free, 1);
+        mbar_init(&bars->s_full, 1);
+        mbar_init(&bars->s_free, 128);
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars->s_full[s], 1);
-            mbar_init(&bars->s_free[s], 128);
+            mbar_init(&bars->kp_full[s], 128);
             mbar_init(&bars->v_full[s], 128);
             mbar_init(&bars->p_full[s], 128);
             mbar_init(&bars->pv_done[s], 1);
             mbar_init(&bars->q_full[s], 128);
-            mbar_init(&bars->red[s], 128);
+            mbar_init(&bars->xf[s], 128);
+            mbar_init(&bars->xm[s], 128);
         }
         mbar_init(&bars->o_free, 128);
+        mbar_init(&bars->xl, 128);
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
         mbar_fence_init();
@@ -366,50 +392,47 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
                 tc_commit(&bars->pv_done[st]);
                 return true;
             };
-            int t = 0;
-            int prev_piece = -1;
-            bool prev_pending = false;  // PV of tile t - 1 not yet issued
-            bool prev_fresh = false;
-            for (; ok && sq.valid; ++t) {
-                if (sq.first()) {
-                    ok = mbar_wait(&bars->q_full[sq.piece & 1], (sq.piece >> 1) & 1, abort, P.err);
-                    if (!ok) break;
-                }
-                ok = mbar_wait(&bars->kp_full, t & 1, abort, P.err);
-                if (ok && t >= 2) ok = mbar_wait(&bars->s_free[t & 1], ((t - 2) >> 1) & 1, abort, P.err);
-                if (!ok) break;
+            // S^T(t) = K'(t) . Q'^T: per block pair, the lo, hi and bias k-steps
+            // of both blocks. sp: the sequence positioned at tile t.
+            auto issue_s = [&](int t, const TcSeq &sp) -> bool {
+                if (sp.first() &&
+                    !mbar_wait(&bars->q_full[sp.piece & 1], (sp.piece >> 1) & 1, abort, P.err))
+                    return false;
+                if (!mbar_wait(&bars->kp_full[t & 1], (t >> 1) & 1, abort, P.err)) return false;
+                if (t >= 1 && !mbar_wait(&bars->s_free, (t - 1) & 1, abort, P.err)) return false;
                 tc_fence_after();
-                // S^T = K' . Q'^T: per block pair, the lo, hi and bias k-steps of both blocks
-                const uint32_t qb = sQ + (sq.piece & 1) * C::QBUF;
-                const uint32_t sd = tmem + ((t & 1) ? C::S1 : C::S0);
+                const uint32_t qb = sQ + (sp.piece & 1) * C::QBUF;
+                const uint32_t ka = (t & 1) ? C::KA1 : C::KA0;
 #pragma unroll
                 for (int b = 0; b < NB; ++b) {
 #pragma unroll
                     for (int k3 = 0; k3 < 3; ++k3) {
                         const int ks = k3 < 2 ? 2 * b + k3 : 2 * NB + b;
-                        const uint64_t bd = desc_sw128(qb + (ks >> 2) * C::QCHUNK + (ks & 3) * 32, 16, 1024);
-                        const uint32_t a = tmem + (k3 < 2 ? C::KA + 16 * b + 8 * k3 : C::BA);
-                        mma_ts(sd + 16 * (b >> 1), a, bd, C::IDESC_S,
+                        const uint64_t bd =
+                            desc_sw128(qb + (ks >> 2) * C::QCHUNK + (ks & 3) * 32, 16, 1024);
+                        const uint32_t a = tmem + (k3 < 2 ? ka + 16 * b + 8 * k3 : C::BA);
+                        mma_ts(tmem + C::S + 16 * (b >> 1), a, bd, C::IDESC_S,
                                ((b & 1) == 0 && k3 == 0) ? 0u : 1u);
                     }
                 }
-                tc_commit(&bars->kp_free);
-                tc_commit(&bars->s_full[t & 1]);
-                if (prev_pending) {
-                    ok = issue_pv(t - 1, prev_fresh, prev_piece);
+                tc_commit(&bars->s_full);
+                return true;
+            };
+            // S(t + 1) is issued before PV(t), so that it runs while the K
+            // group does the softmax of tile t.
+            TcSeq nx = sq;  // positioned at tile t + 1
+            int t = 0;
+            ok = issue_s(0, sq);
+            bool more = ok && nx.next(P, J, bid);
+            for (; ok; ++t) {
+                if (more) {
+                    ok = issue_s(t + 1, nx);
                     if (!ok) break;
-                    prev_pending = false;
                 }
-                if (sq.last()) {
-                    // the piece's epilogue waits for this PV: issue it now
-                    ok = issue_pv(t, sq.first(), sq.piece);
-                    if (!ok) break;
-                } else {
-                    prev_pending = true;
-                    prev_fresh = sq.first();
-                    prev_piece = sq.piece;
-                }
-                sq.next(P, J);
+                ok = issue_pv(t, sq.first(), sq.piece);
+                if (!ok || !more) break;
+                sq.next(P, J, bid);
+                more = nx.next(P, J, bid);
             }
             // every MMA issued must complete before TMEM is released
             tc_commit(&bars->drain);
@@ -426,49 +449,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
             tmem_st8(tmem + lane_base + C::BA, bias_a);
         }
         const uint32_t magic = kMagic;
-        uint32_t w[ROWW];  // raw K row of tile t (then of tile t + 1)
-        TcSeq pf = sq;     // the tile whose row is loaded next
+        uint32_t w[ROWW];  // raw K row of the next tile to turn into K'
+        uint32_t dk[2][NB / 2];  // K block scales (fp16 pairs) of the tiles in the two K' buffers
+        TcSeq pf = sq;     // the tile whose row is in w
         auto row_ptr = [&](const TcSeq &s, const uint8_t *planes) -> const uint8_t * {
             const int key = min(s.key0() + k, s.p);
             return planes + static_cast<size_t>(s.u) * P.plane_bytes + P.body_off +
                    (static_cast<size_t>(s.g) * P.max_seq + key) * ROWB;
         };
-        load_row<ROWW>(w, row_ptr(pf, P.k_planes));
-        float m_ref[8], l_acc[8];
-        int red_uses = 0;
-        bool ok = true;
-        int t = 0;
-        // one tile; the two register buffers alternate, so the loop is
-        // unrolled by two and every buffer index is a constant
-        auto step = [&](auto cur_c) -> bool {
-            constexpr int cur = decltype(cur_c)::value;
-            if (sq.first()) {
-#pragma unroll
-                for (int h = 0; h < 8; ++h) {
-                    m_ref[h] = -INFINITY;
-                    l_acc[h] = 0.0f;
-                }
-            }
-            // V block scales of this key (the P' factors), loaded early
-            const uint8_t *vrow = row_ptr(sq, P.v_planes);
-            uint32_t dvb[NB];
-#pragma unroll
-            for (int b = 0; b < NB; ++b)
-                dvb[b] = __ldg(reinterpret_cast<const unsigned short *>(vrow + 18 * b));
-            // ---- K' of tile t into TMEM, once S(t-1) has read the previous one
-            if (t >= 1) {
-                ok = mbar_wait(&bars->kp_free, (t - 1) & 1, abort, P.err);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) return false;
-                tc_fence_after();
-            }
-            float dk[NB];
+        // K' of the tile in w into buffer kb (its S^T MMAs must be done with it)
+        auto write_kprime = [&](int kb, uint32_t (&dks)[NB / 2]) {
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
                 uint32_t x[4];
-                uint32_t (&wr)[ROWW] = w;
-                block_words<ROWW>(wr, b, x);
-                dk[b] = h2f(block_scale_bits<ROWW>(wr, b));
+                block_words<ROWW>(w, b, x);
+                if (b & 1)
+                    dks[b >> 1] |= block_scale_bits<ROWW>(w, b) << 16;
+                else
+                    dks[b >> 1] = block_scale_bits<ROWW>(w, b);
                 uint32_t col[16];
 #pragma unroll
                 for (int wi = 0; wi < 4; ++wi) {
@@ -478,40 +476,59 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
                     col[8 + 2 * wi] = and_or<0x00F000F0u>(x[wi], magic);
                     col[8 + 2 * wi + 1] = and_or<0x00F000F0u>(y, magic);
                 }
-                tmem_st16(tmem + lane_base + C::KA + 16 * b, col);
+                tmem_st16(tmem + lane_base + (kb ? C::KA1 : C::KA0) + 16 * b, col);
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&bars->kp_full);
-            // the raw row of tile t + 1: it lands while tile t is scored
-            if (pf.valid && pf.next(P, J)) load_row<ROWW>(w, row_ptr(pf, P.k_planes));
-
-            // ---- scores of tile t
-            ok = mbar_wait(&bars->s_full[t & 1], (t >> 1) & 1, abort, P.err);
+            mbar_arrive(&bars->kp_full[kb]);
+        };
+        load_row<ROWW>(w, row_ptr(pf, P.k_planes));
+        write_kprime(0, dk[0]);
+        if (pf.next(P, J, bid)) load_row<ROWW>(w, row_ptr(pf, P.k_planes));
+        float m_ref[8], l_acc[8];
+        int xm_uses[2] = {0, 0}, xl_uses = 0;
+        bool ok = true;
+        int t = 0;
+        // one tile; the K' buffers alternate, so the loop is unrolled by two
+        // and every register index is a constant
+        auto step = [&](auto cur_c) -> bool {
+            constexpr int cur = decltype(cur_c)::value;
+            if (sq.first()) {
+#pragma unroll
+                for (int h = 0; h < 8; ++h) {
+                    m_ref[h] = -INFINITY;
+                    l_acc[h] = 0.0f;
+                }
+            }
+            // ---- S^T(t): s_h = sum_b d_b acc_b,h, 32 columns (4 blocks) at a time
+            ok = mbar_wait(&bars->s_full, t & 1, abort, P.err);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) return false;
             tc_fence_after();
-            // s_h = sum_b d_b acc_b,h, 32 columns (4 blocks) at a time
-            const uint32_t scol = tmem + lane_base + ((t & 1) ? C::S1 : C::S0);
             float s[8];
 #pragma unroll
             for (int h = 0; h < 8; ++h) s[h] = 0.0f;
 #pragma unroll
-            for (int half = 0; half < static_cast<int>(C::SW) / 32; ++half) {
-                uint32_t sr[32];
-                tmem_ld32(scol + 32 * half, sr);
+            for (int pp = 0; pp < static_cast<int>(C::NP); ++pp) {
+                uint32_t sr[16];  // blocks 2 pp (columns 0-7) and 2 pp + 1 (8-15)
+                tmem_ld16(tmem + lane_base + C::S + 16 * pp, sr);
                 tmem_wait_ld();
-                reg_fence32(sr);
+                reg_fence16(sr);
+                const float d0 = h2f(dk[cur][pp] & 0xFFFFu), d1 = h2f(dk[cur][pp] >> 16);
 #pragma unroll
-                for (int bb = 0; bb < 4; ++bb) {
-                    const int b = 4 * half + bb;
-#pragma unroll
-                    for (int h = 0; h < 8; ++h)
-                        s[h] = fmaf(dk[b], __uint_as_float(sr[8 * bb + h]), s[h]);
+                for (int h = 0; h < 8; ++h) {
+                    s[h] = fmaf(d0, __uint_as_float(sr[h]), s[h]);
+                    s[h] = fmaf(d1, __uint_as_float(sr[8 + h]), s[h]);
                 }
             }
             tc_fence_before();
-            mbar_arrive(&bars->s_free[t & 1]);
+            mbar_arrive(&bars->s_free);
+            // ---- K'(t + 1) into the other buffer (S^T(t - 1), its last
+            // reader, is done), so that S^T(t + 1) runs during this softmax
+            if (pf.valid) {
+                write_kprime(cur ^ 1, dk[cur ^ 1]);
+                if (pf.next(P, J, bid)) load_row<ROWW>(w, row_ptr(pf, P.k_planes));
+            }
             const int key = sq.key0() + k;
             const int p = sq.p;
             const bool vis = key <= p && key_visible(p, key, P.sink, P.win) &&
@@ -522,10 +539,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
             bool need = false;
 #pragma unroll
             for (int h = 0; h < 8; ++h) need |= s[h] > m_ref[h] + kRescale;
+            float *red = red2 + (t & 1) * 32;
+            int *flags = flags2 + (t & 1) * 4;
             const unsigned nb_ = __ballot_sync(0xffffffffu, need);
             if (lane == 0) flags[warp] = nb_ != 0;
-            ok = group_sync(&bars->red[red_uses & 1], (red_uses >> 1) & 1, abort, P.err);
-            ++red_uses;
+            ok = group_sync(&bars->xf[t & 1], (t >> 1) & 1, abort, P.err);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) return false;
             const bool any = flags[0] | flags[1] | flags[2] | flags[3];
@@ -545,8 +563,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
                         if (lane == h) v = mx[h];
                     red[warp * 8 + lane] = v;
                 }
-                ok = group_sync(&bars->red[red_uses & 1], (red_uses >> 1) & 1, abort, P.err);
-                ++red_uses;
+                ok = group_sync(&bars->xm[t & 1], xm_uses[cur] & 1, abort, P.err);
+                ++xm_uses[cur];
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) return false;
                 float corr[8];
@@ -564,8 +582,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
                         m_ref[h] = tmax;
                     }
                 }
-                // The next exchange overwrites red[]: every thread has read it
-                // once the group passes that barrier (uses alternate barriers).
                 if (resc && !sq.first()) {
                     // O holds P'V of tiles before t: rescale it after PV(t - 1)
                     ok = mbar_wait(&bars->pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort, P.err);
@@ -590,24 +606,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
                     tmem_wait_st();
                 }
             }
-            float pr[8];
+            float (&pr)[8] = s;  // the weights replace the scores
 #pragma unroll
             for (int h = 0; h < 8; ++h) {
                 pr[h] = vis ? ex2(s[h] - m_ref[h]) : 0.0f;
                 l_acc[h] += pr[h];
             }
-            // ---- P' of tile t: p_h * dv_b as fp16, [key][block][head]
-            if (t >= 2) {
+            // ---- P' of tile t: p_h * dv_b as fp16, [key][block][head]; the V
+            // scales come from the V group with V'(t), the stage is free once
+            // PV(t - 2) is done
+            ok = mbar_wait(&bars->v_full[t & 1], (t >> 1) & 1, abort, P.err);
+            if (ok && t >= 2)
                 ok = mbar_wait(&bars->pv_done[t & 1], ((t - 2) >> 1) & 1, abort, P.err);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) return false;
-            }
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) return false;
+            const uint4 dvw = *reinterpret_cast<const uint4 *>(smem + C::OFF_SC + (t & 1) * C::SCSTAGE + k * 16);
+            const uint32_t dvp[4] = {dvw.x, dvw.y, dvw.z, dvw.w};  // blocks (0,1), (2,3), ...
             const uint32_t ph[4] = {pack_half2(pr[0], pr[1]), pack_half2(pr[2], pr[3]),
                                     pack_half2(pr[4], pr[5]), pack_half2(pr[6], pr[7])};
             uint8_t *prow = smem + C::OFF_P + (t & 1) * C::PSTAGE + k * 128;
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
-                const uint32_t d2 = vis ? (dvb[b] | (dvb[b] << 16)) : 0u;
+                const uint32_t dv = (b & 1) ? (dvp[b >> 1] >> 16) : (dvp[b >> 1] & 0xFFFFu);
+                const uint32_t d2 = vis ? (dv | (dv << 16)) : 0u;
                 uint4 v;
                 v.x = hmul2u(ph[0], d2);
                 v.y = hmul2u(ph[1], d2);
@@ -620,84 +641,68 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
             mbar_arrive(&bars->p_full[t & 1]);
 
             if (sq.last()) {
-                // ---- epilogue of the piece: O^T rows of this lane, l, m
+                // ---- epilogue of the piece: l over the group's keys, then the
+                // O^T rows of this lane (relative to 2^m_ref, like l), m. Every
+                // thread of the group read red[] (the maxima) before its p_full
+                // arrival, so once PV(t) is done red[] may take the sums.
                 ok = mbar_wait(&bars->pv_done[t & 1], (t >> 1) & 1, abort, P.err);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) return false;
                 tc_fence_after();
-                float ov[MT][8];
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    // V' position 128 mt + k of this lane: its block b keeps
-                    // O^T columns 8 b .. 8 b + 7 (its own scale)
-                    const int b = (128 * mt + k) >> 5;
-                    uint32_t o[32];
-                    tmem_ld32(tmem + lane_base + C::O + 64 * mt + 32 * (b >> 2), o);
-                    tmem_wait_ld();
-                    reg_fence32(o);
-#pragma unroll
-                    for (int h = 0; h < 8; ++h) ov[mt][h] = __uint_as_float(o[8 * (b & 3) + h]);
-                }
-                tc_fence_before();
-                mbar_arrive(&bars->o_free);
-                // l: sum over the group's keys
-                float lt[8];
 #pragma unroll
                 for (int h = 0; h < 8; ++h) {
                     float v = l_acc[h];
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                    lt[h] = v;
+                    if (lane == h) red[warp * 8 + h] = v;
                 }
-                if (lane < 8) {
-                    float v = lt[0];
-#pragma unroll
-                    for (int h = 1; h < 8; ++h)
-                        if (lane == h) v = lt[h];
-                    red[warp * 8 + lane] = v;
-                }
-                ok = group_sync(&bars->red[red_uses & 1], (red_uses >> 1) & 1, abort, P.err);
-                ++red_uses;
+                ok = group_sync(&bars->xl, xl_uses & 1, abort, P.err);
+                ++xl_uses;
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) return false;
                 const size_t head0 = static_cast<size_t>(sq.u) * P.Hq + static_cast<size_t>(sq.g) * G;
                 const int e = sq.e;
+#pragma unroll 1
+                for (int mt = 0; mt < MT; ++mt) {
+                    // V' position 128 mt + k of this lane: its block b keeps
+                    // O^T columns 8 b .. 8 b + 7 (its own scale)
+                    const int P0 = 128 * mt + k;
+                    const int b = P0 >> 5;
+                    const int dim = 32 * b + q4_elem(b, P0 & 31);
+                    uint32_t o[32];
+                    tmem_ld32(tmem + lane_base + C::O + 64 * mt + 32 * (b >> 2), o);
+                    tmem_wait_ld();
+                    reg_fence32(o);
 #pragma unroll
-                for (int h = 0; h < 8; ++h) {
-                    if (h >= G) break;
-                    const float L = (red[h] + red[8 + h]) + (red[16 + h] + red[24 + h]);
-                    const size_t row = (head0 + h) * P.stride + e;
-                    if (k == 0) {
-                        P.ws_m[row] = (L > 0.0f) ? m_ref[h] * 0.69314718055994531f : -INFINITY;
-                        P.ws_l[row] = L;
-                    }
-                    if (L > 0.0f) {
-                        const float inv1 = 1.0f;  // acc stays relative to 2^m_ref, like l
-#pragma unroll
-                        for (int mt = 0; mt < MT; ++mt) {
-                            const int P0 = 128 * mt + k;
-                            const int b = P0 >> 5;
-                            const int dim = 32 * b + q4_elem(b, P0 & 31);
-                            P.ws_acc[row * HD + dim] = ov[mt][h] * inv1;
-                        }
+                    for (int h = 0; h < 8; ++h) {
+                        const float L = (red[h] + red[8 + h]) + (red[16 + h] + red[24 + h]);
+                        if (h < G && L > 0.0f)
+                            P.ws_acc[((head0 + h) * P.stride + e) * HD + dim] =
+                                __uint_as_float(o[8 * (b & 3) + h]);
                     }
                 }
-                // the next exchange must not overwrite red[] before all have read it
-                ok = group_sync(&bars->red[red_uses & 1], (red_uses >> 1) & 1, abort, P.err);
-                ++red_uses;
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) return false;
-                if (k == 0) {
+                tc_fence_before();
+                mbar_arrive(&bars->o_free);
+                if (k < G) {
+                    const float L = (red[k] + red[8 + k]) + (red[16 + k] + red[24 + k]);
+                    const size_t row = (head0 + k) * P.stride + e;
+                    float mk = m_ref[0];
+#pragma unroll
+                    for (int h = 1; h < 8; ++h)
+                        if (k == h) mk = m_ref[h];
+                    P.ws_m[row] = (L > 0.0f) ? mk * 0.69314718055994531f : -INFINITY;
+                    P.ws_l[row] = L;
+                }
+                if (sq.j1 == sq.tl.count()) {
                     // later body entries of the pair: empty
-                    if (sq.j1 == sq.tl.count())
-                        for (int ee = e + 1; ee < J.Eb; ++ee)
-                            for (int h = 0; h < G; ++h) {
-                                P.ws_m[(head0 + h) * P.stride + ee] = -INFINITY;
-                                P.ws_l[(head0 + h) * P.stride + ee] = 0.0f;
-                            }
+                    for (int i = k; i < G * (J.Eb - e - 1); i += 128) {
+                        const size_t idx = (head0 + i % G) * P.stride + e + 1 + i / G;
+                        P.ws_m[idx] = -INFINITY;
+                        P.ws_l[idx] = 0.0f;
+                    }
                 }
             }
-            sq.next(P, J);
+            sq.next(P, J, bid);
             ++t;
             return true;
         };
@@ -716,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
                    (static_cast<size_t>(s.g) * P.max_seq + key) * ROWB;
         };
         load_row<ROWW>(w[0], row_ptr(pf));
-        if (pf.next(P, J)) load_row<ROWW>(w[1], row_ptr(pf));
+        if (pf.next(P, J, bid)) load_row<ROWW>(w[1], row_ptr(pf));
         const uint32_t magic = kMagic;
         const uint32_t neg1032 = 0xE408E408u;  // (-1032, -1032)
         const uint32_t sixteenth = 0x2C002C00u;  // (1/16, 1/16)
@@ -811,10 +816,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
                         make_uint4(src[0], src[1], src[2], src[3]);
                 }
             }
+            {   // the key's V block scales, for the K group's P'
+                uint32_t sc[NB / 2];
+#pragma unroll
+                for (int b2 = 0; b2 < NB / 2; ++b2)
+                    sc[b2] = block_scale_bits<ROWW>(w[cur], 2 * b2) |
+                             (block_scale_bits<ROWW>(w[cur], 2 * b2 + 1) << 16);
+                *reinterpret_cast<uint4 *>(smem + C::OFF_SC + (t & 1) * C::SCSTAGE + k * 16) =
+                    make_uint4(sc[0], sc[1], sc[2], sc[3]);
+            }
             fence_proxy_async_smem();
             mbar_arrive(&bars->v_full[t & 1]);
-            if (pf.valid && pf.next(P, J)) load_row<ROWW>(w[cur], row_ptr(pf));
-            sq.next(P, J);
+            if (pf.valid && pf.next(P, J, bid)) load_row<ROWW>(w[cur], row_ptr(pf));
+            sq.next(P, J, bid);
             ++t;
             return true;
         };
