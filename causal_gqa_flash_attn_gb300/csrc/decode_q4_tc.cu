@@ -36,8 +36,6 @@
 // to decode_q4_kernel's auxiliary blocks.
 #include <cuda_fp16.h>
 
-#include <type_traits>
-
 #include "decode_common.cuh"
 
 namespace fa {
@@ -295,6 +293,70 @@ __device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t parity, volat
     return mbar_wait(bar, parity, abort, err);
 }
 
+// Row k of the current tile of s in a K or V plane (keys past p read row p).
+template <int ROWB>
+__device__ __forceinline__ const uint8_t *tile_row(const DecodeParams &P, const TcSeq &s, int k,
+                                                   const uint8_t *planes) {
+    const int key = min(s.key0() + k, s.p);
+    return planes + static_cast<size_t>(s.u) * P.plane_bytes + P.body_off +
+           (static_cast<size_t>(s.g) * P.max_seq + key) * ROWB;
+}
+
+// Q'^T of (slot u, kv head g) into qbase: thread k (of 128) writes row
+// n = k & 15 for block b = k >> 4, its lo, hi and bias k-steps. Rows 0-7 hold
+// the group's heads for even blocks' dims, rows 8-15 for odd blocks' dims
+// (zeros elsewhere and for heads >= G); the lo step holds fp16(q) and the hi
+// step fp16(q / 16) in the K' element order; the bias step holds -(1032 sum
+// lo + 1152 sum hi) as 2^10 t1 + t2 + 2^-10 t3. Kept out of line: it runs once
+// per piece.
+template <int HD>
+__device__ __noinline__ void write_qt(const DecodeParams &P, uint8_t *qbase, int u, int g, int G,
+                                      int k) {
+    using C = TcCfg<HD>;
+    constexpr int NB = C::NB;
+    const int n = k & 15, b = k >> 4;
+    if (b >= NB) return;
+    const int h = n & 7;
+    const bool act = ((n >> 3) == (b & 1)) && h < G;
+    const float *qr =
+        P.q + (static_cast<size_t>(u) * P.Hq + static_cast<size_t>(g) * G + h) * HD + 32 * b;
+    auto put = [&](int ks, int kp, uint32_t pair) {
+        const int K = ks * 16 + kp;  // even
+        const int c = K >> 6, el = K & 63;
+        *reinterpret_cast<uint32_t *>(qbase + c * C::QCHUNK + n * 128 +
+                                      (((el >> 3) ^ (n & 7)) << 4) + (el & 7) * 2) = pair;
+    };
+    double bias = 0.0;
+    for (int hi = 0; hi < 2; ++hi) {
+        for (int kp = 0; kp < 16; kp += 2) {
+            uint32_t pair = 0u;
+            if (act) {
+                const float f = hi ? 0.0625f : 1.0f;
+                const __half a0 = __float2half_rn(qr[q4_elem(b, 16 * hi + kp)] * f);
+                const __half a1 = __float2half_rn(qr[q4_elem(b, 16 * hi + kp + 1)] * f);
+                bias += (hi ? 1152.0 : 1032.0) *
+                        (static_cast<double>(__half2float(a0)) + __half2float(a1));
+                pair = static_cast<uint32_t>(__half_as_ushort(a0)) |
+                       (static_cast<uint32_t>(__half_as_ushort(a1)) << 16);
+            }
+            put(2 * b + hi, kp, pair);
+        }
+    }
+    const double nb0 = -bias;
+    const __half t1 = __double2half(nb0 * 0x1p-10);
+    const double r1 = nb0 - 1024.0 * static_cast<double>(__half2float(t1));
+    const __half t2 = __double2half(r1);
+    const double r2 = r1 - static_cast<double>(__half2float(t2));
+    const __half t3 = __double2half(r2 * 1024.0);
+    const uint32_t p01 = act ? (static_cast<uint32_t>(__half_as_ushort(t1)) |
+                                (static_cast<uint32_t>(__half_as_ushort(t2)) << 16))
+                             : 0u;
+    const uint32_t p23 = act ? static_cast<uint32_t>(__half_as_ushort(t3)) : 0u;
+    put(2 * NB + b, 0, p01);
+    put(2 * NB + b, 2, p23);
+    for (int kp = 4; kp < 16; kp += 2) put(2 * NB + b, kp, 0u);
+}
+
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeParams P) {
     using C = TcCfg<HD>;
@@ -450,13 +512,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
         }
         const uint32_t magic = kMagic;
         uint32_t w[ROWW];  // raw K row of the next tile to turn into K'
-        uint32_t dk[2][NB / 2];  // K block scales (fp16 pairs) of the tiles in the two K' buffers
+        uint32_t dk[NB / 2], dk_next[NB / 2];  // K block scales (fp16 pairs): tiles t, t + 1
         TcSeq pf = sq;     // the tile whose row is in w
-        auto row_ptr = [&](const TcSeq &s, const uint8_t *planes) -> const uint8_t * {
-            const int key = min(s.key0() + k, s.p);
-            return planes + static_cast<size_t>(s.u) * P.plane_bytes + P.body_off +
-                   (static_cast<size_t>(s.g) * P.max_seq + key) * ROWB;
-        };
         // K' of the tile in w into buffer kb (its S^T MMAs must be done with it)
         auto write_kprime = [&](int kb, uint32_t (&dks)[NB / 2]) {
 #pragma unroll
@@ -482,17 +539,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
             tc_fence_before();
             mbar_arrive(&bars->kp_full[kb]);
         };
-        load_row<ROWW>(w, row_ptr(pf, P.k_planes));
-        write_kprime(0, dk[0]);
-        if (pf.next(P, J, bid)) load_row<ROWW>(w, row_ptr(pf, P.k_planes));
+        load_row<ROWW>(w, tile_row<ROWB>(P, pf, k, P.k_planes));
+        write_kprime(0, dk);
+        if (pf.next(P, J, bid)) load_row<ROWW>(w, tile_row<ROWB>(P, pf, k, P.k_planes));
         float m_ref[8], l_acc[8];
-        int xm_uses[2] = {0, 0}, xl_uses = 0;
+        int xm_uses0 = 0, xm_uses1 = 0, xl_uses = 0;
         bool ok = true;
         int t = 0;
-        // one tile; the K' buffers alternate, so the loop is unrolled by two
-        // and every register index is a constant
-        auto step = [&](auto cur_c) -> bool {
-            constexpr int cur = decltype(cur_c)::value;
+        for (; ok && sq.valid; ++t) {
+            const int cur = t & 1;  // K' buffer of tile t
             if (sq.first()) {
 #pragma unroll
                 for (int h = 0; h < 8; ++h) {
@@ -503,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
             // ---- S^T(t): s_h = sum_b d_b acc_b,h, 32 columns (4 blocks) at a time
             ok = mbar_wait(&bars->s_full, t & 1, abort, P.err);
             ok = __all_sync(0xffffffffu, ok);
-            if (!ok) return false;
+            if (!ok) break;
             tc_fence_after();
             float s[8];
 #pragma unroll
@@ -514,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
                 tmem_ld16(tmem + lane_base + C::S + 16 * pp, sr);
                 tmem_wait_ld();
                 reg_fence16(sr);
-                const float d0 = h2f(dk[cur][pp] & 0xFFFFu), d1 = h2f(dk[cur][pp] >> 16);
+                const float d0 = h2f(dk[pp] & 0xFFFFu), d1 = h2f(dk[pp] >> 16);
 #pragma unroll
                 for (int h = 0; h < 8; ++h) {
                     s[h] = fmaf(d0, __uint_as_float(sr[h]), s[h]);
@@ -526,8 +581,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
             // ---- K'(t + 1) into the other buffer (S^T(t - 1), its last
             // reader, is done), so that S^T(t + 1) runs during this softmax
             if (pf.valid) {
-                write_kprime(cur ^ 1, dk[cur ^ 1]);
-                if (pf.next(P, J, bid)) load_row<ROWW>(w, row_ptr(pf, P.k_planes));
+                write_kprime(cur ^ 1, dk_next);
+                if (pf.next(P, J, bid)) load_row<ROWW>(w, tile_row<ROWB>(P, pf, k, P.k_planes));
             }
             const int key = sq.key0() + k;
             const int p = sq.p;
@@ -545,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
             if (lane == 0) flags[warp] = nb_ != 0;
             ok = group_sync(&bars->xf[t & 1], (t >> 1) & 1, abort, P.err);
             ok = __all_sync(0xffffffffu, ok);
-            if (!ok) return false;
+            if (!ok) break;
             const bool any = flags[0] | flags[1] | flags[2] | flags[3];
             if (any) {
                 float mx[8];
@@ -563,10 +618,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
                         if (lane == h) v = mx[h];
                     red[warp * 8 + lane] = v;
                 }
-                ok = group_sync(&bars->xm[t & 1], xm_uses[cur] & 1, abort, P.err);
-                ++xm_uses[cur];
+                ok = group_sync(&bars->xm[t & 1], (cur ? xm_uses1 : xm_uses0) & 1, abort, P.err);
+                if (cur) ++xm_uses1; else ++xm_uses0;
                 ok = __all_sync(0xffffffffu, ok);
-                if (!ok) return false;
+                if (!ok) break;
                 float corr[8];
                 bool resc = false;
 #pragma unroll
@@ -586,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
                     // O holds P'V of tiles before t: rescale it after PV(t - 1)
                     ok = mbar_wait(&bars->pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort, P.err);
                     ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) return false;
+                    if (!ok) break;
                     tc_fence_after();
 #pragma unroll 1
                     for (int mt = 0; mt < MT; ++mt) {
@@ -619,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
             if (ok && t >= 2)
                 ok = mbar_wait(&bars->pv_done[t & 1], ((t - 2) >> 1) & 1, abort, P.err);
             ok = __all_sync(0xffffffffu, ok);
-            if (!ok) return false;
+            if (!ok) break;
             const uint4 dvw = *reinterpret_cast<const uint4 *>(smem + C::OFF_SC + (t & 1) * C::SCSTAGE + k * 16);
             const uint32_t dvp[4] = {dvw.x, dvw.y, dvw.z, dvw.w};  // blocks (0,1), (2,3), ...
             const uint32_t ph[4] = {pack_half2(pr[0], pr[1]), pack_half2(pr[2], pr[3]),
@@ -647,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
                 // arrival, so once PV(t) is done red[] may take the sums.
                 ok = mbar_wait(&bars->pv_done[t & 1], (t >> 1) & 1, abort, P.err);
                 ok = __all_sync(0xffffffffu, ok);
-                if (!ok) return false;
+                if (!ok) break;
                 tc_fence_after();
 #pragma unroll
                 for (int h = 0; h < 8; ++h) {
@@ -659,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
                 ok = group_sync(&bars->xl, xl_uses & 1, abort, P.err);
                 ++xl_uses;
                 ok = __all_sync(0xffffffffu, ok);
-                if (!ok) return false;
+                if (!ok) break;
                 const size_t head0 = static_cast<size_t>(sq.u) * P.Hq + static_cast<size_t>(sq.g) * G;
                 const int e = sq.e;
 #pragma unroll 1
@@ -702,92 +757,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
                     }
                 }
             }
+#pragma unroll
+            for (int i = 0; i < NB / 2; ++i) dk[i] = dk_next[i];
             sq.next(P, J, bid);
-            ++t;
-            return true;
-        };
-        while (ok && sq.valid) {
-            ok = step(std::integral_constant<int, 0>{});
-            if (ok && sq.valid) ok = step(std::integral_constant<int, 1>{});
         }
     } else {
         // ------------------------------------------------ V group: V', Q'^T
         const int k = threadIdx.x - 128;
-        uint32_t w[2][ROWW];
+        uint32_t w[ROWW];  // raw V row of tile t (then of tile t + 1)
         TcSeq pf = sq;
-        auto row_ptr = [&](const TcSeq &s) -> const uint8_t * {
-            const int key = min(s.key0() + k, s.p);
-            return P.v_planes + static_cast<size_t>(s.u) * P.plane_bytes + P.body_off +
-                   (static_cast<size_t>(s.g) * P.max_seq + key) * ROWB;
-        };
-        load_row<ROWW>(w[0], row_ptr(pf));
-        if (pf.next(P, J, bid)) load_row<ROWW>(w[1], row_ptr(pf));
+        load_row<ROWW>(w, tile_row<ROWB>(P, pf, k, P.v_planes));
         const uint32_t magic = kMagic;
-        const uint32_t neg1032 = 0xE408E408u;  // (-1032, -1032)
+        const uint32_t neg1032 = 0xE408E408u;    // (-1032, -1032)
         const uint32_t sixteenth = 0x2C002C00u;  // (1/16, 1/16)
-        const uint32_t neg72 = 0xD480D480u;    // (-72, -72)
+        const uint32_t neg72 = 0xD480D480u;      // (-72, -72)
         bool ok = true;
-        int t = 0;
-        // one tile; the two register buffers alternate, so the loop is
-        // unrolled by two and every buffer index is a constant
-        auto step = [&](auto cur_c) -> bool {
-            constexpr int cur = decltype(cur_c)::value;
-            if (t >= 2) {
+        for (int t = 0; ok && sq.valid; ++t) {
+            if (t >= 2) {  // V'(t - 2), P'(t - 2) and the scales of t - 2 are read
                 ok = mbar_wait(&bars->pv_done[t & 1], ((t - 2) >> 1) & 1, abort, P.err);
                 ok = __all_sync(0xffffffffu, ok);
-                if (!ok) return false;
+                if (!ok) break;
             }
             if (sq.first()) {
-                // ---- Q'^T of this piece's (slot, kv head): thread k writes
-                // row n = k & 15 for block b = k >> 4: its lo, hi and bias k-steps
-                const int n = k & 15, b = k >> 4;
-                const int h = n & 7;
-                const bool act = ((n >> 3) == (b & 1)) && h < G && b < NB;
-                const size_t head = static_cast<size_t>(sq.u) * P.Hq + static_cast<size_t>(sq.g) * G + h;
-                const float *qr = P.q + head * HD + 32 * b;
-                uint8_t *qbase = smem + C::OFF_Q + (sq.piece & 1) * C::QBUF;
-                auto put = [&](int ks, int kp, uint32_t pair) {
-                    const int K = ks * 16 + kp;  // even
-                    const int c = K >> 6, el = K & 63;
-                    *reinterpret_cast<uint32_t *>(qbase + c * C::QCHUNK + n * 128 +
-                                                  ((((el >> 3) ^ (n & 7))) << 4) + (el & 7) * 2) = pair;
-                };
-                if (b < NB) {
-                    double bias = 0.0;
-#pragma unroll
-                    for (int hi = 0; hi < 2; ++hi) {
-#pragma unroll
-                        for (int kp = 0; kp < 16; kp += 2) {
-                            uint32_t pair = 0u;
-                            if (act) {
-                                const float f = hi ? 0.0625f : 1.0f;
-                                const __half a0 = __float2half_rn(qr[q4_elem(b, 16 * hi + kp)] * f);
-                                const __half a1 = __float2half_rn(qr[q4_elem(b, 16 * hi + kp + 1)] * f);
-                                bias += (hi ? 1152.0 : 1032.0) *
-                                        (static_cast<double>(__half2float(a0)) + __half2float(a1));
-                                pair = static_cast<uint32_t>(__half_as_ushort(a0)) |
-                                       (static_cast<uint32_t>(__half_as_ushort(a1)) << 16);
-                            }
-                            put(2 * b + hi, kp, pair);
-                        }
-                    }
-                    // -bias = 2^10 t1 + t2 + 2^-10 t3 with fp16 t1, t2, t3 (k
-                    // elements 0-2 of the bias step, against 2^10, 1, 2^-10)
-                    const double nb0 = -bias;
-                    const __half t1 = __double2half(nb0 * 0x1p-10);
-                    const double r1 = nb0 - 1024.0 * static_cast<double>(__half2float(t1));
-                    const __half t2 = __double2half(r1);
-                    const double r2 = r1 - static_cast<double>(__half2float(t2));
-                    const __half t3 = __double2half(r2 * 1024.0);
-                    const uint32_t p01 = act ? (static_cast<uint32_t>(__half_as_ushort(t1)) |
-                                                (static_cast<uint32_t>(__half_as_ushort(t2)) << 16))
-                                             : 0u;
-                    const uint32_t p23 = act ? static_cast<uint32_t>(__half_as_ushort(t3)) : 0u;
-                    put(2 * NB + b, 0, p01);
-                    put(2 * NB + b, 2, p23);
-#pragma unroll
-                    for (int kp = 4; kp < 16; kp += 2) put(2 * NB + b, kp, 0u);
-                }
+                write_qt<HD>(P, smem + C::OFF_Q + (sq.piece & 1) * C::QBUF, sq.u, sq.g, G, k);
                 fence_proxy_async_smem();
                 mbar_arrive(&bars->q_full[sq.piece & 1]);
             }
@@ -796,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
                 uint32_t x[4];
-                block_words<ROWW>(w[cur], b, x);
+                block_words<ROWW>(w, b, x);
                 uint32_t lo[8], hi[8];
 #pragma unroll
                 for (int wi = 0; wi < 4; ++wi) {
@@ -820,21 +812,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q4_tc_kernel(const DecodeP
                 uint32_t sc[NB / 2];
 #pragma unroll
                 for (int b2 = 0; b2 < NB / 2; ++b2)
-                    sc[b2] = block_scale_bits<ROWW>(w[cur], 2 * b2) |
-                             (block_scale_bits<ROWW>(w[cur], 2 * b2 + 1) << 16);
+                    sc[b2] = block_scale_bits<ROWW>(w, 2 * b2) |
+                             (block_scale_bits<ROWW>(w, 2 * b2 + 1) << 16);
                 *reinterpret_cast<uint4 *>(smem + C::OFF_SC + (t & 1) * C::SCSTAGE + k * 16) =
                     make_uint4(sc[0], sc[1], sc[2], sc[3]);
             }
             fence_proxy_async_smem();
             mbar_arrive(&bars->v_full[t & 1]);
-            if (pf.valid && pf.next(P, J, bid)) load_row<ROWW>(w[cur], row_ptr(pf));
+            // the raw row of tile t + 1: it lands while the K group scores tile t
+            if (pf.valid && pf.next(P, J, bid)) load_row<ROWW>(w, tile_row<ROWB>(P, pf, k, P.v_planes));
             sq.next(P, J, bid);
-            ++t;
-            return true;
-        };
-        while (ok && sq.valid) {
-            ok = step(std::integral_constant<int, 0>{});
-            if (ok && sq.valid) ok = step(std::integral_constant<int, 1>{});
         }
     }
 
