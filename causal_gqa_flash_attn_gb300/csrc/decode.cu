@@ -1239,22 +1239,16 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodeWs &ws, const DecodeS
     if (d.entries > ws.stride) return cudaErrorInvalidValue;
     const int G = a.n_q_heads / a.n_kv_heads;
     if (d.fast) {
-        // The tensor-core kernel computes the body entries over 128-key tiles,
-        // one block per SM; the warp-MMA kernel's auxiliary blocks write the
-        // header, the fp16-shadow and empty entries first. Otherwise the
-        // warp-MMA kernel does everything (32-key tiles, two blocks per SM).
-        const bool tc = q4_tc_supported(a.g.hd, G);
-        P.q4_tile_keys = tc ? q4_tc_tile_keys() : kTileKeys;
-        P.q4_body_blocks = (tc ? 1 : FA_Q4_MIN_BLOCKS) * device_sm_count();
-        cudaError_t e;
+        // 32-key tiles cut over two blocks per SM (one resident wave), after
+        // one auxiliary block per (slot, kv head)
+        P.q4_tile_keys = kTileKeys;
+        P.q4_body_blocks = FA_Q4_MIN_BLOCKS * device_sm_count();
         switch (a.g.hd) {
-            case 64: e = launch_q4<64>(P, !tc, stream); break;
-            case 128: e = launch_q4<128>(P, !tc, stream); break;
-            case 256: e = launch_q4<256>(P, !tc, stream); break;
+            case 64: return launch_q4<64>(P, true, stream);
+            case 128: return launch_q4<128>(P, true, stream);
+            case 256: return launch_q4<256>(P, true, stream);
             default: return cudaErrorInvalidValue;
         }
-        if (e == cudaSuccess && tc) e = launch_q4_tc(P, a.g.hd, stream);
-        return e;
     }
     const bool two = G > 8;
     switch (a.g.hd) {

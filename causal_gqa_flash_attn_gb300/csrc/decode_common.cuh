@@ -156,13 +156,4 @@ static __device__ __forceinline__ void write_empty_range(const DecodeParams &P, 
     }
 }
 
-// The tensor-core Q4_0 decode (decode_q4_tc.cu): head_dim 128 or 256, groups
-// of up to 8 q heads, 16-byte aligned K/V rows per head. It writes the body
-// entries of the job cut into P.q4_tile_keys-key tiles over
-// P.q4_body_blocks blocks (the fp16-shadow entries, empty entries and the
-// workspace header come from the auxiliary blocks of decode_q4_kernel).
-bool q4_tc_supported(int head_dim, int G);
-int q4_tc_tile_keys();
-cudaError_t launch_q4_tc(const DecodeParams &P, int head_dim, cudaStream_t stream);
-
 }  // namespace fa
