@@ -20,30 +20,52 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// One thread per 4 consecutive fp32 values of an input row.
+// One thread per 4 consecutive fp32 values of an input row, four independent
+// coalesced loads in flight per thread. Indices are 32-bit (the host checks).
 __global__ void __launch_bounds__(kThreads)
     kv_append_f32_kernel(const float4 *__restrict__ k_new, const float4 *__restrict__ v_new,
                          uint8_t *__restrict__ k_planes, uint8_t *__restrict__ v_planes,
                          const int32_t *__restrict__ pos0, int nslots, int n, int n_kv, int hd,
                          int max_seq, size_t plane_bytes, size_t body_off, unsigned *err) {
-    const int q4 = hd / 4;
-    const long long total = static_cast<long long>(nslots) * n * n_kv * q4;
-    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int e4 = static_cast<int>(i % q4);
-        long long r = i / q4;
-        const int h = static_cast<int>(r % n_kv);
-        r /= n_kv;
-        const int t = static_cast<int>(r % n);
-        const int u = static_cast<int>(r / n);
+    const uint32_t q4 = static_cast<uint32_t>(hd / 4);
+    const uint32_t total = static_cast<uint32_t>(nslots) * n * n_kv * q4;
+    const uint32_t stride = gridDim.x * blockDim.x;
+    // destination offset of element i, or ~0 if its row is out of range
+    auto dst = [&](uint32_t i) -> size_t {
+        const uint32_t e4 = i % q4;
+        uint32_t r = i / q4;
+        const uint32_t h = r % static_cast<uint32_t>(n_kv);
+        r /= static_cast<uint32_t>(n_kv);
+        const uint32_t t = r % static_cast<uint32_t>(n);
+        const uint32_t u = r / static_cast<uint32_t>(n);
         const int p0 = pos0[u];
         const long long pos = static_cast<long long>(p0) + t;
         if (p0 < 0 || pos >= max_seq) {
             if (e4 == 0) flag_error(err, FA_ERRBIT_DEVICE);
-            continue;
+            return ~static_cast<size_t>(0);
         }
-        const size_t off = static_cast<size_t>(u) * plane_bytes + body_off +
-                           ((static_cast<size_t>(h) * max_seq + pos) * hd + 4 * e4) * 4;
+        return static_cast<size_t>(u) * plane_bytes + body_off +
+               ((static_cast<size_t>(h) * max_seq + pos) * hd + 4 * e4) * 4;
+    };
+    uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < total; i += 4 * stride) {
+        float4 xk[4], xv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            xk[u] = __ldg(k_new + i + u * stride);
+            xv[u] = __ldg(v_new + i + u * stride);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const size_t off = dst(i + u * stride);
+            if (off == ~static_cast<size_t>(0)) continue;
+            *reinterpret_cast<float4 *>(k_planes + off) = xk[u];
+            *reinterpret_cast<float4 *>(v_planes + off) = xv[u];
+        }
+    }
+    for (; i < total; i += stride) {
+        const size_t off = dst(i);
+        if (off == ~static_cast<size_t>(0)) continue;
         *reinterpret_cast<float4 *>(k_planes + off) = __ldg(k_new + i);
         *reinterpret_cast<float4 *>(v_planes + off) = __ldg(v_new + i);
     }
@@ -168,10 +190,22 @@ __global__ void __launch_bounds__(kAppendWarps * 32)
     const uint32_t groups = (total + 3) / 4;
     uint8_t *ik = reinterpret_cast<uint8_t *>(img[wib][0]);
     uint8_t *iv = reinterpret_cast<uint8_t *>(img[wib][1]);
-    for (uint32_t w = blockIdx.x * kAppendWarps + wib; w < groups;
-         w += gridDim.x * kAppendWarps) {
+    const uint32_t wstep = gridDim.x * kAppendWarps;
+    // the next group's values are loaded before this group is quantised
+    float4 nk = make_float4(0.0f, 0.0f, 0.0f, 0.0f), nv = nk;
+    uint32_t w = blockIdx.x * kAppendWarps + wib;
+    if (w < groups && 4 * w + gq < total) {
+        nk = __ldg(k_new + static_cast<size_t>(4 * w + gq) * 8 + li);
+        nv = __ldg(v_new + static_cast<size_t>(4 * w + gq) * 8 + li);
+    }
+    for (; w < groups; w += wstep) {
         const uint32_t blk = 4 * w + gq;
         const bool live = blk < total;
+        const float4 xk = nk, xv = nv;
+        if (w + wstep < groups && 4 * (w + wstep) + gq < total) {
+            nk = __ldg(k_new + static_cast<size_t>(4 * (w + wstep) + gq) * 8 + li);
+            nv = __ldg(v_new + static_cast<size_t>(4 * (w + wstep) + gq) * 8 + li);
+        }
         // this lane's block: row (u, t, h) and its destination
         const uint32_t row = blk >> nb_shift, b = blk & ((1u << nb_shift) - 1);
         const uint32_t r2 = row / static_cast<uint32_t>(n_kv);
@@ -186,11 +220,6 @@ __global__ void __launch_bounds__(kAppendWarps * 32)
         const size_t dst = plane + body_off +
                            (static_cast<size_t>(h) * max_seq + (ok ? pos : 0)) * row_bytes +
                            b * kQ4BlockBytes;
-        float4 xk = make_float4(0.0f, 0.0f, 0.0f, 0.0f), xv = xk;
-        if (live) {
-            xk = __ldg(k_new + static_cast<size_t>(blk) * 8 + li);
-            xv = __ldg(v_new + static_cast<size_t>(blk) * 8 + li);
-        }
         q4_quant_block8(xk, li, ik + 18 * gq);
         q4_quant_block8(xv, li, iv + 18 * gq);
         if (ok) {
@@ -247,6 +276,8 @@ cudaError_t launch_kv_append(const float *k_new, const float *v_new, uint8_t *k_
     const float4 *k4 = reinterpret_cast<const float4 *>(k_new);
     const float4 *v4 = reinterpret_cast<const float4 *>(v_new);
     if (g.fmt == kFmtF32) {
+        if (items4 + 4LL * device_sm_count() * 16 * kThreads >= (1LL << 32))
+            return cudaErrorInvalidValue;  // the kernel's indices are 32-bit
         kv_append_f32_kernel<<<grid_for(items4, kThreads), kThreads, 0, stream>>>(
             k4, v4, k_planes, v_planes, pos0, nslots, n, g.n_kv, g.hd, g.max_seq, g.bytes,
             g.body_off, err);

@@ -24,12 +24,22 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// Q fp32 -> fp16 over the blocks of one grid row; zeroes *counter.
+// Q fp32 -> fp16 over the blocks of one grid row; zeroes *counter. Four
+// independent coalesced loads per thread are in flight at a time.
 __device__ __forceinline__ void stage_q_rows(const float4 *__restrict__ q, uint2 *__restrict__ qh,
                                              long long count4, unsigned *counter) {
     if (blockIdx.x == 0 && threadIdx.x == 0) *counter = 0u;
-    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < count4;
-         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+    for (; i + 3 * stride < count4; i += 4 * stride) {
+        float4 x[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) x[u] = __ldg(q + i + u * stride);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            qh[i + u * stride] = make_uint2(pack_half2(x[u].x, x[u].y), pack_half2(x[u].z, x[u].w));
+    }
+    for (; i < count4; i += stride) {
         const float4 x = __ldg(q + i);
         qh[i] = make_uint2(pack_half2(x.x, x.y), pack_half2(x.z, x.w));
     }
@@ -66,16 +76,28 @@ __global__ void __launch_bounds__(kThreads)
     }
     const uint8_t *__restrict__ plane = prow ? vplane : kplane;
     uint2 *__restrict__ dst = prow ? vdst : kdst;
-    const int q4 = hd / 4;
-    const long long total = static_cast<long long>(n_kv) * n * q4;
-    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int e4 = static_cast<int>(i % q4);
-        const long long r = i / q4;
-        const int s = static_cast<int>(r % n);
-        const int g = static_cast<int>(r / n);
-        const float4 x = __ldg(reinterpret_cast<const float4 *>(
-            plane + body_off + ((static_cast<size_t>(g) * max_seq + s) * hd + 4 * e4) * 4));
+    // Element i of the output (32-bit: the host checks the size) is float4
+    // e4 of row s of kv head g; four independent loads in flight per thread.
+    const uint32_t q4 = static_cast<uint32_t>(hd / 4);
+    const uint32_t total = static_cast<uint32_t>(n_kv) * static_cast<uint32_t>(n) * q4;
+    const uint32_t stride = gridDim.x * blockDim.x;
+    auto src = [&](uint32_t i) {
+        const uint32_t e4 = i % q4, r = i / q4;
+        const uint32_t s = r % static_cast<uint32_t>(n), g = r / static_cast<uint32_t>(n);
+        return reinterpret_cast<const float4 *>(
+            plane + body_off + ((static_cast<size_t>(g) * max_seq + s) * hd + 4 * e4) * 4);
+    };
+    uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < total; i += 4 * stride) {
+        float4 x[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) x[u] = __ldg(src(i + u * stride));
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            dst[i + u * stride] = make_uint2(pack_half2(x[u].x, x[u].y), pack_half2(x[u].z, x[u].w));
+    }
+    for (; i < total; i += stride) {
+        const float4 x = __ldg(src(i));
         dst[i] = make_uint2(pack_half2(x.x, x.y), pack_half2(x.z, x.w));
     }
 }
@@ -199,6 +221,8 @@ cudaError_t launch_stage_kv(const uint8_t *kplane, const uint8_t *vplane, __half
     };
     if (g.fmt == kFmtF32) {
         const long long items = static_cast<long long>(g.n_kv) * n * (g.hd / 4);
+        if (items + 4LL * device_sm_count() * 16 * kThreads >= (1LL << 32))
+            return cudaErrorInvalidValue;  // the kernel's indices are 32-bit
         stage_kv_f32_kernel<<<grid(items), kThreads, 0, stream>>>(
             kplane, vplane, reinterpret_cast<uint2 *>(kdst), reinterpret_cast<uint2 *>(vdst), n,
             g.n_kv, g.hd, g.max_seq, g.body_off, qs);
