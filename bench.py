@@ -670,6 +670,7 @@ def main():
         w = BY_NAME[name]
         kname = {"q4_0": "decode_q4_kernel<256>", "f16": "decode_dense_kernel<256,f16>",
                  "fp8_e4m3": "decode_dense_kernel<256,fp8>"}[w.kv_fmt]
+        srcs = ("decode.cu", "decode_common.cuh") if w.kv_fmt == "q4_0" else ("decode_dense.cu",)
         S = B.decode_setup(w)
         kvb = decode_kv_bytes(w)
         sm, km = B.timed_steps(lambda: B.decode_step(S), args.warmup, args.steps)
@@ -682,8 +683,7 @@ def main():
                                       "achieved": a, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                       "frac": a / peaks["hbm_gbs"], "frac_of_8tbs": a / 8000.0,
                                       "traffic": profiled_traffic(
-                                          kname, src_hash("decode.cu" if w.kv_fmt == "q4_0"
-                                                          else "decode_dense.cu")),
+                                          kname, src_hash(*srcs)),
                                       "kernel_ms": statistics.mean(km)}}
         del S
         torch.cuda.empty_cache()
