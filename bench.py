@@ -170,7 +170,7 @@ class GpuBench:
         self.stream = torch.cuda.current_stream(dev)
         self.flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
         self.flush_read = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-        self.flush_sink = torch.empty(1, dtype=torch.float32, device=dev)
+        self.flush_sink = torch.empty((), dtype=torch.float32, device=dev)
         self.launches = 0
         self.graph_steps = None  # True once a step was timed as graph replays
         self.graph_error = None
@@ -586,7 +586,7 @@ def main():
     value = job_throughput(flops_step, ms, world) / 1e12
     kms = statistics.mean(kern_ms)
     achieved = flops_step / (kms * 1e-3) / 1e12
-    traffic = profiled_traffic("prefill_tc_kernel<256>", src_hash("prefill_tc.cu"))
+    traffic = profiled_traffic("prefill_tc_kernel<256>", src_hash("prefill_tc.cu", "fa_device.cuh"))
     roofline = {"kernel": "prefill_tc_kernel<256>", "bound": "tensor", "achieved": achieved,
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
@@ -670,7 +670,8 @@ def main():
         w = BY_NAME[name]
         kname = {"q4_0": "decode_q4_kernel<256>", "f16": "decode_dense_kernel<256,f16>",
                  "fp8_e4m3": "decode_dense_kernel<256,fp8>"}[w.kv_fmt]
-        srcs = ("decode.cu", "decode_common.cuh") if w.kv_fmt == "q4_0" else ("decode_dense.cu",)
+        srcs = (("decode.cu", "decode_common.cuh") if w.kv_fmt == "q4_0"
+                else ("decode_dense.cu",)) + ("fa_device.cuh",)
         S = B.decode_setup(w)
         kvb = decode_kv_bytes(w)
         sm, km = B.timed_steps(lambda: B.decode_step(S), args.warmup, args.steps)
@@ -706,7 +707,8 @@ def main():
         "bytes_per_step": abytes, "step": "fa_kv_append (one launch)",
         "roofline": {"kernel": "kv_append_q4_kernel", "bound": "hbm", "achieved": a,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": a / peaks["hbm_gbs"],
-                     "traffic": profiled_traffic("kv_append_q4_kernel", src_hash("kv_append.cu")),
+                     "traffic": profiled_traffic("kv_append_q4_kernel",
+                                                 src_hash("kv_append.cu", "fa_device.cuh")),
                      "kernel_ms": statistics.mean(sm)}}
     del S
     torch.cuda.empty_cache()

@@ -74,24 +74,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that may suspend the thread for up to `ns` nanoseconds while the
+// phase is incomplete (it returns as soon as the phase completes), so that a
+// waiting warp does not take issue slots from the warps working beside it.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait until the phase with `parity` of `bar` has completed. Gives up after
 // kSpinCycles clock cycles, or as soon as another thread of the block raised
 // *abort; returns false then.
 constexpr long long kSpinCycles = 4000000000LL;  // about 2 s at 2 GHz
+constexpr uint32_t kWaitSleepNs = 20000;         // longest single suspension
 
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
                                           unsigned *err) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;  // a completed phase: no suspension
     const long long t0 = clock64();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 31u) == 0) {
-            if (*abort) return false;
-            if (clock64() - t0 > kSpinCycles) {
-                *abort = 1;
-                flag_error(err, FA_ERRBIT_TIMEOUT);
-                return false;
-            }
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+        if (*abort) return false;
+        if (clock64() - t0 > kSpinCycles) {
+            *abort = 1;
+            flag_error(err, FA_ERRBIT_TIMEOUT);
+            return false;
         }
     }
 }

@@ -72,10 +72,12 @@ struct Bars {
     uint64_t v_full[2], v_empty[2];
     uint64_t s_full[2], p_full[2];
     uint64_t o_done;
+    uint64_t o_last;  // the last P.V of a unit finished (one phase per unit)
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
 };
+static_assert(sizeof(Bars) <= 256, "barrier block");
 
 // Key tiles a query tile [p0, p1] visits, in ascending order: the sink tiles
 // [0, ns) then the window tiles [lo, hi] (lo >= ns). Visit iff
@@ -190,6 +192,7 @@ __global__ void __launch_bounds__(256, 1)
             mbar_init(&bars->p_full[s], 128);
         }
         mbar_init(&bars->o_done, 1);
+        mbar_init(&bars->o_last, 1);
         mbar_init(&bars->drain, 1);
         for (int k = 0; k < kUnitRing; ++k) {
             mbar_init(&bars->unit_full[k], 1);
@@ -371,6 +374,7 @@ __global__ void __launch_bounds__(256, 1)
                     if (ok) tc_fence_after();
                 }
                 if (ok) ok = issue_pv(t + count - 1, count == 1);
+                if (ok) tc_commit(&bars->o_last);
                 t += count;
             }
             // every MMA issued must complete before TMEM is released
@@ -457,14 +461,21 @@ __global__ void __launch_bounds__(256, 1)
                     pk[c] = pack_half2(a, bq);
                 }
                 l += rs;
-                if (i > 0) {  // O must hold PV(tt-1) before it is rescaled and before P lands
+                // O must hold PV(tt-1) before it is rescaled. Only then is the O
+                // barrier waited on: its phases cannot run ahead of this row's P
+                // (PV(tt) needs it), and S(tt) ready means PV(tt-2) is done, so the
+                // barrier is at phase tt-1 or tt here and the parity is unambiguous.
+                // (P(tt) itself may land at once: PV(tt-2), the last reader of this
+                // S buffer, is done.)
+                const bool any_resc = __any_sync(0xffffffffu, resc);
+                if (any_resc) {
                     ok = mbar_wait(&bars->o_done, (tt - 1) & 1, abort, err);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                 }
                 tc_fence_after();
                 __syncwarp();
-                if (__any_sync(0xffffffffu, resc)) {
+                if (any_resc) {
 #pragma unroll 1
                     for (int c = 0; c < HD / 32; ++c) {
                         uint32_t o[32];
@@ -489,7 +500,7 @@ __global__ void __launch_bounds__(256, 1)
             // ---- epilogue of the unit: wait for its last P.V, then O / l leaves
             // through this warp's two staging boxes [32 rows][32 fp32] (128-byte
             // swizzle) by TMA bulk-tensor stores; rows past n are dropped.
-            ok = mbar_wait(&bars->o_done, (t - 1) & 1, abort, err);
+            ok = mbar_wait(&bars->o_last, j & 1, abort, err);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();

@@ -110,6 +110,7 @@ PREFILL_CASES = [
     (129, 4, 2, 128, 9, 3, "f32", (0, 0)),
     (300, 16, 2, 256, 4, 100, "f32", (0, 0)),
     (300, 2, 1, 256, 0, 300, "f32", (0, 0)),
+    (300, 3, 3, 256, 4, 100, "f32", (0, 0)),
     (1000, 8, 1, 128, 4, 1024, "f32", (0, 0)),
     (700, 16, 2, 256, 0, 0, "f32", (0, 0)),
     (520, 16, 2, 256, 0, 0, "q4_0", (0, 0)),
@@ -131,12 +132,13 @@ def test_prefill_small(oracle_mod, case):
     assert_close(got, want, str(case))
 
 
+@pytest.mark.parametrize("hd", [64, 256])
 @pytest.mark.parametrize("n,sink,win", [(1, 0, 0), (130, 0, 0), (600, 4, 1), (600, 4, 130),
                                         (1000, 0, 256), (1000, 200, 129), (777, 9, 3)])
-def test_prefill_tile_map_bitexact(oracle_mod, n, sink, win):
-    q, k, v = prefill_inputs(n, 2, 1, 64, seed=RNG_SEED + 7)
+def test_prefill_tile_map_bitexact(oracle_mod, n, sink, win, hd):
+    q, k, v = prefill_inputs(n, 2, 1, hd, seed=RNG_SEED + 7)
     _, tm = run_prefill(q, k, v, kv_fmt="f32", sink=sink, win=win, tile_map=True)
-    bq, bk = fa().prefill_tile_shape(64)
+    bq, bk = fa().prefill_tile_shape(hd)
     assert np.array_equal(tm, oracle_mod.tile_map(n, bq, bk, sink, win))
 
 
