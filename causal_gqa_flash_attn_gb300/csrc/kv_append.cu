@@ -11,6 +11,7 @@
 #include <cuda_fp8.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "fa_device.cuh"
 #include "fa_internal.h"
@@ -132,130 +133,197 @@ __global__ void kv_set_scale_kernel(uint8_t *planes, int nslots, size_t plane_by
             scale;
 }
 
-// Quantise one Q4_0 block held by an 8-lane group of the warp (lane li of the
-// group holds elements 4 li .. 4 li + 3 in x) into the 18 bytes at img.
-// Every lane of the warp must call it (the group reductions shuffle).
-__device__ __forceinline__ void q4_quant_block8(float4 x, int li, uint8_t *img) {
+// Q4_0 append: one warp per input row (slot, token, kv head) of K and of V.
+// The row's HD / 32 blocks are spread over the warp, L = 1024 / HD lanes per
+// block, each lane holding VPL = HD / 32 consecutive values: lane l has
+// elements VPL (l % L) .. of block l / L. A block's scale comes from a
+// shuffle reduction over its L lanes; its 16 code bytes (byte j: element j in
+// the low nibble, element j + 16 in the high one) from the lanes of its first
+// half, each joined with the lane L / 2 further on. The row's 18-byte blocks
+// are assembled in shared memory and leave as whole 32-bit words (row_bytes
+// is a multiple of 4). Row indices are 32-bit (the host splits larger appends
+// by slots).
+constexpr int kAppendWarps = 8;
+
+template <int HD>
+__device__ __forceinline__ void load_vals(const float *src, float (&x)[HD / 32]) {
+    constexpr int VPL = HD / 32;
+    if constexpr (VPL >= 4) {
+#pragma unroll
+        for (int k = 0; k < VPL / 4; ++k) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(src) + k);
+            x[4 * k] = v.x;
+            x[4 * k + 1] = v.y;
+            x[4 * k + 2] = v.z;
+            x[4 * k + 3] = v.w;
+        }
+    } else {
+        const float2 v = __ldg(reinterpret_cast<const float2 *>(src));
+        x[0] = v.x;
+        x[1] = v.y;
+    }
+}
+
+// Quantise the block this lane shares with its L - 1 neighbours into the row
+// image (block bb at byte 18 bb). Every lane of the warp must call it.
+template <int HD>
+__device__ __forceinline__ void q4_quant_lane(const float (&x)[HD / 32], int bb, int li,
+                                              uint8_t *img) {
+    constexpr int VPL = HD / 32, L = 32 / VPL;
     // amax: max |x| from +0; NaN never raises it (fmaxf returns the non-NaN operand)
-    float a = fmaxf(fmaxf(fmaxf(0.0f, fabsf(x.x)), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+    float a = 0.0f;
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) a = fmaxf(a, fabsf(x[k]));
+#pragma unroll
+    for (int o = 1; o < L; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
     // d = amax / -8: a scaling by a power of two, so the product by -1/8 is
     // the same correctly rounded value as the division.
     const float d = __fmul_rn(a, -0.125f);
     const float id = (d != 0.0f) ? __frcp_rn(d) : 0.0f;  // IEEE reciprocal, nearest
     // One fp32 multiply (no contraction), a saturating round-half-even
-    // conversion (NaN -> 0), a wrapping +8, then the clamp to [0, 15].
-    const float xs[4] = {x.x, x.y, x.z, x.w};
-    uint32_t codes = 0;
+    // conversion (NaN -> 0), a wrapping +8, then the clamp to [0, 15]; four
+    // codes per word, one per byte.
+    uint32_t codes[(VPL + 3) / 4] = {};
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int q = __float2int_rn(__fmul_rn(xs[k], id));
+    for (int k = 0; k < VPL; ++k) {
+        const int q = __float2int_rn(__fmul_rn(x[k], id));
         int c = static_cast<int>(static_cast<unsigned>(q) + 8u);
         c = c < 0 ? 0 : (c > 15 ? 15 : c);
-        codes |= static_cast<uint32_t>(c) << (8 * k);
+        codes[k / 4] |= static_cast<uint32_t>(c) << (8 * (k % 4));
     }
-    // byte j of the block: element j (low nibble) | element j + 16 (high)
-    const uint32_t hi = __shfl_down_sync(0xffffffffu, codes, 4);
-    if (li < 4) {
-        const uint32_t w = codes | (hi << 4);
-        uint16_t *dst = reinterpret_cast<uint16_t *>(img + 2 + 4 * li);  // 2-byte aligned
-        dst[0] = static_cast<uint16_t>(w);
-        dst[1] = static_cast<uint16_t>(w >> 16);
+    uint16_t *blk = reinterpret_cast<uint16_t *>(img + 18 * bb);  // 2-byte aligned
+#pragma unroll
+    for (int w = 0; w < (VPL + 3) / 4; ++w) {
+        const uint32_t hi = __shfl_down_sync(0xffffffffu, codes[w], L / 2);
+        const uint32_t bytes = codes[w] | (hi << 4);
+        if (li < L / 2) {
+            // VPL bytes of the block's 16 code bytes, from byte VPL li + 4 w
+            uint16_t *dst = blk + 1 + (VPL * li + 4 * w) / 2;
+            dst[0] = static_cast<uint16_t>(bytes);
+            if (VPL >= 4) dst[1] = static_cast<uint16_t>(bytes >> 16);
+        }
     }
-    if (li == 0) *reinterpret_cast<uint16_t *>(img) = __half_as_ushort(__float2half_rn(d));
+    if (li == 0) blk[0] = __half_as_ushort(__float2half_rn(d));
 }
 
-// One warp per 4 consecutive Q4_0 blocks of the input rows (K and V): lane l
-// holds 4 values of block l / 8. The two pairs of blocks (36 bytes each, a
-// 4-byte aligned run of a plane row, since rows hold an even number of
-// blocks) are assembled in shared memory and leave as whole 32-bit words.
-// Block indices are 32-bit (the host splits larger appends by slots) and
-// blocks per row (head_dim / 32) a power of two.
-constexpr int kAppendWarps = 8;
+// The lane's VPL values as fp16 at dst (a sink or ring mirror row).
+template <int HD>
+__device__ __forceinline__ void store_half_vals(uint8_t *dst, const float (&x)[HD / 32]) {
+    constexpr int VPL = HD / 32;
+    if constexpr (VPL == 8) {
+        *reinterpret_cast<uint4 *>(dst) =
+            make_uint4(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]), pack_half2(x[4], x[5]),
+                       pack_half2(x[6], x[7]));
+    } else if constexpr (VPL == 4) {
+        *reinterpret_cast<uint2 *>(dst) =
+            make_uint2(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]));
+    } else {
+        *reinterpret_cast<uint32_t *>(dst) = pack_half2(x[0], x[1]);
+    }
+}
 
+template <int HD>
 __global__ void __launch_bounds__(kAppendWarps * 32)
-    kv_append_q4_kernel(const float4 *__restrict__ k_new, const float4 *__restrict__ v_new,
+    kv_append_q4_kernel(const float *__restrict__ k_new, const float *__restrict__ v_new,
                         uint8_t *__restrict__ k_planes, uint8_t *__restrict__ v_planes,
-                        const int32_t *__restrict__ pos0, int nslots, int n, int n_kv, int hd,
+                        const int32_t *__restrict__ pos0, int nslots, int n, int n_kv,
                         int max_seq, size_t plane_bytes, size_t body_off, size_t row_bytes,
                         size_t sink_off, size_t ring_off, int shadow_sink, int shadow_win,
                         unsigned *err) {
-    __shared__ __align__(16) uint32_t img[kAppendWarps][2][18];  // K, V: 4 blocks each
+    constexpr int VPL = HD / 32, L = 32 / VPL;
+    constexpr int RW = HD / 32 * kQ4BlockBytes / 4;  // 32-bit words of an output row
+    __shared__ __align__(16) uint32_t img[kAppendWarps][2][RW];  // K, V rows
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-    const int gq = lane >> 3, li = lane & 7;
-    const uint32_t nb_shift = hd == 64 ? 1u : (hd == 128 ? 2u : 3u);  // log2(hd / 32)
-    const uint32_t total = static_cast<uint32_t>(nslots) * n * n_kv << nb_shift;  // blocks
-    const uint32_t groups = (total + 3) / 4;
+    const int bb = lane / L, li = lane % L;
+    const uint32_t rows = static_cast<uint32_t>(nslots) * n * n_kv;
+    const uint32_t wstep = gridDim.x * kAppendWarps;
     uint8_t *ik = reinterpret_cast<uint8_t *>(img[wib][0]);
     uint8_t *iv = reinterpret_cast<uint8_t *>(img[wib][1]);
-    const uint32_t wstep = gridDim.x * kAppendWarps;
-    // the next group's values are loaded before this group is quantised
-    float4 nk = make_float4(0.0f, 0.0f, 0.0f, 0.0f), nv = nk;
-    uint32_t w = blockIdx.x * kAppendWarps + wib;
-    if (w < groups && 4 * w + gq < total) {
-        nk = __ldg(k_new + static_cast<size_t>(4 * w + gq) * 8 + li);
-        nv = __ldg(v_new + static_cast<size_t>(4 * w + gq) * 8 + li);
+    const int e = VPL * lane;  // first element of the row this lane holds
+    // the next row's values are loaded before this row is quantised
+    float nk[VPL], nv[VPL];
+    uint32_t row = blockIdx.x * kAppendWarps + wib;
+    if (row < rows) {
+        load_vals<HD>(k_new + static_cast<size_t>(row) * HD + e, nk);
+        load_vals<HD>(v_new + static_cast<size_t>(row) * HD + e, nv);
     }
-    for (; w < groups; w += wstep) {
-        const uint32_t blk = 4 * w + gq;
-        const bool live = blk < total;
-        const float4 xk = nk, xv = nv;
-        if (w + wstep < groups && 4 * (w + wstep) + gq < total) {
-            nk = __ldg(k_new + static_cast<size_t>(4 * (w + wstep) + gq) * 8 + li);
-            nv = __ldg(v_new + static_cast<size_t>(4 * (w + wstep) + gq) * 8 + li);
+    for (; row < rows; row += wstep) {
+        float xk[VPL], xv[VPL];
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            xk[k] = nk[k];
+            xv[k] = nv[k];
         }
-        // this lane's block: row (u, t, h) and its destination
-        const uint32_t row = blk >> nb_shift, b = blk & ((1u << nb_shift) - 1);
+        if (row + wstep < rows) {
+            load_vals<HD>(k_new + static_cast<size_t>(row + wstep) * HD + e, nk);
+            load_vals<HD>(v_new + static_cast<size_t>(row + wstep) * HD + e, nv);
+        }
+        // the row (u, t, h) and its destination (the same for the whole warp)
         const uint32_t r2 = row / static_cast<uint32_t>(n_kv);
         const int h = static_cast<int>(row - r2 * n_kv);
         const uint32_t uu = r2 / static_cast<uint32_t>(n);
         const int t = static_cast<int>(r2 - uu * n);
-        const int p0 = live ? pos0[uu] : 0;
+        const int p0 = pos0[uu];
         const long long pos = static_cast<long long>(p0) + t;
-        const bool ok = live && p0 >= 0 && pos < max_seq;
-        if (live && !ok && li == 0 && b == 0) flag_error(err, FA_ERRBIT_DEVICE);
-        const size_t plane = static_cast<size_t>(uu) * plane_bytes;
-        const size_t dst = plane + body_off +
-                           (static_cast<size_t>(h) * max_seq + (ok ? pos : 0)) * row_bytes +
-                           b * kQ4BlockBytes;
-        q4_quant_block8(xk, li, ik + 18 * gq);
-        q4_quant_block8(xv, li, iv + 18 * gq);
+        const bool ok = p0 >= 0 && pos < max_seq;
+        if (!ok && lane == 0) flag_error(err, FA_ERRBIT_DEVICE);
+        q4_quant_lane<HD>(xk, bb, li, ik);
+        q4_quant_lane<HD>(xv, bb, li, iv);
         if (ok) {
+            const size_t plane = static_cast<size_t>(uu) * plane_bytes;
             // fp16 mirrors: the shadow sink rows, and the rows that stay among
             // the 256 newest after this call (no two rows of a call share a
             // ring slot)
-            const int e = static_cast<int>(b) * kQ4Block + 4 * li;
-            const uint2 hk = make_uint2(pack_half2(xk.x, xk.y), pack_half2(xk.z, xk.w));
-            const uint2 hv = make_uint2(pack_half2(xv.x, xv.y), pack_half2(xv.z, xv.w));
             if (pos < shadow_sink) {
                 const size_t so =
-                    plane + sink_off + ((static_cast<size_t>(h) * kSinkMax + pos) * hd + e) * 2;
-                *reinterpret_cast<uint2 *>(k_planes + so) = hk;
-                *reinterpret_cast<uint2 *>(v_planes + so) = hv;
+                    plane + sink_off + ((static_cast<size_t>(h) * kSinkMax + pos) * HD + e) * 2;
+                store_half_vals<HD>(k_planes + so, xk);
+                store_half_vals<HD>(v_planes + so, xv);
             }
             if (shadow_win > 0 && t >= n - kRingRows) {
-                const size_t ro = plane + ring_off +
-                                  ((static_cast<size_t>(h) * kRingRows + (pos % kRingRows)) * hd +
-                                   e) * 2;
-                *reinterpret_cast<uint2 *>(k_planes + ro) = hk;
-                *reinterpret_cast<uint2 *>(v_planes + ro) = hv;
+                const size_t ro =
+                    plane + ring_off +
+                    ((static_cast<size_t>(h) * kRingRows + (pos % kRingRows)) * HD + e) * 2;
+                store_half_vals<HD>(k_planes + ro, xk);
+                store_half_vals<HD>(v_planes + ro, xv);
+            }
+            const size_t dst =
+                plane + body_off + (static_cast<size_t>(h) * max_seq + pos) * row_bytes;
+            __syncwarp();
+#pragma unroll
+            for (int w = lane; w < RW; w += 32) {
+                *reinterpret_cast<uint32_t *>(k_planes + dst + 4 * w) = img[wib][0][w];
+                *reinterpret_cast<uint32_t *>(v_planes + dst + 4 * w) = img[wib][1][w];
             }
         }
-        // word lane % 9 of pair lane / 9 goes out; the pair's first block is
-        // held by the lanes of group 2 (lane / 9), which pass its destination
-        const int src = 16 * (lane >= 9 ? 1 : 0);
-        const size_t pdst = __shfl_sync(0xffffffffu, dst, src);
-        const bool pok = __shfl_sync(0xffffffffu, ok, src);
-        __syncwarp();
-        if (lane < 18 && pok) {
-            const size_t off = pdst + 4 * (lane % 9);
-            *reinterpret_cast<uint32_t *>(k_planes + off) = img[wib][0][lane];
-            *reinterpret_cast<uint32_t *>(v_planes + off) = img[wib][1][lane];
-        }
-        __syncwarp();
+        __syncwarp();  // the image is read before the next row overwrites it
     }
+}
+
+// Blocks of kernel that are resident on the device at once (one wave), per
+// device and kernel; 0 if the query failed.
+template <typename Kernel>
+int resident_blocks(Kernel kernel, int threads, int slot) {
+    constexpr int kDevs = 64, kSlots = 3;
+    static int blocks[kDevs][kSlots] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs || slot < 0 ||
+        slot >= kSlots) {
+        cudaGetLastError();
+        return 0;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (blocks[dev][slot] == 0) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        blocks[dev][slot] = per_sm * device_sm_count();
+    }
+    return blocks[dev][slot];
 }
 
 int grid_for(long long work_items, int items_per_block) {
@@ -297,10 +365,20 @@ cudaError_t launch_kv_append(const float *k_new, const float *v_new, uint8_t *k_
         for (long long u0 = 0; u0 < nslots; u0 += chunk) {
             const int ns = static_cast<int>(std::min<long long>(chunk, nslots - u0));
             const size_t in_off = static_cast<size_t>(u0) * per_slot * 8;  // float4s
-            const long long groups = (ns * per_slot + 3) / 4;
-            kv_append_q4_kernel<<<grid_for(groups, kAppendWarps), kAppendWarps * 32, 0, stream>>>(
-                k4 + in_off, v4 + in_off, k_planes + static_cast<size_t>(u0) * g.bytes,
-                v_planes + static_cast<size_t>(u0) * g.bytes, pos0 + u0, ns, n, g.n_kv, g.hd,
+            const long long rows = static_cast<long long>(ns) * n * g.n_kv;
+            auto kernel = g.hd == 64    ? kv_append_q4_kernel<64>
+                          : g.hd == 128 ? kv_append_q4_kernel<128>
+                                        : kv_append_q4_kernel<256>;
+            // one wave: every warp loops over rows with the next row's loads in flight
+            const int slot = g.hd == 64 ? 0 : (g.hd == 128 ? 1 : 2);
+            const int resident = resident_blocks(kernel, kAppendWarps * 32, slot);
+            const long long want = (rows + kAppendWarps - 1) / kAppendWarps;
+            const int grid = resident > 0 ? static_cast<int>(std::min<long long>(want, resident))
+                                          : grid_for(rows, kAppendWarps);
+            kernel<<<grid, kAppendWarps * 32, 0, stream>>>(
+                k_new + in_off * 4, v_new + in_off * 4,
+                k_planes + static_cast<size_t>(u0) * g.bytes,
+                v_planes + static_cast<size_t>(u0) * g.bytes, pos0 + u0, ns, n, g.n_kv,
                 g.max_seq, g.bytes, g.body_off, g.row_bytes, g.sink_off, g.ring_off, shadow_sink,
                 shadow_win, err);
         }
