@@ -705,9 +705,9 @@ def main():
     extra["append_q4_n8192_h2_d256_shadow4_256"] = {
         "value": a, "unit": "GB/s", "ms_per_step": statistics.mean(sm),
         "bytes_per_step": abytes, "step": "fa_kv_append (one launch)",
-        "roofline": {"kernel": "kv_append_q4_kernel", "bound": "hbm", "achieved": a,
+        "roofline": {"kernel": "kv_append_q4_kernel<256>", "bound": "hbm", "achieved": a,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": a / peaks["hbm_gbs"],
-                     "traffic": profiled_traffic("kv_append_q4_kernel",
+                     "traffic": profiled_traffic("kv_append_q4_kernel<256>",
                                                  src_hash("kv_append.cu", "fa_device.cuh")),
                      "kernel_ms": statistics.mean(sm)}}
     del S
