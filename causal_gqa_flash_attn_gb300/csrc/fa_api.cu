@@ -469,6 +469,7 @@ fa_status fa_prefill_chunk(const float *q, const void *k, const void *v, float *
     a.sink = sink;
     a.win = win;
     a.scale = 1.0f / sqrtf(static_cast<float>(head_dim));
+    a.prefetch_kv = direct;
     e = record_start(s);
     if (e == cudaSuccess) e = fa::launch_prefill_tc(a, d->err, s);
     if (e == cudaSuccess) e = record_stop(s);

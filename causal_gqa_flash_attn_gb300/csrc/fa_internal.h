@@ -78,6 +78,9 @@ struct PrefillArgs {
     // fp16 window split_w is narrower than the ring (near: key >= split_f and
     // key > p - split_w); 1 and 2 need lse
     int split = 0, split_f = 0, split_w = 0;
+    // K/V are cache planes read in place (not staged just before): the kernel
+    // asks for their rows in L2 at its start
+    bool prefetch_kv = false;
 };
 constexpr int kPrefillBQ = 128;
 constexpr int kPrefillBK = 128;

@@ -156,7 +156,8 @@ __global__ void __launch_bounds__(256, 1)
                       const __grid_constant__ CUtensorMap tm_o, uint8_t *__restrict__ tile_map,
                       unsigned *__restrict__ work_counter, float *__restrict__ lse, int pos0,
                       int n, int Hq, int Hkv, int sink, int win, float sl2, unsigned *err,
-                      int split_f, int split_w) {
+                      int split_f, int split_w, const uint8_t *pf_k, const uint8_t *pf_v,
+                      unsigned long long pf_head_stride, unsigned pf_head_bytes) {
     using C = Cfg<HD>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -227,6 +228,21 @@ __global__ void __launch_bounds__(256, 1)
     if (warp == 0) {
         // ------------------------------------------------------- TMA producer
         if (lane == 0) {
+            // K/V rows not just written by a staging pass (an fp16 cache read in
+            // place): this block asks for its share of them in L2 before its
+            // first unit, so the first passes over the key tiles do not wait on
+            // DRAM (pf_k null: nothing to do)
+            if (pf_k) {
+                constexpr unsigned kPiece = 65536;
+                const unsigned per_head = (pf_head_bytes + kPiece - 1) / kPiece;
+                const unsigned pieces = 2u * static_cast<unsigned>(Hkv) * per_head;
+                for (unsigned i = blockIdx.x; i < pieces; i += gridDim.x) {
+                    const unsigned piece = i % per_head, hv = i / per_head;
+                    const unsigned off = piece * kPiece;
+                    bulk_prefetch_l2(((hv & 1) ? pf_v : pf_k) + (hv >> 1) * pf_head_stride + off,
+                                     min(kPiece, pf_head_bytes - off));
+                }
+            }
             int k_arms[2] = {0, 0}, v_arms[2] = {0, 0}, q_arms = 0;
             int t = 0;  // global tile index of this block
             bool ok = true;
@@ -639,9 +655,14 @@ cudaError_t launch_hd(const PrefillArgs &a, unsigned *err, cudaStream_t stream) 
     const int units = nqt * a.n_q_heads;
     const int grid = units < device_sm_count() ? units : device_sm_count();
     const float sl2 = a.scale * 1.4426950408889634f;
+    // 32-bit byte counts per kv head (up to 8M rows at head_dim 256)
+    const bool prefetch = a.prefetch_kv && L * HD * 2 < (1ull << 31);
     kernel<<<grid, 256, C::SMEM, stream>>>(
         tq, tk, tv, to, a.tile_map, a.work_counter, a.lse, a.pos0, a.n, a.n_q_heads,
-        a.n_kv_heads, a.sink, a.win, sl2, err, a.split_f, a.split_w);
+        a.n_kv_heads, a.sink, a.win, sl2, err, a.split_f, a.split_w,
+        prefetch ? reinterpret_cast<const uint8_t *>(a.kh) : nullptr,
+        reinterpret_cast<const uint8_t *>(a.vh), static_cast<unsigned long long>(head_stride),
+        static_cast<unsigned>(L * HD * 2));
     return cudaGetLastError();
 }
 
