@@ -440,7 +440,7 @@ constexpr int kPRing = 2;      // P records in flight per pair
 #define FA_Q4_KSTAGES 2
 #endif
 #ifndef FA_Q4_VSTAGES
-#define FA_Q4_VSTAGES 3
+#define FA_Q4_VSTAGES 2
 #endif
 #ifndef FA_Q4_MIN_BLOCKS
 #define FA_Q4_MIN_BLOCKS 2
@@ -450,7 +450,7 @@ constexpr int kPRing = 2;      // P records in flight per pair
 // and the code small. (The QK warp walks the blocks outermost and both halves
 // inside, so that a block's Q fragments are read once per tile.)
 #ifndef FA_Q4_PV_HALVES
-#define FA_Q4_PV_HALVES 1
+#define FA_Q4_PV_HALVES 2
 #endif
 constexpr int kPVHalves = FA_Q4_PV_HALVES;
 // Unroll factor of the QK warp's loop over pairs of 32-element blocks (an even
