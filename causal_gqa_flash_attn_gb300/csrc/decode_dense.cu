@@ -48,7 +48,7 @@ constexpr float kRescaleDense = 8.0f;  // lazy-rescale threshold (log2 units)
 #define FA_DENSE_NW_SMALL 8
 #endif
 #ifndef FA_DENSE_NW_FP8
-#define FA_DENSE_NW_FP8 7
+#define FA_DENSE_NW_FP8 5
 #endif
 // Keys per tile of the fp8 kernel (16 or 32; fp16 uses 16): a longer tile
 // spreads each tile's fixed work (waits, copies, masks, the softmax step)
