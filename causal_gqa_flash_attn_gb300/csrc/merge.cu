@@ -12,8 +12,9 @@
 //     out = prefix * wp / (wp + ws) + suffix * ws / (wp + ws),
 //     lse = log(wp + ws) + m.
 // Arithmetic is fp32. The work is a stream over 3 D floats per (t, h): one
-// thread per 4 consecutive floats of a row, 128-bit loads and stores, a grid of
-// a few blocks per SM striding over the rows.
+// warp per (t, h) row (its index arithmetic and weights once), each lane
+// 128-bit loads of up to four float4s of the row issued together, a grid of a
+// few blocks per SM striding over the rows.
 #include "fa_device.cuh"
 #include "fa_internal.h"
 
@@ -23,23 +24,33 @@ namespace fa {
 namespace {
 
 constexpr int kMergeThreads = 256;
+constexpr int kMergeWarps = kMergeThreads / 32;
 
+// D4C: float4s per row when fixed at compile time (head_dim 64, 128, 256),
+// else 0 and the row is walked in pieces of 32 float4s (d4 of them in all).
+template <int D4C>
 __global__ void __launch_bounds__(kMergeThreads)
     merge_attn_states_kernel(float *__restrict__ out, float *__restrict__ out_lse,
-                             const float4 *__restrict__ prefix, const float *__restrict__ prefix_lse,
-                             const float4 *__restrict__ suffix, const float *__restrict__ suffix_lse,
-                             int T, int H, int D4, int with_context) {
-    const long long total = static_cast<long long>(T) * H * D4;
-    for (long long i = blockIdx.x * static_cast<long long>(kMergeThreads) + threadIdx.x; i < total;
-         i += static_cast<long long>(gridDim.x) * kMergeThreads) {
-        const long long row = i / D4;  // t * H + h
-        const int d4 = static_cast<int>(i - row * D4);
-        const int t = static_cast<int>(row / H), h = static_cast<int>(row - static_cast<long long>(t) * H);
+                             const float4 *__restrict__ prefix,
+                             const float *__restrict__ prefix_lse,
+                             const float4 *__restrict__ suffix,
+                             const float *__restrict__ suffix_lse, int T, int H, int d4,
+                             int with_context) {
+    constexpr int PER = D4C > 0 ? (D4C + 31) / 32 : 1;  // float4s of a row per lane and piece
+    const int D4 = D4C > 0 ? D4C : d4;
+    const int lane = threadIdx.x & 31;
+    const long long rows = static_cast<long long>(T) * H;
+    const long long step = static_cast<long long>(gridDim.x) * kMergeWarps;
+    for (long long row = blockIdx.x * static_cast<long long>(kMergeWarps) + (threadIdx.x >> 5);
+         row < rows; row += step) {
+        const int t = static_cast<int>(row / H);
+        const int h = static_cast<int>(row - static_cast<long long>(t) * H);
         const long long li = static_cast<long long>(h) * T + t;
-        float4 r;
-        float lse;
+        // the row's case (warp-uniform): 0 the suffix as it is, 1 the prefix as it
+        // is (neither side has a key), 2 the weighted sum
+        int mode = 0;
+        float a = 0.0f, b = 0.0f, lse;
         if (with_context >= 0 && t >= with_context) {
-            r = __ldg(suffix + i);
             lse = __ldg(suffix_lse + li);
         } else {
             float lp = __ldg(prefix_lse + li), ls = __ldg(suffix_lse + li);
@@ -47,19 +58,38 @@ __global__ void __launch_bounds__(kMergeThreads)
             if (ls == INFINITY) ls = -INFINITY;
             const float m = fmaxf(lp, ls);
             if (m == -INFINITY) {
-                r = __ldg(prefix + i);
+                mode = 1;
                 lse = -INFINITY;
             } else {
+                mode = 2;
                 const float wp = expf(lp - m), ws = expf(ls - m), tot = wp + ws;
-                const float a = wp / tot, b = ws / tot;
-                const float4 x = __ldg(prefix + i), y = __ldg(suffix + i);
-                r = make_float4(x.x * a + y.x * b, x.y * a + y.y * b, x.z * a + y.z * b,
-                                x.w * a + y.w * b);
+                a = wp / tot;
+                b = ws / tot;
                 lse = logf(tot) + m;
             }
         }
-        reinterpret_cast<float4 *>(out)[i] = r;
-        if (out_lse && d4 == 0) out_lse[li] = lse;
+        for (int c0 = 0; c0 < D4; c0 += 32 * PER) {  // a single piece when D4C > 0
+            const float4 *px = prefix + row * D4 + c0, *sx = suffix + row * D4 + c0;
+            float4 *ox = reinterpret_cast<float4 *>(out) + row * D4 + c0;
+            const int rem = D4 - c0;  // this piece's float4s are those below rem
+            float4 x[PER], y[PER];
+#pragma unroll
+            for (int k = 0; k < PER; ++k)
+                if (lane + 32 * k < rem) {
+                    if (mode != 0) x[k] = __ldg(px + lane + 32 * k);
+                    if (mode != 1) y[k] = __ldg(sx + lane + 32 * k);
+                }
+#pragma unroll
+            for (int k = 0; k < PER; ++k)
+                if (lane + 32 * k < rem)
+                    ox[lane + 32 * k] =
+                        mode == 0 ? y[k]
+                        : mode == 1
+                            ? x[k]
+                            : make_float4(x[k].x * a + y[k].x * b, x[k].y * a + y[k].y * b,
+                                          x[k].z * a + y[k].z * b, x[k].w * a + y[k].w * b);
+        }
+        if (out_lse && lane == 0) out_lse[li] = lse;
     }
 }
 
@@ -69,12 +99,16 @@ cudaError_t launch_merge_attn_states(float *out, float *out_lse, const float *pr
                                      const float *prefix_lse, const float *suffix,
                                      const float *suffix_lse, int T, int H, int D,
                                      int with_context, cudaStream_t stream) {
-    const long long items = static_cast<long long>(T) * H * (D / 4);
-    long long blocks = (items + kMergeThreads - 1) / kMergeThreads;
+    const long long rows = static_cast<long long>(T) * H;
+    long long blocks = (rows + kMergeWarps - 1) / kMergeWarps;
     const long long cap = static_cast<long long>(device_sm_count()) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    merge_attn_states_kernel<<<static_cast<int>(blocks), kMergeThreads, 0, stream>>>(
+    auto kernel = D == 64    ? merge_attn_states_kernel<16>
+                  : D == 128 ? merge_attn_states_kernel<32>
+                  : D == 256 ? merge_attn_states_kernel<64>
+                             : merge_attn_states_kernel<0>;
+    kernel<<<static_cast<int>(blocks), kMergeThreads, 0, stream>>>(
         out, out_lse, reinterpret_cast<const float4 *>(prefix), prefix_lse,
         reinterpret_cast<const float4 *>(suffix), suffix_lse, T, H, D / 4, with_context);
     return cudaGetLastError();
