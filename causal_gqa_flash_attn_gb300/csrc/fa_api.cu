@@ -98,21 +98,25 @@ fa_status check_shadow(int kv_fmt, int shadow_sink, int shadow_win) {
     return FA_OK;
 }
 
-// Prefill workspace: a 256-byte header holding the kernel's work counters,
-// then the fp16 staging of Q [n][Hq][hd], K and V [Hkv][n][hd]. A split
+// Prefill workspace: a 256-byte header holding the kernel's work counters
+// and its Q staging counter, one Q-ready flag per unit, then the fp16 staging
+// of Q [n][Hq][hd], K and V [Hkv][n][hd]. A split
 // prefill (Q4_0 with a shadow window narrower than the ring) adds a second
 // K and V staging (the fp16 ring values) and the two parts' outputs
 // [n][Hq][hd] and lses [Hq][n], fp32.
 struct PrefillWs {
-    size_t ctr_off, ctr2_off, q_off, k_off, v_off, bytes;
+    size_t ctr_off, qctr_off, ctr2_off, flag_off, q_off, k_off, v_off, bytes;
     size_t k2_off, v2_off, o1_off, o2_off, l1_off, l2_off;  // split only
 };
 // n query rows over nk key rows
 PrefillWs prefill_ws(int n, int nk, int hq, int hkv, int hd, bool split = false) {
     PrefillWs w;
     w.ctr_off = 0;
+    w.qctr_off = 64;
     w.ctr2_off = 128;
-    w.q_off = 256;
+    w.flag_off = 256;
+    const size_t units = static_cast<size_t>((n + fa::kPrefillBQ - 1) / fa::kPrefillBQ) * hq;
+    w.q_off = w.flag_off + up256(units * 4);
     w.k_off = w.q_off + up256(static_cast<size_t>(n) * hq * hd * 2);
     const size_t kv = up256(static_cast<size_t>(hkv) * nk * hd * 2);
     w.v_off = w.k_off + kv;
@@ -147,6 +151,15 @@ bool plane_geom(int fmt, int n_kv, int max_seq, int hd, PlaneGeom *g);
 
 namespace {
 
+// The prefill kernel converts the Q tiles past its first wave of units
+// itself: its arguments for that.
+void set_q_staging(fa::PrefillArgs *a, const float *q, uint8_t *ws, const PrefillWs &w) {
+    a->q = q;
+    a->q_flags = reinterpret_cast<unsigned *>(ws + w.flag_off);
+    a->q_stage_counter = reinterpret_cast<unsigned *>(ws + w.qctr_off);
+    a->q_w0 = fa::prefill_units_staged_first(a->pos0, a->n, a->n_q_heads, a->sink, a->win);
+}
+
 // The split prefill after the Q staging and the far K/V staging: stage the
 // fp16 ring values, run the far part and the near part (each with its lse)
 // and merge them into out (and lse when requested).
@@ -168,8 +181,7 @@ fa_status prefill_split(const float *q, const void *k, const void *v, float *out
     const int F = nk - FA_Q4_RING_ROWS > shadow_sink ? nk - FA_Q4_RING_ROWS : shadow_sink;
     cudaError_t e = fa::launch_stage_kv(static_cast<const uint8_t *>(k),
                                         static_cast<const uint8_t *>(v), kh2, vh2, nk, g,
-                                        shadow_sink, FA_Q4_RING_ROWS, nullptr, nullptr, 0,
-                                        nullptr, s);
+                                        shadow_sink, FA_Q4_RING_ROWS, nullptr, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(ctr2, 0, sizeof(unsigned), s);
     fa::PrefillArgs a;
     a.qh = qh;
@@ -192,6 +204,7 @@ fa_status prefill_split(const float *q, const void *k, const void *v, float *out
     a.tile_map = tile_map;
     a.work_counter = reinterpret_cast<unsigned *>(ws + w.ctr_off);
     a.split = 1;
+    set_q_staging(&a, q, ws, w);
     if (e == cudaSuccess) e = record_start(s);
     if (e == cudaSuccess) e = fa::launch_prefill_tc(a, err, s);
     // near part
@@ -202,6 +215,7 @@ fa_status prefill_split(const float *q, const void *k, const void *v, float *out
     a.tile_map = nullptr;
     a.work_counter = ctr2;
     a.split = 2;
+    a.q = nullptr;  // the far part left every Q tile staged
     if (e == cudaSuccess) e = fa::launch_prefill_tc(a, err, s);
     if (e == cudaSuccess) e = record_stop(s);
     if (e == cudaSuccess)
@@ -431,7 +445,20 @@ fa_status fa_prefill_chunk(const float *q, const void *k, const void *v, float *
     __half *kh = reinterpret_cast<__half *>(ws + w.k_off);
     __half *vh = reinterpret_cast<__half *>(ws + w.v_off);
     unsigned *ctr = reinterpret_cast<unsigned *>(ws + w.ctr_off);
-    const size_t q_count = static_cast<size_t>(n) * n_q_heads * head_dim;
+    // Q rows of the query tiles the prefill kernel's first wave covers are
+    // staged here; the kernel converts the rest while it runs
+    const int units = ((n + fa::kPrefillBQ - 1) / fa::kPrefillBQ) * n_q_heads;
+    const int w0 = fa::prefill_units_staged_first(pos0, n, n_q_heads, sink, win);
+    const size_t row0 = static_cast<size_t>(units - w0) / n_q_heads * fa::kPrefillBQ;
+    const size_t row_vals = static_cast<size_t>(n_q_heads) * head_dim;
+    fa::QStageArgs qs;
+    qs.q = q + row0 * row_vals;
+    qs.qh = qh + row0 * row_vals;
+    qs.count = (static_cast<size_t>(n) - row0) * row_vals;
+    qs.work_counter = ctr;
+    qs.stage_counter = reinterpret_cast<unsigned *>(ws + w.qctr_off);
+    qs.flags = reinterpret_cast<unsigned *>(ws + w.flag_off);
+    qs.n_flags = units - w0;
     cudaError_t e = cudaSuccess;
     // An fp16 cache body is already the kernel's operand layout ([Hkv][rows]
     // [hd] binary16): the kernel's tensor maps read the planes in place.
@@ -439,14 +466,15 @@ fa_status fa_prefill_chunk(const float *q, const void *k, const void *v, float *
     if (direct) {
         kh = reinterpret_cast<__half *>(static_cast<uint8_t *>(const_cast<void *>(k)) + g.body_off);
         vh = reinterpret_cast<__half *>(static_cast<uint8_t *>(const_cast<void *>(v)) + g.body_off);
-        e = fa::launch_stage_q(q, qh, q_count, ctr, s);
+        e = fa::launch_stage_q(qs, s);
     } else {
-        // one launch stages Q (and zeroes the work counter), K and V; the
+        // one launch stages Q's first rows (and zeroes the counters and
+        // flags), K and V; the
         // split's far part reads sinks and Q4_0 rows (no ring), the other
         // paths what the shadow geometry gives every query
         const int sw_stage = split ? 0 : shadow_win;
         e = fa::launch_stage_kv(static_cast<const uint8_t *>(k), static_cast<const uint8_t *>(v),
-                                kh, vh, nk, g, shadow_sink, sw_stage, q, qh, q_count, ctr, s);
+                                kh, vh, nk, g, shadow_sink, sw_stage, &qs, s);
     }
     if (e != cudaSuccess) return FA_ERR_CUDA;
     if (split) return prefill_split(q, k, v, out, lse, pos0, n, n_q_heads, n_kv_heads, head_dim,
@@ -470,6 +498,7 @@ fa_status fa_prefill_chunk(const float *q, const void *k, const void *v, float *
     a.win = win;
     a.scale = 1.0f / sqrtf(static_cast<float>(head_dim));
     a.prefetch_kv = direct;
+    set_q_staging(&a, q, ws, w);
     e = record_start(s);
     if (e == cudaSuccess) e = fa::launch_prefill_tc(a, d->err, s);
     if (e == cudaSuccess) e = record_stop(s);

@@ -50,16 +50,24 @@ cudaError_t launch_kv_append(const float *k_new, const float *v_new, uint8_t *k_
                              unsigned *err, cudaStream_t stream);
 
 // ---- prefill_stage.cu: fp16 staging of Q and of the K/V rows a prefill reads
-// Converts q and zeroes *counter (the prefill kernel's work queue).
-cudaError_t launch_stage_q(const float *q, __half *qh, size_t count, unsigned *counter,
-                           cudaStream_t stream);
+// The part of Q converted before the prefill kernel (the query tiles of its
+// first wave of units; the kernel converts the rest itself) and the kernel's
+// counters and Q-ready flags, which the same launch zeroes.
+struct QStageArgs {
+    const float *q = nullptr;  // first element to convert (fp32)
+    __half *qh = nullptr;      // its fp16 destination
+    size_t count = 0;          // values to convert (a multiple of 4)
+    unsigned *work_counter = nullptr;  // the prefill's work queue
+    unsigned *stage_counter = nullptr; // the prefill's Q staging queue
+    unsigned *flags = nullptr;         // the prefill's Q-ready flags
+    int n_flags = 0;
+};
+cudaError_t launch_stage_q(const QStageArgs &qs, cudaStream_t stream);
 // Stages rows 0..n-1 of the K and the V plane into kdst and vdst in one launch;
-// when q is not null the same launch also does launch_stage_q's work (q_count
-// values of q into qh, *counter zeroed).
+// when qs is not null the same launch also does launch_stage_q's work.
 cudaError_t launch_stage_kv(const uint8_t *kplane, const uint8_t *vplane, __half *kdst,
                             __half *vdst, int n, const PlaneGeom &g, int shadow_sink,
-                            int shadow_win, const float *q, __half *qh, size_t q_count,
-                            unsigned *counter, cudaStream_t stream);
+                            int shadow_win, const QStageArgs *qs, cudaStream_t stream);
 
 // ---- prefill_tc.cu
 struct PrefillArgs {
@@ -81,10 +89,24 @@ struct PrefillArgs {
     // K/V are cache planes read in place (not staged just before): the kernel
     // asks for their rows in L2 at its start
     bool prefetch_kv = false;
+    // Q staged by the kernel itself: units w >= q_w0 (heaviest first) have
+    // their rows converted from q (fp32 [n][Hq][hd]) into qh by two warps of
+    // the kernel, which set q_flags[w - q_w0] once a tile is there
+    // (q null: all of Q was staged before the launch)
+    const float *q = nullptr;
+    unsigned *q_flags = nullptr;
+    unsigned *q_stage_counter = nullptr;
+    int q_w0 = 0;
 };
 constexpr int kPrefillBQ = 128;
 constexpr int kPrefillBK = 128;
 cudaError_t launch_prefill_tc(const PrefillArgs &a, unsigned *err, cudaStream_t stream);
+// Blocks of the prefill kernel for n query rows of Hq heads (one per SM, at
+// most one per unit), and the units whose Q must be staged before it: the
+// whole query tiles that its first wave of units covers (its first two waves
+// when those units are short).
+int prefill_grid(int n, int Hq);
+int prefill_units_staged_first(int pos0, int n, int Hq, int sink, int win);
 
 // 128-byte-swizzled tiled tensor map (rank 1..5, zero fill outside the
 // tensor); strides_bytes holds rank-1 entries. False if the driver refuses.

@@ -2,7 +2,9 @@
 //
 // The prefill kernel runs its two contractions on tcgen05 tensor cores with
 // fp16 operands, fed by TMA. These single-pass kernels produce those operands:
-//   * Q: fp32 [n][Hq][hd] -> fp16 [n][Hq][hd], round to nearest even;
+//   * Q: fp32 [n][Hq][hd] -> fp16 [n][Hq][hd], round to nearest even, for the
+//     query tiles of the prefill kernel's first wave of units (the kernel
+//     converts the other tiles itself, while it computes);
 //   * K and V: the cache rows 0..n-1 of every kv head (n = the key rows: pos0
 //     plus the chunk's queries) -> fp16 [Hkv][n][hd], the value each key has
 //     for every query of the prefill. For an fp32 cache
@@ -24,14 +26,29 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// Q fp32 -> fp16 over the blocks of one grid row; zeroes *counter. Four
-// independent coalesced loads per thread are in flight at a time.
-__device__ __forceinline__ void stage_q_rows(const float4 *__restrict__ q, uint2 *__restrict__ qh,
-                                             long long count4, unsigned *counter) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) *counter = 0u;
+// Q fp32 -> fp16 over the blocks of one grid row (the rows of the prefill's
+// first wave of units; its kernel converts the rest), and the prefill's
+// counters and Q-ready flags zeroed. Four independent coalesced loads per
+// thread are in flight at a time.
+struct QStage {
+    const float4 *q;
+    uint2 *qh;
+    long long count4;
+    unsigned *counter, *stage_counter, *flags;
+    int n_flags;
+};
+
+__device__ __forceinline__ void stage_q_rows(const QStage &qs) {
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
     long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
-    for (; i + 3 * stride < count4; i += 4 * stride) {
+    if (i == 0) {
+        *qs.counter = 0u;
+        if (qs.stage_counter) *qs.stage_counter = 0u;
+    }
+    for (long long f = i; f < qs.n_flags; f += stride) qs.flags[f] = 0u;
+    const float4 *__restrict__ q = qs.q;
+    uint2 *__restrict__ qh = qs.qh;
+    for (; i + 3 * stride < qs.count4; i += 4 * stride) {
         float4 x[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) x[u] = __ldg(q + i + u * stride);
@@ -39,25 +56,13 @@ __device__ __forceinline__ void stage_q_rows(const float4 *__restrict__ q, uint2
         for (int u = 0; u < 4; ++u)
             qh[i + u * stride] = make_uint2(pack_half2(x[u].x, x[u].y), pack_half2(x[u].z, x[u].w));
     }
-    for (; i < count4; i += stride) {
+    for (; i < qs.count4; i += stride) {
         const float4 x = __ldg(q + i);
         qh[i] = make_uint2(pack_half2(x.x, x.y), pack_half2(x.z, x.w));
     }
 }
 
-__global__ void __launch_bounds__(kThreads)
-    stage_q_kernel(const float4 *__restrict__ q, uint2 *__restrict__ qh, long long count4,
-                   unsigned *counter) {
-    stage_q_rows(q, qh, count4, counter);
-}
-
-// Q staged in the same launch as K and V (when q is not null).
-struct QStage {
-    const float4 *q;
-    uint2 *qh;
-    long long count4;
-    unsigned *counter;
-};
+__global__ void __launch_bounds__(kThreads) stage_q_kernel(QStage qs) { stage_q_rows(qs); }
 
 // The K and V planes are staged by one launch: blockIdx.y picks the plane.
 // When Q comes along it takes grid row 0 and K, V rows 1 and 2, so that the
@@ -71,7 +76,7 @@ __global__ void __launch_bounds__(kThreads)
                         int hd, int max_seq, size_t body_off, QStage qs) {
     const int prow = static_cast<int>(blockIdx.y) - (qs.q ? 1 : 0);
     if (prow < 0) {
-        stage_q_rows(qs.q, qs.qh, qs.count4, qs.counter);
+        stage_q_rows(qs);
         return;
     }
     const uint8_t *__restrict__ plane = prow ? vplane : kplane;
@@ -109,7 +114,7 @@ __global__ void __launch_bounds__(kThreads)
                         int hd, int max_seq, size_t body_off, size_t scale_off, QStage qs) {
     const int prow = static_cast<int>(blockIdx.y) - (qs.q ? 1 : 0);
     if (prow < 0) {
-        stage_q_rows(qs.q, qs.qh, qs.count4, qs.counter);
+        stage_q_rows(qs);
         return;
     }
     const uint8_t *__restrict__ plane = prow ? vplane : kplane;
@@ -138,7 +143,7 @@ __global__ void __launch_bounds__(kThreads)
                        size_t ring_off, int shadow_sink, int shadow_win, QStage qs) {
     const int prow = static_cast<int>(blockIdx.y) - (qs.q ? 1 : 0);
     if (prow < 0) {
-        stage_q_rows(qs.q, qs.qh, qs.count4, qs.counter);
+        stage_q_rows(qs);
         return;
     }
     const uint8_t *__restrict__ plane = prow ? vplane : kplane;
@@ -198,26 +203,29 @@ int grid_for(long long items) {
     return static_cast<int>(blocks);
 }
 
+QStage to_stage(const QStageArgs *a) {
+    if (!a) return QStage{nullptr, nullptr, 0, nullptr, nullptr, nullptr, 0};
+    return QStage{reinterpret_cast<const float4 *>(a->q), reinterpret_cast<uint2 *>(a->qh),
+                  static_cast<long long>(a->count / 4), a->work_counter, a->stage_counter,
+                  a->flags, a->n_flags};
+}
+
 }  // namespace
 
-cudaError_t launch_stage_q(const float *q, __half *qh, size_t count, unsigned *counter,
-                           cudaStream_t stream) {
-    const long long c4 = static_cast<long long>(count / 4);
-    stage_q_kernel<<<grid_for(c4), kThreads, 0, stream>>>(reinterpret_cast<const float4 *>(q),
-                                                           reinterpret_cast<uint2 *>(qh), c4,
-                                                           counter);
+cudaError_t launch_stage_q(const QStageArgs &a, cudaStream_t stream) {
+    const QStage qs = to_stage(&a);
+    const long long items = qs.count4 > qs.n_flags ? qs.count4 : qs.n_flags;
+    stage_q_kernel<<<grid_for(items), kThreads, 0, stream>>>(qs);
     return cudaGetLastError();
 }
 
 cudaError_t launch_stage_kv(const uint8_t *kplane, const uint8_t *vplane, __half *kdst,
                             __half *vdst, int n, const PlaneGeom &g, int shadow_sink,
-                            int shadow_win, const float *q, __half *qh, size_t q_count,
-                            unsigned *counter, cudaStream_t stream) {
-    const QStage qs{reinterpret_cast<const float4 *>(q), reinterpret_cast<uint2 *>(qh),
-                    static_cast<long long>(q_count / 4), counter};
-    const unsigned rows = q ? 3u : 2u;
+                            int shadow_win, const QStageArgs *qa, cudaStream_t stream) {
+    const QStage qs = to_stage(qa);
+    const unsigned rows = qa ? 3u : 2u;
     auto grid = [&](long long items) {
-        return dim3(grid_for(q && qs.count4 > items ? qs.count4 : items), rows);
+        return dim3(grid_for(qa && qs.count4 > items ? qs.count4 : items), rows);
     };
     if (g.fmt == kFmtF32) {
         const long long items = static_cast<long long>(g.n_kv) * n * (g.hd / 4);

@@ -15,6 +15,9 @@
 //               TMEM accumulator (tcgen05.mma, fp16 x fp16 -> fp32), then
 //               O += P_{i-1} V_{i-1} with P read from TMEM (A operand in TMEM)
 //               and V from shared memory (MN-major B).
+//   warps 2-3   Q staging (large prefills): the query tiles past the first
+//               wave of units are converted from fp32 to fp16 here, ahead of
+//               the units that need them, while the tensor cores run.
 //   warps 4-7   softmax, one thread per query row (TMEM lane): tcgen05.ld of
 //               S, masking, running max in the exp2 domain (scale * log2 e
 //               folded into one FMA), P packed to fp16 and tcgen05.st back over
@@ -63,6 +66,58 @@ struct Cfg {
 
 constexpr int kUnitRing = 4;
 
+// ------------------------------------------------- flags in global memory
+// A producer block publishes data for other blocks: every writing thread
+// fences its stores (GPU scope, and towards the async proxy, for TMA readers),
+// the writers synchronise, one thread release-stores the flag. A reader
+// acquire-loads the flag and fences towards the async proxy before it issues
+// TMA copies of the data.
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// After a relaxed load saw a flag set: makes that load an acquire.
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_release_gpu(unsigned *p, unsigned v) {
+    asm volatile("st.release.gpu.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Order this thread's generic-proxy global accesses with its async-proxy ones.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Wait until *flag is non-zero: bounded like mbar_wait (timeout recorded, the
+// block's abort flag raised, false returned), and false as soon as *abort is.
+__device__ __forceinline__ bool flag_wait(const unsigned *flag, volatile int *abort,
+                                          unsigned *err) {
+    if (ld_acquire_gpu(flag)) return true;
+    const long long t0 = clock64();
+    for (;;) {
+        __nanosleep(256);
+        if (ld_acquire_gpu(flag)) return true;
+        if (*abort) return false;
+        if (clock64() - t0 > kSpinCycles) {
+            *abort = 1;
+            flag_error(err, FA_ERRBIT_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+
 struct Bars {
     uint64_t q_full, q_empty;
     uint64_t o_free;
@@ -87,7 +142,7 @@ struct TilePlan {
     __device__ int kt(int i) const { return i < ns ? i : lo + (i - ns); }
 };
 
-__device__ __forceinline__ TilePlan tile_plan(int p0, int p1, int sink, int win, int bk) {
+__host__ __device__ __forceinline__ TilePlan tile_plan(int p0, int p1, int sink, int win, int bk) {
     TilePlan t;
     const int hi = p1 / bk;
     if (win <= 0) {
@@ -157,7 +212,9 @@ __global__ void __launch_bounds__(256, 1)
                       unsigned *__restrict__ work_counter, float *__restrict__ lse, int pos0,
                       int n, int Hq, int Hkv, int sink, int win, float sl2, unsigned *err,
                       int split_f, int split_w, const uint8_t *pf_k, const uint8_t *pf_v,
-                      unsigned long long pf_head_stride, unsigned pf_head_bytes) {
+                      unsigned long long pf_head_stride, unsigned pf_head_bytes,
+                      const float *__restrict__ q32, __half *__restrict__ qh,
+                      unsigned *q_flags, unsigned *q_stage_ctr, int q_w0) {
     using C = Cfg<HD>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -244,73 +301,102 @@ __global__ void __launch_bounds__(256, 1)
                 }
             }
             int k_arms[2] = {0, 0}, v_arms[2] = {0, 0}, q_arms = 0;
-            int t = 0;  // global tile index of this block
             bool ok = true;
-            Unit u;
-            for (int j = 0; ok; ++j) {
-                // take the next unit and publish it to the other warps
-                const int w = (j == 0) ? static_cast<int>(blockIdx.x)
-                                       : G + static_cast<int>(atomicAdd(work_counter, 1u));
+            // hand unit id w to the MMA and softmax warps through ring slot j
+            auto publish = [&](int j, int w) -> bool {
                 const int slot = j % kUnitRing;
                 if (j >= kUnitRing &&
-                    !mbar_wait(&bars->unit_empty[slot], ((j / kUnitRing) - 1) & 1, abort, err)) {
-                    ok = false;
-                    break;
-                }
+                    !mbar_wait(&bars->unit_empty[slot], ((j / kUnitRing) - 1) & 1, abort, err))
+                    return false;
                 bars->unit_id[slot] = w;
                 mbar_arrive(&bars->unit_full[slot]);
-                if (!to_unit(w, &u)) break;
-                // query rows q0.. of the chunk, at positions p0 .. p1
-                const int q0 = u.qt * C::BQ;
-                const int p0 = pos0 + q0, p1 = pos0 + min(n, q0 + C::BQ) - 1;
-                const int g = u.h / (Hq / Hkv);
-                const TilePlan plan = unit_plan<SPLIT>(p0, p1, sink, win, split_w, C::BK);
-                // the Q buffer is free once the previous unit's last QK^T completed
-                if (j > 0 && !mbar_wait(&bars->q_empty, (j - 1) & 1, abort, err)) {
-                    ok = false;
-                    break;
+                return true;
+            };
+            // key tile kt of kv head g into stage tt % NS (tt: this block's tile count)
+            auto load = [&](int tt, int kt, int g, int qt, bool is_k) -> bool {
+                const int st = tt % C::NS;
+                uint64_t *empty = is_k ? &bars->k_empty[st] : &bars->v_empty[st];
+                uint64_t *full = is_k ? &bars->k_full[st] : &bars->v_full[st];
+                if (tt >= C::NS && !mbar_wait(empty, ((tt / C::NS) - 1) & 1, abort, err))
+                    return false;
+                mbar_arrive_expect_tx(full, C::TILE_BYTES);
+                const uint32_t base = (is_k ? C::OFF_K : C::OFF_V) + st * C::TILE_BYTES;
+                for (int c = 0; c < C::NCHUNK; ++c)
+                    tma_load_3d(smem + base + c * C::CHUNK_BYTES, is_k ? &tm_k : &tm_v, full,
+                                c * 64, kt * C::BK, g);
+                if (is_k) {
+                    ++k_arms[st];
+                    if (tile_map) tile_map[static_cast<size_t>(qt) * nkt + kt] = 1;
+                } else {
+                    ++v_arms[st];
+                }
+                return true;
+            };
+            // Q tile of the j-th unit w, once the buffer is free (the previous
+            // unit's last QK^T completed) and, for a unit staged by this
+            // kernel, once its rows are in fp16
+            auto load_q = [&](int j, int w, const Unit &u, unsigned peek) -> bool {
+                if (j > 0 && !mbar_wait(&bars->q_empty, (j - 1) & 1, abort, err)) return false;
+                if (w >= q_w0) {
+                    if (peek)
+                        fence_acq_rel_gpu();
+                    else if (!flag_wait(q_flags + (w - q_w0), abort, err))
+                        return false;
+                    fence_proxy_async_global();
                 }
 #ifdef FA_TEST_SKIP_FIRST_Q
                 // Test-only build: the first Q tile is never armed or loaded, so
                 // the MMA warp's bounded wait on it runs out and the launch must
                 // report FA_ERR_TIMEOUT and leave the context usable.
-                if (j > 0)
+                if (j == 0) return true;
 #endif
-                {
-                    mbar_arrive_expect_tx(&bars->q_full, C::TILE_BYTES);
-                    for (int c = 0; c < C::NCHUNK; ++c)
-                        tma_load_3d(smem + C::OFF_Q + c * C::CHUNK_BYTES, &tm_q, &bars->q_full,
-                                    c * 64, u.h, q0);
-                    ++q_arms;
+                mbar_arrive_expect_tx(&bars->q_full, C::TILE_BYTES);
+                for (int c = 0; c < C::NCHUNK; ++c)
+                    tma_load_3d(smem + C::OFF_Q + c * C::CHUNK_BYTES, &tm_q, &bars->q_full,
+                                c * 64, u.h, u.qt * C::BQ);
+                ++q_arms;
+                return true;
+            };
+            auto plan_of = [&](const Unit &u) {
+                const int q0 = u.qt * C::BQ;
+                return unit_plan<SPLIT>(pos0 + q0, pos0 + min(n, q0 + C::BQ) - 1, sink, win,
+                                        split_w, C::BK);
+            };
+            const int group = Hq / Hkv;
+            int t = 0;  // tiles of this block before the current unit
+            // block b starts with unit b; later units come from the global counter
+            int w = static_cast<int>(blockIdx.x);
+            Unit u;
+            ok = publish(0, w);
+            bool have = ok && to_unit(w, &u);
+            if (have) ok = load_q(0, w, u, 0u);
+            for (int j = 0; have && ok; ++j) {
+                const int g = u.h / group;
+                const TilePlan plan = plan_of(u);
+                const int cnt = plan.count;
+                // consumption order of the MMA warp: K0, K1, V0, K2, V1, ...,
+                // V(cnt-1). The next unit is taken with the last K tile, so that
+                // the counter's round trip overlaps the waits for the V stages.
+                int w_next = -1;
+                unsigned peek = 0;
+                for (int i = 0; i < cnt && ok; ++i) {
+                    ok = load(t + i, plan.kt(i), g, u.qt, true);
+                    if (ok && i == cnt - 1)
+                        w_next = G + static_cast<int>(atomicAdd(work_counter, 1u));
+                    if (ok && i >= 1) ok = load(t + i - 1, plan.kt(i - 1), g, u.qt, false);
                 }
-                auto load = [&](int i, bool is_k) -> bool {
-                    const int tt = t + i;
-                    const int st = tt % C::NS;
-                    uint64_t *empty = is_k ? &bars->k_empty[st] : &bars->v_empty[st];
-                    uint64_t *full = is_k ? &bars->k_full[st] : &bars->v_full[st];
-                    if (tt >= C::NS && !mbar_wait(empty, ((tt / C::NS) - 1) & 1, abort, err))
-                        return false;
-                    const int kt = plan.kt(i);
-                    mbar_arrive_expect_tx(full, C::TILE_BYTES);
-                    const uint32_t base = (is_k ? C::OFF_K : C::OFF_V) + st * C::TILE_BYTES;
-                    for (int c = 0; c < C::NCHUNK; ++c)
-                        tma_load_3d(smem + base + c * C::CHUNK_BYTES, is_k ? &tm_k : &tm_v, full,
-                                    c * 64, kt * C::BK, g);
-                    if (is_k) {
-                        ++k_arms[st];
-                        if (tile_map) tile_map[static_cast<size_t>(u.qt) * nkt + kt] = 1;
-                    } else {
-                        ++v_arms[st];
-                    }
-                    return true;
-                };
-                // consumption order of the MMA warp: K0, K1, V0, K2, V1, ..., V(n-1)
-                for (int i = 0; i < plan.count && ok; ++i) {
-                    ok = load(i, true);
-                    if (ok && i >= 1) ok = load(i - 1, false);
-                }
-                if (ok) ok = load(plan.count - 1, false);
-                t += plan.count;
+                // a first look at the next unit's Q flag, read after the last V
+                // tile is issued
+                if (ok && w_next >= q_w0 && w_next < n_units)
+                    peek = ld_relaxed_gpu(q_flags + (w_next - q_w0));
+                if (ok) ok = load(t + cnt - 1, plan.kt(cnt - 1), g, u.qt, false);
+                t += cnt;
+                if (!ok) break;
+                Unit un;
+                ok = publish(j + 1, w_next);
+                have = ok && to_unit(w_next, &un);
+                if (have) ok = load_q(j + 1, w_next, un, peek);
+                u = un;
             }
             if (!ok) {  // let every copy already issued land before exit
                 if (q_arms) drain_wait(&bars->q_full, (q_arms - 1) & 1);
@@ -397,7 +483,52 @@ __global__ void __launch_bounds__(256, 1)
             tc_commit(&bars->drain);
             drain_wait(&bars->drain, 0);
         }
-    } else if (warp >= 4) {
+    } else if (warp < 4) {
+        // ------------------------------------------------------ Q staging
+        // Warps 2 and 3 each take units w >= q_w0 in order from a global
+        // counter and convert the unit's Q rows (fp32 [n][Hq][hd]) to the fp16
+        // rows the tensor map reads, then set the unit's flag. They wait on
+        // nothing, so every claimed unit is finished by a running block, and
+        // the producer warps of all blocks (this one included) only wait for
+        // units some block has claimed or will claim.
+        if (q32) {
+            constexpr int V4 = HD / 4;  // float4 per row
+            constexpr int kInFlight = 16;  // 24 or more made the kernel spill
+            const size_t rstride = static_cast<size_t>(Hq) * V4;
+            for (;;) {
+                unsigned claim = 0;  // past the last unit once the block aborted
+                if (lane == 0) claim = *abort ? static_cast<unsigned>(n_units) : atomicAdd(q_stage_ctr, 1u);
+                claim = __shfl_sync(0xffffffffu, claim, 0);
+                if (claim >= static_cast<unsigned>(n_units - q_w0)) break;
+                const int w = q_w0 + static_cast<int>(claim);
+                const int q0 = (nqt - 1 - w / Hq) * C::BQ;
+                const int total = min(C::BQ, n - q0) * V4;
+                const size_t base = (static_cast<size_t>(q0) * Hq + w % Hq) * V4;
+                const float4 *src = reinterpret_cast<const float4 *>(q32) + base;
+                uint2 *dst = reinterpret_cast<uint2 *>(qh) + base;
+                for (int i0 = 0; i0 < total; i0 += 32 * kInFlight) {
+                    float4 x[kInFlight];
+#pragma unroll
+                    for (int k = 0; k < kInFlight; ++k) {
+                        const int i = i0 + 32 * k + lane;
+                        if (i < total) x[k] = __ldcs(src + (i / V4) * rstride + i % V4);
+                    }
+#pragma unroll
+                    for (int k = 0; k < kInFlight; ++k) {
+                        const int i = i0 + 32 * k + lane;
+                        if (i < total)
+                            __stcs(dst + (i / V4) * rstride + i % V4,
+                                   make_uint2(pack_half2(x[k].x, x[k].y),
+                                              pack_half2(x[k].z, x[k].w)));
+                    }
+                }
+                __threadfence();
+                fence_proxy_async_global();
+                __syncwarp();
+                if (lane == 0) st_release_gpu(q_flags + (w - q_w0), 1u);
+            }
+        }
+    } else {
         // ----------------------------------------------- softmax and epilogue
         const int r = threadIdx.x - 128;  // tile row == TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -651,22 +782,45 @@ cudaError_t launch_hd(const PrefillArgs &a, unsigned *err, cudaStream_t stream) 
     cudaError_t e =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    const int nqt = (a.n + C::BQ - 1) / C::BQ;
-    const int units = nqt * a.n_q_heads;
-    const int grid = units < device_sm_count() ? units : device_sm_count();
+    const int units = ((a.n + C::BQ - 1) / C::BQ) * a.n_q_heads;
+    const int grid = prefill_grid(a.n, a.n_q_heads);
+    if (a.q && a.q_w0 < prefill_units_staged_first(a.pos0, a.n, a.n_q_heads, a.sink, a.win))
+        return cudaErrorInvalidValue;  // a first-wave unit's Q would never be staged
     const float sl2 = a.scale * 1.4426950408889634f;
     // 32-bit byte counts per kv head (up to 8M rows at head_dim 256)
     const bool prefetch = a.prefetch_kv && L * HD * 2 < (1ull << 31);
+    // units from q_w0 on have their Q converted by the kernel (all of them
+    // staged before: q_w0 = units)
+    const bool own_q = a.q && a.q_w0 < units;
     kernel<<<grid, 256, C::SMEM, stream>>>(
         tq, tk, tv, to, a.tile_map, a.work_counter, a.lse, a.pos0, a.n, a.n_q_heads,
         a.n_kv_heads, a.sink, a.win, sl2, err, a.split_f, a.split_w,
         prefetch ? reinterpret_cast<const uint8_t *>(a.kh) : nullptr,
         reinterpret_cast<const uint8_t *>(a.vh), static_cast<unsigned long long>(head_stride),
-        static_cast<unsigned>(L * HD * 2));
+        static_cast<unsigned>(L * HD * 2), own_q ? a.q : nullptr, const_cast<__half *>(a.qh),
+        a.q_flags, a.q_stage_counter, own_q ? a.q_w0 : units);
     return cudaGetLastError();
 }
 
 }  // namespace
+
+int prefill_grid(int n, int Hq) {
+    const int units = ((n + kPrefillBQ - 1) / kPrefillBQ) * Hq;
+    return units < device_sm_count() ? units : device_sm_count();
+}
+
+int prefill_units_staged_first(int pos0, int n, int Hq, int sink, int win) {
+    const int nqt = (n + kPrefillBQ - 1) / kPrefillBQ;
+    // The staging warps convert one unit's rows in ~16 tile times of the
+    // tensor cores (at any head_dim: both scale with it) and the blocks a wave
+    // of units. When the first units are shorter than that (windows), two
+    // waves are staged before the launch so that the warps start ahead.
+    const TilePlan heavy =
+        tile_plan(pos0 + (nqt - 1) * kPrefillBQ, pos0 + n - 1, sink, win, kPrefillBK);
+    const int waves = heavy.count < 24 ? 2 : 1;
+    const int w0 = (waves * prefill_grid(n, Hq) + Hq - 1) / Hq * Hq;
+    return w0 < nqt * Hq ? w0 : nqt * Hq;
+}
 
 cudaError_t launch_prefill_tc(const PrefillArgs &a, unsigned *err, cudaStream_t stream) {
     switch (a.head_dim) {

@@ -166,7 +166,8 @@ fa_status fa_kv_append(const float *k_new, const float *v_new, void *k_planes, v
 
 /* ------------------------------------------------------------------ prefill */
 
-/* Workspace bytes fa_prefill needs (fp16 staging of K and V) for every cache
+/* Workspace bytes fa_prefill needs (its work queues, one Q-ready flag per
+ * (query tile, q head), the fp16 staging of Q, K and V) for every cache
  * but a Q4_0 one whose shadow window is neither 0 nor FA_Q4_RING_ROWS; that
  * case needs fa_prefill_chunk_workspace_bytes_for(). */
 size_t fa_prefill_workspace_bytes(int n, int n_q_heads, int n_kv_heads, int head_dim);
@@ -200,7 +201,8 @@ fa_status fa_prefill_tile_shape(int head_dim, int *bq, int *bk);
  *              fa_prefill_chunk_workspace_bytes_for for the workspace).
  *   max_seq    row capacity of the planes (n <= max_seq).
  *   workspace  >= fa_prefill_workspace_bytes() bytes of device memory; its
- *              contents are scratch and need no initialisation.
+ *              contents are scratch and need no initialisation. Calls that
+ *              share a workspace must not overlap on the GPU.
  *   tile_map   NULL, or [ceil(n/bq)][ceil(n/bk)] bytes (device) the kernel sets
  *              to 1 for every (query tile, key tile) it visits. Bytes of
  *              tiles it skips are left untouched (clear them first).
