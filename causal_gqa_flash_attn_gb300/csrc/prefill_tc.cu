@@ -492,32 +492,41 @@ __global__ void __launch_bounds__(256, 1)
         // the producer warps of all blocks (this one included) only wait for
         // units some block has claimed or will claim.
         if (q32) {
-            constexpr int V4 = HD / 4;  // float4 per row
-            constexpr int kInFlight = 16;  // 24 or more made the kernel spill
-            const size_t rstride = static_cast<size_t>(Hq) * V4;
+            constexpr int V4 = HD / 4;         // float4 per row
+            constexpr int kInFlight = 16;      // 24 or more made the kernel spill
+            constexpr int LPR = V4 < 32 ? V4 : 32;  // lanes on one row in a warp-wide load
+            constexpr int RPS = 32 / LPR;      // rows one warp-wide load covers
+            constexpr int SPR = V4 / LPR;      // warp-wide loads per row
+            constexpr int RPB = kInFlight / SPR * RPS;  // rows per batch of loads
+            static_assert(kInFlight % SPR == 0, "whole rows per batch");
+            const uint32_t rs = static_cast<uint32_t>(Hq) * V4;  // float4 from row to row
+            const int lane_row = lane / LPR;
+            const uint32_t lane_off = static_cast<uint32_t>(lane_row) * rs + lane % LPR;
             for (;;) {
                 unsigned claim = 0;  // past the last unit once the block aborted
-                if (lane == 0) claim = *abort ? static_cast<unsigned>(n_units) : atomicAdd(q_stage_ctr, 1u);
+                if (lane == 0)
+                    claim = *abort ? static_cast<unsigned>(n_units) : atomicAdd(q_stage_ctr, 1u);
                 claim = __shfl_sync(0xffffffffu, claim, 0);
                 if (claim >= static_cast<unsigned>(n_units - q_w0)) break;
                 const int w = q_w0 + static_cast<int>(claim);
                 const int q0 = (nqt - 1 - w / Hq) * C::BQ;
-                const int total = min(C::BQ, n - q0) * V4;
-                const size_t base = (static_cast<size_t>(q0) * Hq + w % Hq) * V4;
-                const float4 *src = reinterpret_cast<const float4 *>(q32) + base;
-                uint2 *dst = reinterpret_cast<uint2 *>(qh) + base;
-                for (int i0 = 0; i0 < total; i0 += 32 * kInFlight) {
+                const int rows = min(C::BQ, n - q0);
+                const size_t base = (static_cast<size_t>(q0) * Hq + w % Hq) * V4 + lane_off;
+                for (int r0 = 0; r0 < rows; r0 += RPB) {
+                    const size_t at = base + static_cast<size_t>(r0) * rs;
+                    const float4 *src = reinterpret_cast<const float4 *>(q32) + at;
+                    uint2 *dst = reinterpret_cast<uint2 *>(qh) + at;
                     float4 x[kInFlight];
 #pragma unroll
                     for (int k = 0; k < kInFlight; ++k) {
-                        const int i = i0 + 32 * k + lane;
-                        if (i < total) x[k] = __ldcs(src + (i / V4) * rstride + i % V4);
+                        const int rr = k / SPR * RPS;  // this load's row in the batch
+                        if (r0 + rr + lane_row < rows) x[k] = __ldcs(src + rr * rs + (k % SPR) * 32);
                     }
 #pragma unroll
                     for (int k = 0; k < kInFlight; ++k) {
-                        const int i = i0 + 32 * k + lane;
-                        if (i < total)
-                            __stcs(dst + (i / V4) * rstride + i % V4,
+                        const int rr = k / SPR * RPS;
+                        if (r0 + rr + lane_row < rows)
+                            __stcs(dst + rr * rs + (k % SPR) * 32,
                                    make_uint2(pack_half2(x[k].x, x[k].y),
                                               pack_half2(x[k].z, x[k].w)));
                     }
