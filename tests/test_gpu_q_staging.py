@@ -104,3 +104,41 @@ def test_prefill_repeat_same_workspace(oracle_mod):
     for q, out in zip((q1, q2), outs):
         assert_close(out.cpu().numpy(), oracle_mod.prefill(q, k, v, kv_fmt="f32", sink=0, win=0),
                      "repeat")
+
+
+def test_prefill_graph_replay_kernel_stages_q(oracle_mod):
+    """A prefill captured once in a CUDA graph and replayed with new queries:
+    each replay's staging launch clears the counters and flags again, so the
+    kernel waits for this replay's Q tiles, not the last one's."""
+    import torch
+
+    from gpu_util import build_cache, fmt_code
+
+    m = fa()
+    n, hq, hkv, hd = 3200, 16, 2, 64
+    assert _staged_in_kernel(oracle_mod, n, hq, 0, 0) > 0
+    _, k, v = prefill_inputs(n, hq, hkv, hd, seed=SEED + 4)
+    qs = [prefill_inputs(n, hq, hkv, hd, seed=SEED + 5 + i)[0] for i in range(3)]
+    kp, vp, max_seq = build_cache(k, v, kv_fmt="f32")
+    ws = torch.empty(m.prefill_workspace_bytes(n, hq, hkv, hd), dtype=torch.uint8, device="cuda")
+    q_s = torch.zeros(n, hq, hd, dtype=torch.float32, device="cuda")
+    out = torch.zeros(n, hq, hd, dtype=torch.float32, device="cuda")
+
+    def step():
+        m.prefill(q_s, kp, vp, out, n, hq, hkv, hd, 0, 0, fmt_code("f32"), max_seq=max_seq,
+                  workspace=ws)
+
+    step()  # one-time set-up inside the library, outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for i, q in enumerate(qs):
+        q_s.copy_(torch.from_numpy(q))
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        st = m.get_device_error()
+        assert st == m.OK, m.status_string(st)
+        want = oracle_mod.prefill(q, k, v, kv_fmt="f32", sink=0, win=0)
+        assert_close(out.cpu().numpy(), want, f"replay {i}")
