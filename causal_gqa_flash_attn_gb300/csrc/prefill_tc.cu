@@ -499,9 +499,9 @@ __global__ void __launch_bounds__(256, 1)
             constexpr int SPR = V4 / LPR;      // warp-wide loads per row
             constexpr int RPB = kInFlight / SPR * RPS;  // rows per batch of loads
             static_assert(kInFlight % SPR == 0, "whole rows per batch");
-            const uint32_t rs = static_cast<uint32_t>(Hq) * V4;  // float4 from row to row
+            const size_t rs = static_cast<size_t>(Hq) * V4;  // float4 from row to row
             const int lane_row = lane / LPR;
-            const uint32_t lane_off = static_cast<uint32_t>(lane_row) * rs + lane % LPR;
+            const size_t lane_off = static_cast<size_t>(lane_row) * rs + lane % LPR;
             for (;;) {
                 unsigned claim = 0;  // past the last unit once the block aborted
                 if (lane == 0)
@@ -520,13 +520,14 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
                     for (int k = 0; k < kInFlight; ++k) {
                         const int rr = k / SPR * RPS;  // this load's row in the batch
-                        if (r0 + rr + lane_row < rows) x[k] = __ldcs(src + rr * rs + (k % SPR) * 32);
+                        if (r0 + rr + lane_row < rows)
+                            x[k] = __ldcs(src + static_cast<size_t>(rr) * rs + (k % SPR) * 32);
                     }
 #pragma unroll
                     for (int k = 0; k < kInFlight; ++k) {
                         const int rr = k / SPR * RPS;
                         if (r0 + rr + lane_row < rows)
-                            __stcs(dst + rr * rs + (k % SPR) * 32,
+                            __stcs(dst + static_cast<size_t>(rr) * rs + (k % SPR) * 32,
                                    make_uint2(pack_half2(x[k].x, x[k].y),
                                               pack_half2(x[k].z, x[k].w)));
                     }
