@@ -61,6 +61,21 @@ def test_plane_sizes(fa):
 def test_workspace_sizes(fa):
     n, hq, hkv, hd = 8192, 16, 2, 256
     assert fa.prefill_workspace_bytes(n, hq, hkv, hd) >= 2 * (n * hq * hd + 2 * hkv * n * hd)
+
+    def up256(x):
+        return (x + 255) // 256 * 256
+
+    # the layout fa.h documents: 256-byte header (work queues), one 4-byte Q-ready
+    # flag per (query tile, q head), then fp16 Q [n][Hq][hd], K and V [Hkv][rows][hd]
+    for n, hq, hkv, hd in ((8192, 16, 2, 256), (1500, 32, 4, 128), (1, 8, 1, 64)):
+        units = -(-n // 128) * hq
+        want = 256 + up256(4 * units) + up256(2 * n * hq * hd) + 2 * up256(2 * hkv * n * hd)
+        assert fa.prefill_workspace_bytes(n, hq, hkv, hd) == want, (n, hq, hkv, hd)
+    pos0, n = 700, 1400
+    units = -(-n // 128) * 32
+    want = (256 + up256(4 * units) + up256(2 * n * 32 * 128)
+            + 2 * up256(2 * 4 * (pos0 + n) * 128))
+    assert fa.prefill_chunk_workspace_bytes(pos0, n, 32, 4, 128) == want
     d = fa.decode_workspace_bytes(32, 16, 256, 128)
     assert d >= 256 + 32 * 16 * 128 * (2 + 256) * 4
     assert fa.decode_workspace_bytes(0, 16, 256, 128) == 0
