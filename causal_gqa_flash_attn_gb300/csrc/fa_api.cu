@@ -469,9 +469,8 @@ fa_status fa_prefill_chunk(const float *q, const void *k, const void *v, float *
         e = fa::launch_stage_q(qs, s);
     } else {
         // one launch stages Q's first rows (and zeroes the counters and
-        // flags), K and V; the
-        // split's far part reads sinks and Q4_0 rows (no ring), the other
-        // paths what the shadow geometry gives every query
+        // flags), K and V; the split's far part reads sinks and Q4_0 rows
+        // (no ring), the other paths what the shadow geometry gives every query
         const int sw_stage = split ? 0 : shadow_win;
         e = fa::launch_stage_kv(static_cast<const uint8_t *>(k), static_cast<const uint8_t *>(v),
                                 kh, vh, nk, g, shadow_sink, sw_stage, &qs, s);
